@@ -1,0 +1,56 @@
+"""The oracle's pins must catch plausible slips.
+
+Each case copies the oracle to a temporary directory, plants one mistake in the
+copy's C source (never in the committed oracle), rebuilds it and runs the pin
+suite against the copy, which must fail.  This runs on the CPU only.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    # the decay also multiplying the new write beta v k^T
+    "decay_on_write": ("decay * (s - bt * Sk[j] * k[i]) + bt * vt[j] * k[i]",
+                       "decay * (s - bt * Sk[j] * k[i] + bt * vt[j] * k[i])"),
+    # S^T k in place of S k
+    "transposed_state": ("acc += S[j * d_k + i] * k[i];\n      Sk[j]",
+                         "acc += S[(i % d_v) * d_k + (j % d_k)] * k[i];\n      Sk[j]"),
+    # conv taps applied newest-first
+    "reversed_taps": ("(double)conv_weight[c * conv_w + w]",
+                      "(double)conv_weight[c * conv_w + (conv_w - 1 - w)]"),
+    # tiled instead of repeat-interleaved key heads
+    "tiled_key_heads": ("const int64_t hk = h / (h_v / h_k);", "const int64_t hk = h % h_k;"),
+    # query not scaled by 1/sqrt(d_k)
+    "no_query_scale": ("1.0 / sqrt((double)d_k), qhat", "1.0, qhat"),
+    # initial window read newest-first
+    "window_order": ("window0[((conv_w - 1) + tau) * conv_dim + c]",
+                     "window0[(-tau - 1) * conv_dim + c]"),
+    # softplus with the wrong sign inside
+    "softplus_sign": ("log1p(exp(-fabs(z)))", "log1p(exp(fabs(z)))"),
+    # output read without the current token's write
+    "output_before_write": (
+        "for (int64_t i = 0; i < d_k; ++i) acc += S[j * d_k + i] * q[i];",
+        "for (int64_t i = 0; i < d_k; ++i) acc += (S[j * d_k + i] - bt * vt[j] * k[i]) * q[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    before, after = MUTATIONS[name]
+    src = open(os.path.join(ROOT, "oracle", "gdn_oracle.c")).read()
+    assert before in src, "mutation site moved; update the mutation table"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "gdn_oracle.c").write_text(src.replace(before, after, 1))
+    shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__", "golden"))
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-q",
+                        "-x", "-p", "no:cacheprovider"], cwd=tmp_path,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 1, f"pins did not catch '{name}':\n{r.stdout[-2000:]}"
