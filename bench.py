@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the Gated DeltaNet layer library on GB300.
+
+One step = one gdn_prefill call over the Qwen3.5-4B-shaped layer workload
+(B=1, T=4096, H_k=16 -> H_v=32, d_k=d_v=128, conv over 8192 channels, bf16
+I/O, fp32 state, chunk 64, zero initial state), inputs resident in HBM, L2
+flushed (a 256 MiB write) before every timed step.  The same JSON line also
+carries the decode step (24 layers x 64 slots, one bf16 token per slot,
+shuffled slots, random fp32 states) as a second measured quantity, the
+end-to-end figure through the C ABI with host buffers, the roofline of the
+dominant kernel and the float64 CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+With N > 1 it is launched by torch.distributed.run, one rank per GPU; every
+rank runs its own replica of the workload (the layer has no cross-GPU
+exchange) and rank 0 prints the line with the max-over-ranks time.
+--impl reference times the float64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("gdn", "reference"), default="gdn")
+    p.add_argument("--decode-steps", type=int, default=None,
+                   help="timed decode steps (default: --steps)")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        loaded = [v for v in sm if mx and v >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def gpu_id_of(torch, dev_index):
+    try:
+        props = torch.cuda.get_device_properties(dev_index)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", None)
+        pdev = getattr(props, "pci_device_id", None)
+        if bus is not None and dom is not None and pdev is not None:
+            return f"{dom:08x}:{bus:02x}:{pdev:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ---------------------------------------------------------------- workloads
+
+def alg_flops_per_token_head(C, d):
+    """Method FLOPs per (token, value head): five C x C x d contractions
+    (K K^T, Q K^T, T (beta V), T (beta e^gamma K), P W) and three C x d x d
+    contractions (Wk S^T, Q S^T, W^T K) per chunk, 2 FLOP per multiply-add."""
+    return 10 * C * d + 6 * d * d
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_07_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if the
+    sources have not changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec or rec.get("source_sha") != source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class Prefill:
+    def __init__(self, torch, gdn, inp, device):
+        d = inp["dims"]
+        self.torch, self.gdn, self.inp, self.dims = torch, gdn, inp, d
+        io = torch.bfloat16 if d.io == "bf16" else torch.float32
+        self.io = io
+        t = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)  # noqa: E731
+        self.host = {k: inp[k] for k in ("x", "a", "b")}
+        self.x, self.a, self.b = t(inp["x"], io), t(inp["a"], io), t(inp["b"], io)
+        self.cw, self.A_log, self.dt_bias = t(inp["conv_weight"]), t(inp["A_log"]), t(inp["dt_bias"])
+        self.cu = t(inp["cu_seqlens"].astype(np.int32))
+        self.slot = t(inp["slot_idx"].astype(np.int32))
+        self.init = t(inp["has_init"].astype(np.uint8))
+        self.state = t(inp["state_pool"])
+        self.conv = t(inp["conv_pool"], io)
+        T = inp["x"].shape[0]
+        self.T = T
+        self.o = torch.empty((T, d.h_v, d.d_v), dtype=io, device=device)
+        ws = gdn.gdn_prefill_workspace_size(d, T, len(inp["lengths"]))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def __call__(self, trace=None, x=None, a=None, b=None, cu=None, slot=None, init=None, o=None):
+        self.gdn.gdn_prefill(self.dims, self.cw, self.A_log, self.dt_bias,
+                             self.x if x is None else x, self.a if a is None else a,
+                             self.b if b is None else b, self.cu if cu is None else cu,
+                             self.slot if slot is None else slot, self.init if init is None else init,
+                             self.state, self.conv, self.o if o is None else o, self.ws,
+                             d_status=self.status, trace=trace)
+
+
+def bench_prefill(torch, gdn, workloads, device, steps, warmup):
+    inp = workloads.prefill_4b()
+    run = Prefill(torch, gdn, inp, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    ns = gdn.STAGES
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(max(warmup, 1)):
+        run()
+    torch.cuda.synchronize()
+    ev = [{"s": mk(), "e": mk(), "b": [mk() for _ in ns], "f": [mk() for _ in ns]}
+          for _ in range(steps)]
+    stream = torch.cuda.current_stream()
+    for e in ev:   # create the event handles before handing them to the library
+        for x in [e["s"], e["e"], *e["b"], *e["f"]]:
+            x.record(stream)
+    torch.cuda.synchronize()
+    launches = 0
+    traces = []
+    for e in ev:
+        flush.fill_(1.0)
+        e["s"].record(stream)
+        tr = gdn.make_trace(e["b"], e["f"])
+        run(trace=tr)
+        e["e"].record(stream)
+        launches += tr.launches
+        traces.append(tr)
+    torch.cuda.synchronize()
+    step_ms = [e["s"].elapsed_time(e["e"]) for e in ev]
+    stage_ms = {}
+    for i, name in enumerate(ns):
+        vals = []
+        for e, tr in zip(ev, traces):
+            if tr.stages_run & (1 << i):
+                vals.append(e["b"][i].elapsed_time(e["f"][i]))
+        if vals:
+            stage_ms[name] = statistics.mean(vals)
+    status = int(run.status.item())
+    return {"inp": inp, "run": run, "step_ms": step_ms, "stage_ms": stage_ms,
+            "launches": launches, "status": status}
+
+
+def bench_e2e(torch, gdn, run, steps, warmup):
+    """Host (pinned) inputs -> H2D -> gdn_prefill -> D2H of the output, all
+    inside the timed region, on one stream."""
+    inp = run.inp
+    io = run.io
+    pin = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(dtype=dt).pin_memory()  # noqa: E731
+    hx, ha, hb = pin(inp["x"], io), pin(inp["a"], io), pin(inp["b"], io)
+    hcu = pin(inp["cu_seqlens"].astype(np.int32))
+    hslot = pin(inp["slot_idx"].astype(np.int32))
+    hinit = pin(inp["has_init"].astype(np.uint8))
+    ho = torch.empty(run.o.shape, dtype=io).pin_memory()
+    dev = run.x.device
+    dx, da, db = (torch.empty_like(t, device=dev) for t in (hx, ha, hb))
+    dcu, dslot, dinit = (torch.empty_like(t, device=dev) for t in (hcu, hslot, hinit))
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, ha, hb, hcu, hslot, hinit))
+    d2h = ho.numel() * ho.element_size()
+
+    def step():
+        for d_, h_ in ((dx, hx), (da, ha), (db, hb), (dcu, hcu), (dslot, hslot), (dinit, hinit)):
+            d_.copy_(h_, non_blocking=True)
+        run(x=dx, a=da, b=db, cu=dcu, slot=dslot, init=dinit)
+        ho.copy_(run.o, non_blocking=True)
+
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+
+
+def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64):
+    runs = []
+    for layer in range(layers):
+        inp = workloads.decode_4b(layer, slots=slots)
+        d = inp["dims"]
+        io = torch.bfloat16
+        t = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)  # noqa: E731
+        runs.append(dict(dims=d, x=t(inp["x"], io), a=t(inp["a"], io), b=t(inp["b"], io),
+                         cw=t(inp["conv_weight"]), A=t(inp["A_log"]), dt=t(inp["dt_bias"]),
+                         slot=t(inp["slot_idx"]), state=t(inp["state_pool"]),
+                         conv=t(inp["conv_pool"], io),
+                         o=torch.empty((slots, d.h_v, d.d_v), dtype=io, device=device)))
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def step():
+        for r in runs:
+            gdn.gdn_decode_step(r["dims"], r["cw"], r["A"], r["dt"], r["x"], r["a"], r["b"],
+                                r["slot"], r["state"], r["conv"], r["o"], d_status=status)
+
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(mk(), mk()) for _ in range(steps)]
+    # one timed per-layer call as well (the kernel's own launch duration)
+    one = [(mk(), mk()) for _ in range(steps)]
+    for (s, e), (s1, e1) in zip(evs, one):
+        s.record(stream)
+        for i, r in enumerate(runs):
+            if i == 0:
+                s1.record(stream)
+            gdn.gdn_decode_step(r["dims"], r["cw"], r["A"], r["dt"], r["x"], r["a"], r["b"],
+                                r["slot"], r["state"], r["conv"], r["o"], d_status=status)
+            if i == 0:
+                e1.record(stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    layer_ms = [s.elapsed_time(e) for s, e in one]
+    d = runs[0]["dims"]
+    state_bytes = 2 * layers * slots * d.h_v * d.d_k * d.d_v * 4
+    return {"step_ms": step_ms, "layer_ms": layer_ms, "state_bytes": state_bytes,
+            "layers": layers, "slots": slots, "status": int(status.item())}
+
+
+def oracle_prefill_time(inp, n_threads):
+    import oracle
+    d = inp["dims"]
+    ov = __import__("gated_deltanet_linear_07_gb300.workloads", fromlist=["x"]).oracle_view(inp)
+    t0 = time.perf_counter()
+    oracle.layer(inp["x"], inp["a"], inp["b"], inp["conv_weight"], inp["A_log"], inp["dt_bias"],
+                 inp["cu_seqlens"], d.h_k, d.h_v, d.d_k, d.d_v, window0=ov["window0"],
+                 state0=ov["state0"], l2_eps=d.l2_eps, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def config_of(inp):
+    d = inp["dims"]
+    return {"workload": "Qwen3.5-4B-shaped Gated DeltaNet layer prefill",
+            "B": len(inp["lengths"]), "T": int(inp["x"].shape[0]), "h_k": d.h_k, "h_v": d.h_v,
+            "d_k": d.d_k, "d_v": d.d_v, "conv_dim": d.conv_dim, "conv_w": d.conv_w,
+            "chunk": d.chunk, "io": d.io, "state": "fp32, zero initial",
+            "l2": "flushed by a 256 MiB write before every timed step",
+            "parallelism": "replicas (no cross-GPU exchange in the layer)"}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from gated_deltanet_linear_07_gb300 import workloads
+    inp = workloads.prefill_4b()
+    cores = os.cpu_count() or 1
+    for _ in range(max(args.warmup, 0)):
+        oracle_prefill_time(inp, cores)
+    times = [oracle_prefill_time(inp, cores) for _ in range(args.steps)]
+    T = inp["x"].shape[0]
+    ms = 1e3 * statistics.mean(times)
+    value = T / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(inp),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"the whole workload ({T} tokens x 32 heads) per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gdn(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device visible"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    import gated_deltanet_linear_07_gb300 as gdn
+    from gated_deltanet_linear_07_gb300 import workloads
+    gdn.load()
+    peaks, peak_src = load_peaks()
+    sampler = ClockSampler(gpu_id_of(torch, local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    sampler.start()
+    time.sleep(0.2)
+    pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
+    barrier()
+    dec = None
+    if not args.no_decode:
+        dec = bench_decode(torch, gdn, workloads, device, args.decode_steps or args.steps,
+                           args.warmup)
+        barrier()
+    clocks = sampler.stop()
+    e2e = None if args.no_e2e else bench_e2e(torch, gdn, pf["run"], args.steps, args.warmup)
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    inp = pf["inp"]
+    d = inp["dims"]
+    T = inp["x"].shape[0]
+    ms = max_over_ranks(statistics.mean(pf["step_ms"]))
+    value = world * T / (ms / 1e3)
+    flops_launch = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
+    stage = pf["stage_ms"]
+    dom = max(stage, key=stage.get) if stage else None
+    peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    roof = None
+    if dom:
+        dom_ms = max_over_ranks(stage[dom])
+        if dom == "scan":
+            ach = flops_launch / (dom_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": ach / peak_tf, "traffic": recorded_traffic("prefill_" + dom),
+                    "kernel": f"prefill stage '{dom}'", "peak_source": f"bf16_tflops ({peak_src})",
+                    "launch_ms": dom_ms, "flops_per_launch": flops_launch}
+    out = None
+    if rank == 0:
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": config_of(inp),
+            "roofline": roof,
+            "tc_roofline_frac_whole_step": flops_launch / (ms / 1e3) / 1e12 / peak_tf,
+            "stages_ms": stage, "gpu_launches": pf["launches"], "clocks": clocks,
+            "device_status": pf["status"],
+        }
+        if e2e:
+            line["e2e"] = {"value": world * T / (max_over_ranks(e2e["ms"]) / 1e3),
+                           "unit": "tokens/s", "ms_per_step": e2e["ms"],
+                           "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+        if dec:
+            dms = statistics.mean(dec["step_ms"])
+            lms = statistics.mean(dec["layer_ms"])
+            gbs = dec["state_bytes"] / (dms / 1e3) / 1e9
+            lgbs = dec["state_bytes"] / dec["layers"] / (lms / 1e3) / 1e9
+            line["decode"] = {
+                "metric": "decode state GB/s", "value": gbs, "unit": "GB/s",
+                "ms_per_step": dms, "steps": args.decode_steps or args.steps,
+                "config": {"workload": "decode step, 24 layers x 64 slots, one bf16 token per "
+                                       "slot, shuffled slots, fp32 32x128x128 states",
+                           "state_bytes_per_step": dec["state_bytes"],
+                           "l2": "inputs larger than L2 (3.2 GB of state)"},
+                "roofline": {"bound": "hbm", "achieved": lgbs, "peak": hbm, "unit": "GB/s",
+                             "frac": lgbs / hbm, "traffic": recorded_traffic("decode_step"),
+                             "kernel": "decode_step_kernel (one per-layer call)",
+                             "peak_source": f"hbm_gbs ({peak_src})", "launch_ms": lms},
+                "frac_whole_step": gbs / hbm, "gpu_launches": dec["layers"] * len(dec["step_ms"]),
+                "device_status": dec["status"]}
+        if not args.no_cpu_baseline and world == 1:
+            cores = os.cpu_count() or 1
+            secs = oracle_prefill_time(inp, cores)
+            line["cpu_baseline"] = {"value": T / secs, "unit": "tokens/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"the whole workload once ({T} tokens x {d.h_v} heads), "
+                                              f"{secs:.2f} s"}
+        out = line
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gdn(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

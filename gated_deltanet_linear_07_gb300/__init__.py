@@ -1,2 +1,13 @@
-"""Gated DeltaNet linear-attention layer for GB300 (sm_103a): C-ABI CUDA library
-and its thin Python binding."""
+"""Gated DeltaNet linear-attention layer for GB300 (sm_103a).
+
+The compute lives in libgdn_gb300.so, a C-ABI CUDA library (include/gdn.h);
+this package is its thin ctypes binding (same function names), the in-tree
+build step and the seeded synthetic workloads.  There is no CPU or Python
+fallback for any step of the layer.
+"""
+from ._binding import (GDN_BF16, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_BAD_SLOT,  # noqa: F401
+                       GDN_DEV_WAIT_TIMEOUT, GDN_FP32, GdnError, conv_dim, dims_from,
+                       gdn_conv1d_update, gdn_decode_step, gdn_dims, gdn_params,
+                       gdn_prefill, gdn_prefill_workspace_size, gdn_trace, load, make_dims,
+                       make_trace, STAGES)
+from ._build import build  # noqa: F401

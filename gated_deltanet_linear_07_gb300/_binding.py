@@ -1,0 +1,218 @@
+"""Thin ctypes binding of libgdn_gb300.so (include/gdn.h), same names as the C
+ABI.  It only marshals arguments: shapes and device pointers of torch tensors
+go in, a non-zero gdn_status comes back as GdnError.  Every step of the layer
+runs in the library's CUDA kernels; there is no Python or CPU fallback, and
+loading fails loudly when the library has not been built."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgdn_gb300.so")
+
+GDN_FP32, GDN_BF16 = 0, 1
+GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+STATUS = {0: "GDN_OK", -1: "GDN_EINVAL", -2: "GDN_EUNSUPPORTED", -3: "GDN_ECUDA",
+          -4: "GDN_EWORKSPACE", -5: "GDN_EALIGN"}
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        msg = _lib.gdn_status_str(status).decode() if _lib is not None else ""
+        super().__init__(f"{func} returned {STATUS.get(status, status)} ({msg})")
+
+
+class gdn_dims(ctypes.Structure):
+    _fields_ = [("h_k", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("conv_w", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("io", ctypes.c_int32), ("l2_eps", ctypes.c_float)]
+
+
+class gdn_params(ctypes.Structure):
+    _fields_ = [("conv_weight", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p)]
+
+
+GDN_NUM_STAGES = 3
+STAGES = ("frontend", "chunk", "scan")
+
+
+class gdn_trace(ctypes.Structure):
+    _fields_ = [("begin", ctypes.c_void_p * GDN_NUM_STAGES),
+                ("end", ctypes.c_void_p * GDN_NUM_STAGES),
+                ("launches", ctypes.c_int32), ("stages_run", ctypes.c_int32)]
+
+
+def make_dims(h_k, h_v, d_k, d_v, chunk=64, io="bf16", conv_w=4, l2_eps=1e-6) -> gdn_dims:
+    io_code = {"fp32": GDN_FP32, "bf16": GDN_BF16}[io] if isinstance(io, str) else int(io)
+    return gdn_dims(h_k, h_v, d_k, d_v, conv_w, chunk, io_code, l2_eps)
+
+
+def dims_from(d) -> gdn_dims:
+    """gdn_dims from any object with h_k, h_v, d_k, d_v, chunk, io, conv_w, l2_eps."""
+    if isinstance(d, gdn_dims):
+        return d
+    return make_dims(d.h_k, d.h_v, d.d_k, d.d_v, d.chunk, d.io, d.conv_w, d.l2_eps)
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D, PR = ctypes.POINTER(gdn_dims), ctypes.POINTER(gdn_params)
+    lib.gdn_status_str.argtypes = [ctypes.c_int]
+    lib.gdn_status_str.restype = ctypes.c_char_p
+    lib.gdn_conv1d_update.argtypes = [D, P, P, P, I64, P, I32, P, P, P]
+    lib.gdn_conv1d_update.restype = ctypes.c_int
+    lib.gdn_prefill_workspace_size.argtypes = [D, I64, I32]
+    lib.gdn_prefill_workspace_size.restype = SZ
+    lib.gdn_prefill.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P, SZ, P, P]
+    lib.gdn_prefill.restype = ctypes.c_int
+    lib.gdn_prefill_traced.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P, SZ, P,
+                                       ctypes.POINTER(gdn_trace), P]
+    lib.gdn_prefill_traced.restype = ctypes.c_int
+    lib.gdn_decode_step.argtypes = [D, PR, P, P, P, P, I32, P, P, I64, P, P, P]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(func, rc):
+    if rc != 0:
+        raise GdnError(func, rc)
+
+
+def _io_dtype(d: gdn_dims):
+    import torch
+    return torch.bfloat16 if d.io == GDN_BF16 else torch.float32
+
+
+def _expect(t, name, dtype=None, numel=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+
+
+def conv_dim(d: gdn_dims) -> int:
+    return 2 * d.h_k * d.d_k + d.h_v * d.d_v
+
+
+def gdn_prefill_workspace_size(dims, total_tokens: int, num_seqs: int) -> int:
+    d = dims_from(dims)
+    return int(load().gdn_prefill_workspace_size(ctypes.byref(d), int(total_tokens), int(num_seqs)))
+
+
+def gdn_conv1d_update(dims, conv_weight, x, conv_pool, slot_idx, y, d_status=None, stream=None):
+    import torch
+    d = dims_from(dims)
+    n = int(slot_idx.numel())
+    io = _io_dtype(d)
+    _expect(conv_weight, "conv_weight", torch.float32, conv_dim(d) * d.conv_w)
+    _expect(x, "x", io, n * conv_dim(d))
+    _expect(y, "y", io, n * conv_dim(d))
+    _expect(conv_pool, "conv_pool", io)
+    _expect(slot_idx, "slot_idx", torch.int32)
+    num_slots = conv_pool.numel() // ((d.conv_w - 1) * conv_dim(d))
+    rc = load().gdn_conv1d_update(ctypes.byref(d), _ptr(conv_weight), _ptr(x), _ptr(conv_pool),
+                                  num_slots, _ptr(slot_idx), n, _ptr(y), _ptr(d_status),
+                                  _stream(stream))
+    _check("gdn_conv1d_update", rc)
+
+
+def gdn_prefill(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx,
+                has_initial_state, state_pool, conv_pool, o, workspace, d_status=None,
+                stream=None, trace=None):
+    """Whole layer over a varlen batch (see gdn_prefill in include/gdn.h).
+
+    trace: optional gdn_trace (stage events + launch count); when given the call
+    goes through gdn_prefill_traced."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    B = int(cu_seqlens.numel()) - 1
+    T = int(x.shape[0]) if x is not None else 0
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, T * cd)
+    _expect(a, "a", io, T * d.h_v)
+    _expect(b, "b", io, T * d.h_v)
+    _expect(o, "o", io, T * d.h_v * d.d_v)
+    _expect(cu_seqlens, "cu_seqlens", torch.int32)
+    _expect(slot_idx, "slot_idx", torch.int32, B)
+    _expect(has_initial_state, "has_initial_state", torch.uint8, B)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = (ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b), _ptr(cu_seqlens), B, T,
+            _ptr(slot_idx), _ptr(has_initial_state), _ptr(state_pool), _ptr(conv_pool),
+            num_slots, _ptr(o), _ptr(workspace), ws_bytes, _ptr(d_status))
+    if trace is None:
+        _check("gdn_prefill", load().gdn_prefill(*args, _stream(stream)))
+    else:
+        _check("gdn_prefill_traced",
+               load().gdn_prefill_traced(*args, ctypes.byref(trace), _stream(stream)))
+
+
+def make_trace(begin_events=None, end_events=None) -> gdn_trace:
+    """gdn_trace from lists (per stage) of torch.cuda.Event or None."""
+    tr = gdn_trace()
+    for i in range(GDN_NUM_STAGES):
+        for dst, evs in ((tr.begin, begin_events), (tr.end, end_events)):
+            ev = evs[i] if evs is not None else None
+            dst[i] = ev.cuda_event if ev is not None else None
+    return tr
+
+
+def gdn_decode_step(dims, conv_weight, A_log, dt_bias, x, a, b, slot_idx, state_pool,
+                    conv_pool, o, d_status=None, stream=None):
+    """One decode token per row (see gdn_decode_step in include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    n = int(slot_idx.numel())
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, n * cd)
+    _expect(a, "a", io, n * d.h_v)
+    _expect(b, "b", io, n * d.h_v)
+    _expect(o, "o", io, n * d.h_v * d.d_v)
+    _expect(slot_idx, "slot_idx", torch.int32)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    rc = load().gdn_decode_step(ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b),
+                                _ptr(slot_idx), n, _ptr(state_pool), _ptr(conv_pool), num_slots,
+                                _ptr(o), _ptr(d_status), _stream(stream))
+    _check("gdn_decode_step", rc)

@@ -1,0 +1,196 @@
+// gdn_api.cu -- the C ABI declared in include/gdn.h: host-side argument
+// checks, workspace carve-up and kernel dispatch.  Nothing here allocates,
+// synchronises or keeps state between calls.
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn_common.cuh"
+
+#define GDN_EXPORT extern "C" __attribute__((visibility("default")))
+
+size_t gdn_simt_scan_smem_bytes(int chunk, int d_k, int d_v);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kMaxSmem = 227 * 1024;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool pow2_dim(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t conv_dim_of(const gdn_dims* d) {
+  return 2 * (int64_t)d->h_k * d->d_k + (int64_t)d->h_v * d->d_v;
+}
+
+int check_dims(const gdn_dims* d) {
+  if (!d) return GDN_EINVAL;
+  if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0) return GDN_EINVAL;
+  if (!(d->l2_eps >= 0.0f)) return GDN_EINVAL;
+  if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
+  if (d->conv_w != 4) return GDN_EUNSUPPORTED;
+  if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
+  if (d->h_k > 65535) return GDN_EUNSUPPORTED;
+  // the prefill front end stages one token's conv output in shared memory
+  if (conv_dim_of(d) * (int64_t)sizeof(float) > (int64_t)kMaxSmem) return GDN_EUNSUPPORTED;
+  return GDN_OK;
+}
+
+int check_prefill_dims(const gdn_dims* d) {
+  int rc = check_dims(d);
+  if (rc != GDN_OK) return rc;
+  if (d->chunk != 16 && d->chunk != 32 && d->chunk != 64) return GDN_EUNSUPPORTED;
+  if (gdn_simt_scan_smem_bytes(d->chunk, d->d_k, d->d_v) > kMaxSmem) return GDN_EUNSUPPORTED;
+  return GDN_OK;
+}
+
+struct PrefillLayout {
+  size_t flag, q, k, v, g, beta, total;
+};
+
+PrefillLayout prefill_layout(const gdn_dims* d, int64_t T) {
+  PrefillLayout L;
+  size_t o = 0;
+  L.flag = o; o += align_up(16);
+  L.q = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
+  L.k = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
+  L.v = o; o += align_up((size_t)T * d->h_v * d->d_v * sizeof(float));
+  L.g = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+  L.beta = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
+
+}  // namespace
+
+GDN_EXPORT const char* gdn_status_str(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_EINVAL: return "invalid argument";
+    case GDN_EUNSUPPORTED: return "unsupported dimensions";
+    case GDN_ECUDA: return "CUDA launch or runtime error";
+    case GDN_EWORKSPACE: return "workspace missing or too small";
+    case GDN_EALIGN: return "device pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+GDN_EXPORT int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
+                                 const void* x, void* conv_pool, int64_t num_slots,
+                                 const int32_t* slot_idx, int32_t n, void* y,
+                                 int32_t* d_status, gdn_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (n < 0 || num_slots < 0) return GDN_EINVAL;
+  if (n == 0) return GDN_OK;
+  if (!conv_weight || !x || !conv_pool || !slot_idx || !y) return GDN_EINVAL;
+  if (!aligned16(conv_weight) || !aligned16(conv_pool)) return GDN_EALIGN;
+  GdnConvArgs a;
+  a.conv_dim = (int32_t)conv_dim_of(dims);
+  a.conv_w = dims->conv_w;
+  a.n = n;
+  a.num_slots = num_slots;
+  a.x = x;
+  a.slot_idx = slot_idx;
+  a.conv_weight = conv_weight;
+  a.conv_pool = conv_pool;
+  a.y = y;
+  a.d_status = d_status;
+  return cuda_rc(gdn_launch_conv_update(a, dims->io, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
+                                             int32_t num_seqs) {
+  if (check_prefill_dims(dims) != GDN_OK || total_tokens < 0 || num_seqs < 0) return 0;
+  return prefill_layout(dims, total_tokens).total;
+}
+
+GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
+                                  const void* x, const void* a, const void* b,
+                                  const int32_t* cu_seqlens, int32_t num_seqs,
+                                  int64_t total_tokens, const int32_t* slot_idx,
+                                  const uint8_t* has_initial_state, float* state_pool,
+                                  void* conv_pool, int64_t num_slots, void* o, void* workspace,
+                                  size_t workspace_bytes, int32_t* d_status, gdn_trace* trace,
+                                  gdn_stream_t stream) {
+  if (trace) {
+    trace->launches = 0;
+    trace->stages_run = 0;
+  }
+  int rc = check_prefill_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (!params || num_seqs < 0 || total_tokens < 0 || num_slots < 0) return GDN_EINVAL;
+  if (total_tokens > INT32_MAX) return GDN_EUNSUPPORTED;
+  if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_EINVAL;
+  if (!params->conv_weight || !params->A_log || !params->dt_bias || !cu_seqlens || !slot_idx ||
+      !state_pool || !conv_pool)
+    return GDN_EINVAL;
+  if (total_tokens > 0 && (!x || !a || !b || !o)) return GDN_EINVAL;
+  if (!aligned16(params->conv_weight) || !aligned16(state_pool) || !aligned16(conv_pool) ||
+      (x && !aligned16(x)) || (o && !aligned16(o)))
+    return GDN_EALIGN;
+  const PrefillLayout L = prefill_layout(dims, total_tokens);
+  if (!workspace || workspace_bytes < L.total) return GDN_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return GDN_EALIGN;
+
+  GdnPrefillArgs p;
+  memset(&p, 0, sizeof(p));
+  p.h_k = dims->h_k; p.h_v = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
+  p.conv_w = dims->conv_w; p.chunk = dims->chunk;
+  p.conv_dim = (int32_t)conv_dim_of(dims);
+  p.num_seqs = num_seqs; p.total_tokens = total_tokens; p.num_slots = num_slots;
+  p.l2_eps = dims->l2_eps;
+  p.x = x; p.a = a; p.b = b;
+  p.cu_seqlens = cu_seqlens; p.slot_idx = slot_idx; p.has_init = has_initial_state;
+  p.conv_weight = params->conv_weight; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
+  p.state_pool = state_pool; p.conv_pool = conv_pool; p.o = o; p.d_status = d_status;
+  char* ws = reinterpret_cast<char*>(workspace);
+  p.ws_flag = reinterpret_cast<int32_t*>(ws + L.flag);
+  p.ws_q = reinterpret_cast<float*>(ws + L.q);
+  p.ws_k = reinterpret_cast<float*>(ws + L.k);
+  p.ws_v = reinterpret_cast<float*>(ws + L.v);
+  p.ws_g = reinterpret_cast<float*>(ws + L.g);
+  p.ws_beta = reinterpret_cast<float*>(ws + L.beta);
+  return cuda_rc(
+      gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace));
+}
+
+GDN_EXPORT int gdn_prefill(const gdn_dims* dims, const gdn_params* params, const void* x,
+                           const void* a, const void* b, const int32_t* cu_seqlens,
+                           int32_t num_seqs, int64_t total_tokens, const int32_t* slot_idx,
+                           const uint8_t* has_initial_state, float* state_pool,
+                           void* conv_pool, int64_t num_slots, void* o, void* workspace,
+                           size_t workspace_bytes, int32_t* d_status, gdn_stream_t stream) {
+  return gdn_prefill_traced(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
+                            has_initial_state, state_pool, conv_pool, num_slots, o, workspace,
+                            workspace_bytes, d_status, nullptr, stream);
+}
+
+GDN_EXPORT int gdn_decode_step(const gdn_dims* dims, const gdn_params* params, const void* x,
+                               const void* a, const void* b, const int32_t* slot_idx, int32_t n,
+                               float* state_pool, void* conv_pool, int64_t num_slots, void* o,
+                               int32_t* d_status, gdn_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (!params || n < 0 || num_slots < 0) return GDN_EINVAL;
+  if (n == 0) return GDN_OK;
+  if (!params->conv_weight || !params->A_log || !params->dt_bias || !x || !a || !b ||
+      !slot_idx || !state_pool || !conv_pool || !o)
+    return GDN_EINVAL;
+  if (!aligned16(params->conv_weight) || !aligned16(state_pool) || !aligned16(conv_pool) ||
+      !aligned16(x) || !aligned16(o))
+    return GDN_EALIGN;
+  GdnDecodeArgs p;
+  p.h_k = dims->h_k; p.h_v = dims->h_v;
+  p.conv_dim = (int32_t)conv_dim_of(dims);
+  p.n = n; p.l2_eps = dims->l2_eps; p.num_slots = num_slots;
+  p.x = x; p.a = a; p.b = b; p.slot_idx = slot_idx;
+  p.conv_weight = params->conv_weight; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
+  p.state_pool = state_pool; p.conv_pool = conv_pool; p.o = o; p.d_status = d_status;
+  return cuda_rc(gdn_launch_decode(p, dims->d_k, dims->d_v, dims->io,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}

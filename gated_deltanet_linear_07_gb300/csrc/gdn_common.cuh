@@ -1,0 +1,142 @@
+// gdn_common.cuh -- element I/O, gate math and small device helpers shared by
+// the Gated DeltaNet kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+// ---- element I/O --------------------------------------------------------
+
+template <typename T>
+__device__ __forceinline__ float ld_io(const T* p);
+template <>
+__device__ __forceinline__ float ld_io<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_io(T* p, float v);
+template <>
+__device__ __forceinline__ void st_io<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+// Raw copy of one element (window roll: the stored inputs stay bit-exact).
+template <typename T>
+__device__ __forceinline__ void copy_io(T* dst, const T* src) { *dst = *src; }
+
+// ---- gate and activation math (fp32, CUDA math library calls) -------------
+
+// SiLU(z) = z * sigmoid(z)
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// softplus(z) = log(1 + e^z) = max(z, 0) + log1p(e^{-|z|})
+__device__ __forceinline__ float softplusf_(float z) {
+  return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
+}
+
+// g = -exp(A_log) * softplus(a + dt_bias)   (log-decay, <= 0)
+__device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
+  return -expf(A_log) * softplusf_(a + dt_bias);
+}
+
+__device__ __forceinline__ void set_status(int32_t* d_status, int bits) {
+  if (d_status) atomicOr(d_status, bits);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Streaming (evict-first) 128-bit accesses for data touched exactly once.
+__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
+
+}  // namespace gdn
+
+// Host-side launch descriptors shared between the API translation unit and
+// the kernel translation units.
+struct GdnDecodeArgs {
+  int32_t h_k, h_v, conv_dim, n;
+  float l2_eps;
+  int64_t num_slots;
+  const void* x;
+  const void* a;
+  const void* b;
+  const int32_t* slot_idx;
+  const float* conv_weight;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  void* conv_pool;
+  void* o;
+  int32_t* d_status;
+};
+
+struct GdnConvArgs {
+  int32_t conv_dim, conv_w, n;
+  int64_t num_slots;
+  const void* x;
+  const int32_t* slot_idx;
+  const float* conv_weight;
+  void* conv_pool;
+  void* y;
+  int32_t* d_status;
+};
+
+struct GdnPrefillArgs {
+  int32_t h_k, h_v, d_k, d_v, conv_w, chunk, conv_dim, num_seqs;
+  int64_t total_tokens, num_slots;
+  float l2_eps;
+  const void* x;
+  const void* a;
+  const void* b;
+  const int32_t* cu_seqlens;
+  const int32_t* slot_idx;
+  const uint8_t* has_init;
+  const float* conv_weight;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  void* conv_pool;
+  void* o;
+  int32_t* d_status;
+  // workspace carve-up (device)
+  int32_t* ws_flag;  // [0] = 1 when cu_seqlens is valid
+  float* ws_q;       // [T][h_k][d_k] normalised, scaled queries
+  float* ws_k;       // [T][h_k][d_k] normalised keys
+  float* ws_v;       // [T][h_v][d_v]
+  float* ws_g;       // [T][h_v] log-decay
+  float* ws_beta;    // [T][h_v]
+};
+
+// Launchers (defined in the kernel translation units); return cudaError_t.
+cudaError_t gdn_launch_decode(const GdnDecodeArgs& a, int d_k, int d_v, int io,
+                              cudaStream_t s);
+cudaError_t gdn_launch_conv_update(const GdnConvArgs& a, int io, cudaStream_t s);
+cudaError_t gdn_launch_prefill_simt(const GdnPrefillArgs& a, int io, cudaStream_t s,
+                                    gdn_trace* trace);
+
+// Stage-trace helpers: record the caller's event (if any) on the stream.
+inline cudaError_t gdn_trace_mark(gdn_trace* tr, int stage, bool begin, cudaStream_t s) {
+  if (!tr) return cudaSuccess;
+  tr->stages_run |= 1 << stage;
+  void* ev = begin ? tr->begin[stage] : tr->end[stage];
+  return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s) : cudaSuccess;
+}
+inline void gdn_trace_count(gdn_trace* tr, int n) {
+  if (tr) tr->launches += n;
+}

@@ -1,0 +1,211 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet linear-attention library.
+ *
+ * The layer (per sequence b, value head h, token t):
+ *   1. causal width-W conv over the mixed q|k|v channels, the W-1 previous raw
+ *      inputs coming from a rolling per-sequence window, then SiLU
+ *      (Vallmo README, "What's here": causal conv1d; oxydllm 0.0.0-alpha.12.2
+ *      release notes, New Features, "Gated DeltaNet runtime": the causal-conv
+ *      window kept in the sequence's slot);
+ *   2. split into q (H_k heads of d_k), k (H_k x d_k), v (H_v x d_v),
+ *      head-major; value head h uses key head h / (H_v/H_k); q and k are L2
+ *      normalised (eps inside the root) and q is scaled by 1/sqrt(d_k)
+ *      (PicoLM changelog, "GPU: Device-Native Pipeline Rewrite": conv1d,
+ *      l2norm, head_permute kernels);
+ *   3. gates g = -exp(A_log[h]) * softplus(a + dt_bias[h]) and
+ *      beta = sigmoid(b) (oxydllm notes, New Features: ssm_a holds the
+ *      negated exponential of A_log; the scalars stay F32);
+ *   4. the gated delta rule on a d_v x d_k fp32 memory S:
+ *        S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *        o_t = S_t q_t
+ *      (Gated DeltaNet, named as prior art in the valkyr README's License
+ *      section; the 32x128x128 F32 memory, the chunked parallel scan for
+ *      prefill and the O(1) recurrent step for decode are in the oxydllm
+ *      notes, New Features, "Gated DeltaNet runtime").
+ *
+ * Memory layouts (row-major; "IO" is the element type named by gdn_dims.io):
+ *   x            [rows][conv_dim] IO, conv_dim = 2*h_k*d_k + h_v*d_v,
+ *                channels ordered q | k | v, each head-major
+ *   a, b         [rows][h_v] IO
+ *   o            [rows][h_v][d_v] IO
+ *   conv_weight  [conv_dim][conv_w] fp32; tap conv_w-1 multiplies the newest
+ *                input
+ *   A_log, dt_bias [h_v] fp32
+ *   state_pool   [num_slots][h_v][d_k][d_v] fp32: S stored transposed, so the
+ *                value index is contiguous
+ *   conv_pool    [num_slots][conv_w-1][conv_dim] IO: the last conv_w-1 raw
+ *                inputs of the slot's sequence, oldest row first
+ *
+ * Ownership and threading: the caller owns every buffer; all data pointers
+ * are DEVICE pointers except the dims/params structs, which are read on the
+ * host during the call.  The library allocates no device memory, keeps no
+ * mutable global state, never synchronises the stream and returns as soon as
+ * the work is enqueued on `stream`.  Calls on different streams that touch
+ * different slots may run concurrently.
+ *
+ * Errors: a negative gdn_status is returned synchronously for anything the
+ * host can check (null pointers, unsupported dimensions, misalignment, a
+ * workspace that is too small, a failed launch); nothing is enqueued then.
+ * Problems only the device can see set bits in *d_status (optional device
+ * int32, OR-ed, never cleared by the library; read it after the stream
+ * synchronises) and the affected row or sequence is skipped.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_EINVAL = -1,        /* null pointer, negative size, bad cu_seqlens count */
+  GDN_EUNSUPPORTED = -2,  /* dimensions this build has no kernel for */
+  GDN_ECUDA = -3,         /* a CUDA launch or runtime call failed */
+  GDN_EWORKSPACE = -4,    /* workspace null or smaller than required */
+  GDN_EALIGN = -5         /* a device pointer is not 16-byte aligned */
+} gdn_status;
+
+typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Bits of *d_status. */
+#define GDN_DEV_BAD_SLOT 0x1        /* slot index >= num_slots: row/sequence skipped */
+#define GDN_DEV_BAD_CU_SEQLENS 0x2  /* cu_seqlens not 0..total_tokens non-decreasing: call skipped */
+#define GDN_DEV_WAIT_TIMEOUT 0x4    /* an inter-CTA wait gave up: results invalid */
+
+typedef struct {
+  int32_t h_k;     /* key/query heads */
+  int32_t h_v;     /* value heads; multiple of h_k */
+  int32_t d_k;     /* key head dim: 16, 32, 64 or 128 */
+  int32_t d_v;     /* value head dim: 16, 32, 64 or 128 */
+  int32_t conv_w;  /* conv width; must be 4 */
+  int32_t chunk;   /* prefill chunk length: 16, 32 or 64 */
+  int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
+  float l2_eps;    /* added to the sum of squares inside the L2-norm root */
+} gdn_dims;
+
+typedef struct {
+  const float* conv_weight; /* [conv_dim][conv_w] */
+  const float* A_log;       /* [h_v] */
+  const float* dt_bias;     /* [h_v] */
+} gdn_params;
+
+/*
+ * gdn_conv1d_update -- one decode token per row through the causal conv:
+ *   y[n][c] = SiLU( sum_w conv_weight[c][w] * hist_w[c] ),
+ * hist = (conv_pool[slot][0..W-2][c], x[n][c]); then the slot's window is
+ * rolled to (rows 1..W-2, x[n]).  (Vallmo README, "What's here": causal
+ * conv1d; oxydllm notes, New Features, "Gated DeltaNet runtime".)
+ *   x          [n][conv_dim] IO (device)
+ *   conv_pool  [num_slots][W-1][conv_dim] IO (device), updated in place
+ *   slot_idx   [n] int32 (device); < 0 marks a padding row (y zeroed, no
+ *              window touched); >= num_slots sets GDN_DEV_BAD_SLOT
+ *   y          [n][conv_dim] IO (device), post-SiLU
+ * Slots must be distinct within a call.
+ */
+int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
+                      const void* x, void* conv_pool, int64_t num_slots,
+                      const int32_t* slot_idx, int32_t n, void* y,
+                      int32_t* d_status, gdn_stream_t stream);
+
+/* Bytes of device workspace gdn_prefill needs for this shape (0 on bad dims). */
+size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
+                                  int32_t num_seqs);
+
+/*
+ * gdn_prefill -- the whole layer over a varlen batch, chunked (chunk length
+ * dims->chunk) as the oxydllm notes describe: a chunked parallel scan for
+ * prefill with the state-independent work batched ahead of the cross-chunk
+ * loop (New Features, "Gated DeltaNet runtime"; Performance, "Gated DeltaNet
+ * fast paths").  Each chunk's unit-lower-triangular system
+ * (I + strict_tril(diag(beta) K K^T * exp(gamma_r - gamma_s)))^-1 is solved
+ * by exact substitution, which stays finite on fully correlated keys.
+ *   x [total_tokens][conv_dim], a, b [total_tokens][h_v] IO (device)
+ *   cu_seqlens [num_seqs+1] int32 (device): 0 = cu[0] <= cu[1] <= ... =
+ *              total_tokens, else GDN_DEV_BAD_CU_SEQLENS and nothing runs
+ *   slot_idx [num_seqs] int32 (device), distinct; out of range ->
+ *              GDN_DEV_BAD_SLOT and that sequence is skipped
+ *   has_initial_state [num_seqs] uint8 (device) or NULL (= all zero): when
+ *              zero the sequence starts from S = 0 and an all-zero window,
+ *              ignoring what its slot holds
+ *   state_pool, conv_pool: read (initial state) and overwritten with the
+ *              final state / last W-1 raw inputs at each sequence's slot; a
+ *              zero-length sequence writes its initial (or zero) state back
+ *   o [total_tokens][h_v][d_v] IO (device)
+ *   workspace: device scratch of gdn_prefill_workspace_size() bytes, 256-byte
+ *              aligned, owned by the caller, clobbered by the call.
+ */
+int gdn_prefill(const gdn_dims* dims, const gdn_params* params,
+                const void* x, const void* a, const void* b,
+                const int32_t* cu_seqlens, int32_t num_seqs,
+                int64_t total_tokens, const int32_t* slot_idx,
+                const uint8_t* has_initial_state, float* state_pool,
+                void* conv_pool, int64_t num_slots, void* o,
+                void* workspace, size_t workspace_bytes, int32_t* d_status,
+                gdn_stream_t stream);
+
+/*
+ * gdn_decode_step -- one token for each of n rows, O(1) in sequence length
+ * (oxydllm notes, New Features, "Gated DeltaNet runtime": the recurrent step
+ * for decode).  Row n uses slot s = slot_idx[n]: the conv runs on the slot's
+ * window plus x[n] and rolls the window, then the slot's state is read once
+ * and written once:
+ *   u = S k^, r = S q^, delta = beta (v - alpha u),
+ *   S' = alpha S + delta k^T, o = alpha r + delta (k^ . q^),  alpha = e^g,
+ * which equals the recurrence above for one token.
+ *   x [n][conv_dim], a, b [n][h_v] IO (device); slot_idx [n] int32 (device),
+ *   distinct, < 0 = padding row (o zeroed, nothing else touched);
+ *   o [n][h_v][d_v] IO (device).
+ */
+int gdn_decode_step(const gdn_dims* dims, const gdn_params* params,
+                    const void* x, const void* a, const void* b,
+                    const int32_t* slot_idx, int32_t n, float* state_pool,
+                    void* conv_pool, int64_t num_slots, void* o,
+                    int32_t* d_status, gdn_stream_t stream);
+
+/*
+ * Stage tracing for gdn_prefill_traced.  Each non-NULL handle is a CUDA event
+ * (cudaEvent_t) owned by the caller; the call records begin[i] on `stream`
+ * right before stage i's first kernel and end[i] right after its last kernel,
+ * sets `launches` to the number of kernels the call enqueued and `stages_run`
+ * to a bit mask of the stages it ran.  A stage the call does not run records
+ * nothing.
+ *   stage 0  front end: argument check on the device, conv + SiLU, L2 norm,
+ *            gates, conv-window write-back
+ *   stage 1  per-chunk state-independent work (tensor-core path only)
+ *   stage 2  cross-chunk state scan and outputs
+ */
+#define GDN_NUM_STAGES 3
+typedef struct {
+  void* begin[GDN_NUM_STAGES];
+  void* end[GDN_NUM_STAGES];
+  int32_t launches;   /* written by the call */
+  int32_t stages_run; /* written by the call: bit i = stage i ran */
+} gdn_trace;
+
+/* gdn_prefill with stage tracing; trace may be NULL (then identical to
+ * gdn_prefill). */
+int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
+                       const void* x, const void* a, const void* b,
+                       const int32_t* cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, const int32_t* slot_idx,
+                       const uint8_t* has_initial_state, float* state_pool,
+                       void* conv_pool, int64_t num_slots, void* o,
+                       void* workspace, size_t workspace_bytes,
+                       int32_t* d_status, gdn_trace* trace,
+                       gdn_stream_t stream);
+
+/* Static description of a gdn_status code. */
+const char* gdn_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,122 @@
+"""C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+function include/gdn.h declares, and its host-side checks reject bad calls
+before anything is launched (so these run on a CPU-only host: every call below
+fails validation and never reaches the CUDA runtime)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_deltanet_linear_07_gb300 as gdn
+from gated_deltanet_linear_07_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdn.build()
+    return gdn.load()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = _declared()
+    assert {"gdn_prefill", "gdn_decode_step", "gdn_conv1d_update",
+            "gdn_prefill_workspace_size", "gdn_status_str"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln and "gdn_" in ln}
+    assert exported == declared, exported ^ declared
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.gdn_status_str(code).decode() not in ("", "unknown status")
+    assert lib.gdn_status_str(7).decode() == "unknown status"
+
+
+D4B = dict(h_k=16, h_v=32, d_k=128, d_v=128, chunk=64, io="bf16")
+
+
+def test_workspace_size_rules(lib):
+    d = gdn.make_dims(**D4B)
+    w1 = gdn.gdn_prefill_workspace_size(d, 4096, 1)
+    w2 = gdn.gdn_prefill_workspace_size(d, 8192, 1)
+    assert w1 > 0 and w2 > w1
+    # at least the normalised q, k, v and the two gates per token, in fp32
+    assert w1 >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
+    for bad in (dict(D4B, d_k=48), dict(D4B, chunk=128), dict(D4B, h_v=33),
+                dict(D4B, conv_w=3), dict(D4B, io=7)):
+        assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**bad), 4096, 1) == 0
+    assert gdn.gdn_prefill_workspace_size(d, -1, 1) == 0
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address: validation fails first
+
+
+def _prefill(lib, dims, ws_bytes=1 << 40, ptrs=None, B=1, T=64, slots=1):
+    p = _binding.gdn_params(FAKE, FAKE, FAKE)
+    ptr = dict(x=FAKE, a=FAKE, b=FAKE, cu=FAKE, slot=FAKE, init=None, state=FAKE,
+               conv=FAKE, o=FAKE, ws=FAKE)
+    ptr.update(ptrs or {})
+    return lib.gdn_prefill(ctypes.byref(dims), ctypes.byref(p), ptr["x"], ptr["a"], ptr["b"],
+                           ptr["cu"], B, T, ptr["slot"], ptr["init"], ptr["state"], ptr["conv"],
+                           slots, ptr["o"], ptr["ws"], ws_bytes, None, None)
+
+
+def test_prefill_rejects_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    assert _prefill(lib, gdn.make_dims(**dict(D4B, d_k=48))) == -2
+    assert _prefill(lib, gdn.make_dims(**dict(D4B, h_v=24))) == -1
+    assert _prefill(lib, d, ptrs=dict(cu=None)) == -1
+    assert _prefill(lib, d, ptrs=dict(state=None)) == -1
+    assert _prefill(lib, d, ptrs=dict(x=None)) == -1
+    assert _prefill(lib, d, ws_bytes=16) == -4
+    assert _prefill(lib, d, ptrs=dict(ws=None)) == -4
+    assert _prefill(lib, d, ptrs=dict(x=FAKE + 2)) == -5
+    assert _prefill(lib, d, ptrs=dict(state=FAKE + 4)) == -5
+    assert _prefill(lib, d, ptrs=dict(ws=FAKE + 16)) == -5
+    assert _prefill(lib, d, B=-1) == -1
+    assert _prefill(lib, d, B=0, T=5) == -1
+    assert _prefill(lib, d, B=0, T=0) == 0        # empty batch: nothing to do
+
+
+def test_decode_and_conv_reject_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    p = _binding.gdn_params(FAKE, FAKE, FAKE)
+    call = lambda **kw: lib.gdn_decode_step(  # noqa: E731
+        ctypes.byref(kw.get("dims", d)), ctypes.byref(p), kw.get("x", FAKE), FAKE, FAKE, FAKE,
+        kw.get("n", 4), kw.get("state", FAKE), FAKE, 8, kw.get("o", FAKE), None, None)
+    assert call(dims=gdn.make_dims(**dict(D4B, d_v=24))) == -2
+    assert call(x=None) == -1
+    assert call(n=-1) == -1
+    assert call(n=0) == 0
+    assert call(o=FAKE + 8) == -5
+    assert call(state=FAKE + 12) == -5
+    assert lib.gdn_conv1d_update(ctypes.byref(d), FAKE, None, FAKE, 8, FAKE, 4, FAKE, None,
+                                 None) == -1
+    assert lib.gdn_conv1d_update(ctypes.byref(d), FAKE + 4, FAKE, FAKE, 8, FAKE, 4, FAKE, None,
+                                 None) == -5
+    assert lib.gdn_conv1d_update(ctypes.byref(d), FAKE, FAKE, FAKE, 8, FAKE, 0, FAKE, None,
+                                 None) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _binding.load()
