@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--decode-steps", type=int, default=None,
                    help="timed decode steps (default: --steps)")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="measure only the decode step (profiling runs)")
+    p.add_argument("--decode-layers", type=int, default=24)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -401,14 +404,24 @@ def run_gdn(args):
     barrier()
     sampler.start()
     time.sleep(0.2)
-    pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
-    barrier()
+    pf = None
+    if not args.no_prefill:
+        pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
+        barrier()
     dec = None
     if not args.no_decode:
         dec = bench_decode(torch, gdn, workloads, device, args.decode_steps or args.steps,
-                           args.warmup)
+                           args.warmup, layers=args.decode_layers)
         barrier()
     clocks = sampler.stop()
+    if pf is None:
+        if rank == 0 and dec is not None:
+            print(json.dumps({"decode_only": True, "ms_per_step": statistics.mean(dec["step_ms"]),
+                              "layer_ms": statistics.mean(dec["layer_ms"]),
+                              "state_bytes": dec["state_bytes"], "clocks": clocks}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
     e2e = None if args.no_e2e else bench_e2e(torch, gdn, pf["run"], args.steps, args.warmup)
 
     def max_over_ranks(v):
