@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_prefill_traced.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P, SZ, P,
                                        ctypes.POINTER(gdn_trace), P]
     lib.gdn_prefill_traced.restype = ctypes.c_int
+    lib.gdn_prefill_noalloc.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P, P]
+    lib.gdn_prefill_noalloc.restype = ctypes.c_int
     lib.gdn_decode_step.argtypes = [D, PR, P, P, P, P, I32, P, P, I64, P, P, P]
     lib.gdn_decode_step.restype = ctypes.c_int
     _lib = lib
@@ -180,6 +182,41 @@ def gdn_prefill(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx
     else:
         _check("gdn_prefill_traced",
                load().gdn_prefill_traced(*args, ctypes.byref(trace), _stream(stream)))
+
+
+GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def gdn_prefill_noalloc(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx,
+                        has_initial_state, state_pool, conv_pool, o, d_status=None, stream=None):
+    """gdn_prefill without a workspace argument, for callers that cannot allocate
+    device memory: the library uses its own fixed device scratch array of
+    GDN_NOALLOC_SCRATCH_BYTES (see gdn_prefill_noalloc in include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    B = int(cu_seqlens.numel()) - 1
+    T = int(x.shape[0]) if x is not None else 0
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, T * cd)
+    _expect(a, "a", io, T * d.h_v)
+    _expect(b, "b", io, T * d.h_v)
+    _expect(o, "o", io, T * d.h_v * d.d_v)
+    _expect(cu_seqlens, "cu_seqlens", torch.int32)
+    _expect(slot_idx, "slot_idx", torch.int32, B)
+    _expect(has_initial_state, "has_initial_state", torch.uint8, B)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    rc = load().gdn_prefill_noalloc(ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b),
+                                    _ptr(cu_seqlens), B, T, _ptr(slot_idx),
+                                    _ptr(has_initial_state), _ptr(state_pool), _ptr(conv_pool),
+                                    num_slots, _ptr(o), _ptr(d_status), _stream(stream))
+    _check("gdn_prefill_noalloc", rc)
 
 
 def make_trace(begin_events=None, end_events=None) -> gdn_trace:

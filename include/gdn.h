@@ -201,6 +201,37 @@ int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
                        int32_t* d_status, gdn_trace* trace,
                        gdn_stream_t stream);
 
+/*
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate device
+ * memory (no counterpart in the paper: it is a deployment variant).  Code
+ * running inside a host framework whose allocator already owns nearly all of
+ * HBM, or on a path where cudaMalloc's implicit synchronisation is not
+ * acceptable, cannot obtain the workspace gdn_prefill wants.  This entry point
+ * takes the same arguments minus the workspace and uses a scratch array of
+ * GDN_NOALLOC_SCRATCH_BYTES that is part of the library's device image: every
+ * GPU that loads the library holds those bytes until the process exits.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Returns GDN_EWORKSPACE, with nothing enqueued, when the call would need
+ *     more than GDN_NOALLOC_SCRATCH_BYTES of workspace
+ *     (gdn_prefill_workspace_size() > GDN_NOALLOC_SCRATCH_BYTES; about 2000
+ *     tokens at the Qwen3.5-4B layer shape).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     kernels overlap on the GPU (different streams, or different host
+ *     threads) race on it: serialise them.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+int gdn_prefill_noalloc(const gdn_dims* dims, const gdn_params* params,
+                        const void* x, const void* a, const void* b,
+                        const int32_t* cu_seqlens, int32_t num_seqs,
+                        int64_t total_tokens, const int32_t* slot_idx,
+                        const uint8_t* has_initial_state, float* state_pool,
+                        void* conv_pool, int64_t num_slots, void* o,
+                        int32_t* d_status, gdn_stream_t stream);
+
 /* Static description of a gdn_status code. */
 const char* gdn_status_str(int status);
 
