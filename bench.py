@@ -152,24 +152,33 @@ def alg_flops_per_token_head(C, d):
     return 10 * C * d + 6 * d * d
 
 
-def source_sha():
+KERNEL_SOURCES = {
+    "decode_step": ("gdn_decode.cu", "gdn_common.cuh"),
+    "prefill_scan": ("gdn_prefill_simt.cu", "gdn_common.cuh"),
+}
+
+
+def source_sha(kernel_key):
+    """Hash of the sources a kernel is built from (the files named in
+    KERNEL_SOURCES; all of csrc/ for a kernel not listed)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_linear_07_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    files = KERNEL_SOURCES.get(kernel_key) or sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_key):
-    """DRAM bytes per launch of a kernel from the committed ncu summary, if the
-    sources have not changed since it was captured."""
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if its
+    sources have not changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel_key)
-    if not rec or rec.get("source_sha") != source_sha():
+    if not rec or rec.get("source_sha") != source_sha(kernel_key):
         return None
     return rec.get("dram_bytes_per_launch")
 
