@@ -1,0 +1,176 @@
+// gdn_tc.cuh -- Blackwell (sm_100 family, built for sm_103a) tensor-core
+// building blocks written as inline PTX: mbarriers, tensor memory (TMEM)
+// allocation and loads, tcgen05.mma of bf16 operands with fp32 accumulation,
+// shared-memory matrix descriptors for 128-byte-swizzled tiles, and the
+// fences that order the generic, async and tensor proxies.
+//
+// Operand tiles live in shared memory in the 128-byte-swizzle canonical
+// layouts the tcgen05 descriptors describe:
+//   K-major   (rows = M or N index, 64 bf16 of K per 128-byte row): element
+//             (r, k) of an R-row tile sits in K-block k/64 (R*128 bytes
+//             each) at row r, byte 2*(k%64);
+//   MN-major  (rows = K index, 64 bf16 of M/N per 128-byte row): element
+//             (mn, k) of a tile with KR K-rows sits in MN-atom mn/64 (KR*128
+//             bytes each) at row k, byte 2*(mn%64);
+// and in both the 16-byte chunk index inside a row is XOR-ed with the row
+// index mod 8 (tile bases are 1024-byte aligned).
+#pragma once
+
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- 128B swizzle ---------------------------------------------------------
+
+// Byte offset of a swizzled position given its unswizzled offset inside a
+// 1024-byte aligned tile.
+__host__ __device__ __forceinline__ uint32_t sw128(uint32_t off) {
+  return off ^ (((off >> 7) & 7u) << 4);
+}
+// K-major tile of R rows: element (r, k), 2-byte elements.
+__host__ __device__ __forceinline__ uint32_t kmaj_off(int R, int r, int k) {
+  return (uint32_t)((k >> 6) * R * 128) + sw128((uint32_t)(r * 128 + (k & 63) * 2));
+}
+// MN-major tile with KR K-rows: element (mn, k), 2-byte elements.
+__host__ __device__ __forceinline__ uint32_t mnmaj_off(int KR, int mn, int k) {
+  return (uint32_t)((mn >> 6) * KR * 128) + sw128((uint32_t)(k * 128 + (mn & 63) * 2));
+}
+
+// ---- descriptors ------------------------------------------------------------
+
+// Shared-memory matrix descriptor (tcgen05, version 1): start address,
+// leading- and stride-dimension byte offsets (16-byte units), 128B swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for sm_100 family
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+// K-major tile of R rows, MMA K-step ks (16 elements).
+__device__ __forceinline__ uint64_t sdesc_kmaj(uint32_t tile, int R, int ks) {
+  return sdesc_sw128(tile + (uint32_t)((ks >> 2) * R * 128 + (ks & 3) * 32), 16, 1024);
+}
+// MN-major tile with KR K-rows, MMA K-step ks (16 K-rows).
+__device__ __forceinline__ uint64_t sdesc_mnmaj(uint32_t tile, int KR, int ks) {
+  return sdesc_sw128(tile + (uint32_t)(ks * 16 * 128), (uint32_t)(KR * 128), 1024);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- mbarriers ----------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false when the limit runs out (the caller records the timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// ---- fences ----------------------------------------------------------------------
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (MMA reads).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- tensor memory ------------------------------------------------------------------
+
+// Whole-warp calls.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32*(w%4) .. +31; taddr carries the lane base in bits 31:16), then the wait
+// for the load.  The registers pass through the wait as in/out operands so no
+// use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace tc
+}  // namespace gdn
