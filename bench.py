@@ -154,7 +154,8 @@ def alg_flops_per_token_head(C, d):
 
 KERNEL_SOURCES = {
     "decode_step": ("gdn_decode.cu", "gdn_common.cuh"),
-    "prefill_scan": ("gdn_prefill_simt.cu", "gdn_common.cuh"),
+    "prefill_scan": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
+    "prefill_chunk": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
 }
 
 
@@ -349,6 +350,14 @@ def oracle_prefill_time(inp, n_threads):
     return time.perf_counter() - t0
 
 
+def prefill_dtype(d):
+    """Arithmetic type of the prefill: the tensor-core path (Qwen3.5-4B layer
+    shape, bf16 I/O) multiplies bf16 operands with fp32 accumulation and an
+    fp32 state; every other shape runs fp32 SIMT arithmetic."""
+    tc = d.d_k == 128 and d.d_v == 128 and d.chunk == 64 and d.io == "bf16" and d.h_v == 2 * d.h_k
+    return "bf16" if tc else "f32"
+
+
 def config_of(inp):
     d = inp["dims"]
     return {"workload": "Qwen3.5-4B-shaped Gated DeltaNet layer prefill",
@@ -465,7 +474,7 @@ def run_gdn(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic", "config": config_of(inp),
+            "dtype": prefill_dtype(inp["dims"]), "data": "synthetic", "config": config_of(inp),
             "roofline": roof,
             "tc_roofline_frac_whole_step": flops_launch / (ms / 1e3) / 1e12 / peak_tf,
             "stages_ms": stage, "gpu_launches": pf["launches"], "clocks": clocks,

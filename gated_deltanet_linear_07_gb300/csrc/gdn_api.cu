@@ -46,19 +46,37 @@ int check_prefill_dims(const gdn_dims* d) {
   return GDN_OK;
 }
 
+bool use_tc(const gdn_dims* d) {
+  return gdn_tc_prefill_supported(d->h_k, d->h_v, d->d_k, d->d_v, d->chunk, d->io);
+}
+
 struct PrefillLayout {
-  size_t flag, q, k, v, g, beta, total;
+  // SIMT path
+  size_t flag, q, k, v, g, beta;
+  // tensor-core path
+  size_t chunk_off, kq, vh;
+  int64_t max_chunks;
+  size_t total;
 };
 
-PrefillLayout prefill_layout(const gdn_dims* d, int64_t T) {
+PrefillLayout prefill_layout(const gdn_dims* d, int64_t T, int64_t B) {
   PrefillLayout L;
+  memset(&L, 0, sizeof(L));
   size_t o = 0;
   L.flag = o; o += align_up(16);
-  L.q = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
-  L.k = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
-  L.v = o; o += align_up((size_t)T * d->h_v * d->d_v * sizeof(float));
-  L.g = o; o += align_up((size_t)T * d->h_v * sizeof(float));
-  L.beta = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+  if (use_tc(d)) {
+    L.max_chunks = (T + d->chunk - 1) / d->chunk + B;
+    L.chunk_off = o; o += align_up((size_t)(B + 1) * sizeof(int32_t));
+    o = (o + 1023) / 1024 * 1024;
+    L.kq = o; o += (size_t)L.max_chunks * d->h_k * gdn_tc_kq_bytes();
+    L.vh = o; o += (size_t)L.max_chunks * d->h_v * gdn_tc_vh_bytes();
+  } else {
+    L.q = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
+    L.k = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
+    L.v = o; o += align_up((size_t)T * d->h_v * d->d_v * sizeof(float));
+    L.g = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+    L.beta = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+  }
   L.total = o;
   return L;
 }
@@ -106,7 +124,7 @@ GDN_EXPORT int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
 GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                              int32_t num_seqs) {
   if (check_prefill_dims(dims) != GDN_OK || total_tokens < 0 || num_seqs < 0) return 0;
-  return prefill_layout(dims, total_tokens).total;
+  return prefill_layout(dims, total_tokens, num_seqs).total;
 }
 
 GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
@@ -133,7 +151,7 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   if (!aligned16(params->conv_weight) || !aligned16(state_pool) || !aligned16(conv_pool) ||
       (x && !aligned16(x)) || (o && !aligned16(o)))
     return GDN_EALIGN;
-  const PrefillLayout L = prefill_layout(dims, total_tokens);
+  const PrefillLayout L = prefill_layout(dims, total_tokens, num_seqs);
   if (!workspace || workspace_bytes < L.total) return GDN_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return GDN_EALIGN;
 
@@ -155,6 +173,13 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   p.ws_v = reinterpret_cast<float*>(ws + L.v);
   p.ws_g = reinterpret_cast<float*>(ws + L.g);
   p.ws_beta = reinterpret_cast<float*>(ws + L.beta);
+  if (use_tc(dims)) {
+    p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
+    p.max_chunks = L.max_chunks;
+    p.kq_ws = reinterpret_cast<uint8_t*>(ws + L.kq);
+    p.vh_ws = reinterpret_cast<uint8_t*>(ws + L.vh);
+    return cuda_rc(gdn_launch_prefill_tc(p, reinterpret_cast<cudaStream_t>(stream), trace));
+  }
   return cuda_rc(
       gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace));
 }

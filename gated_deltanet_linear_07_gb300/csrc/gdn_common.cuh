@@ -121,6 +121,11 @@ struct GdnPrefillArgs {
   float* ws_v;       // [T][h_v][d_v]
   float* ws_g;       // [T][h_v] log-decay
   float* ws_beta;    // [T][h_v]
+  // tensor-core path workspace
+  int32_t* chunk_off;   // [num_seqs+1] first global chunk of each sequence
+  int64_t max_chunks;   // bound on the number of chunks: ceil(T/64) + num_seqs
+  uint8_t* kq_ws;       // [max_chunks][h_k] [K;Q] tile images
+  uint8_t* vh_ws;       // [max_chunks][h_v] U^T | Wk^T | P | gamma records
 };
 
 // Launchers (defined in the kernel translation units); return cudaError_t.
@@ -129,6 +134,14 @@ cudaError_t gdn_launch_decode(const GdnDecodeArgs& a, int d_k, int d_v, int io,
 cudaError_t gdn_launch_conv_update(const GdnConvArgs& a, int io, cudaStream_t s);
 cudaError_t gdn_launch_prefill_simt(const GdnPrefillArgs& a, int io, cudaStream_t s,
                                     gdn_trace* trace);
+
+cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* trace);
+// Pieces of the prefill shared by both paths (defined with the SIMT path).
+cudaError_t gdn_launch_check(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* trace);
+cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, gdn_trace* trace);
+bool gdn_tc_prefill_supported(int h_k, int h_v, int d_k, int d_v, int chunk, int io);
+size_t gdn_tc_kq_bytes();
+size_t gdn_tc_vh_bytes();
 
 // Stage-trace helpers: record the caller's event (if any) on the stream.
 inline cudaError_t gdn_trace_mark(gdn_trace* tr, int stage, bool begin, cudaStream_t s) {

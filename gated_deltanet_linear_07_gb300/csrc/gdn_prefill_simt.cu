@@ -351,6 +351,23 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
 
 }  // namespace gdn
 
+cudaError_t gdn_launch_check(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
+  gdn::check_cu_seqlens_kernel<<<1, 256, 0, s>>>(a.cu_seqlens, a.num_seqs, a.total_tokens,
+                                                 a.ws_flag, a.d_status);
+  gdn_trace_count(tr, 1);
+  return cudaGetLastError();
+}
+
+cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, gdn_trace* tr) {
+  dim3 wgrid(a.num_seqs, (a.conv_dim + 255) / 256);
+  if (io == GDN_BF16)
+    gdn::window_writeback_kernel<__nv_bfloat16><<<wgrid, 256, 0, s>>>(a);
+  else
+    gdn::window_writeback_kernel<float><<<wgrid, 256, 0, s>>>(a);
+  gdn_trace_count(tr, 1);
+  return cudaGetLastError();
+}
+
 size_t gdn_simt_scan_smem_bytes(int chunk, int d_k, int d_v) {
   return (size_t)gdn::ScanSmem(chunk, d_k, gdn::scan_dv_tile(d_v)).n * sizeof(float);
 }
