@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/gdn.h"
+#include "gdn.h"
 
 namespace gdn {
 

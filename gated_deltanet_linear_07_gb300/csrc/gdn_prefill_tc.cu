@@ -41,9 +41,12 @@ using namespace gdn::tc;
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // d_k = d_v
 constexpr uint32_t KQ_BYTES = 128 * 128 * 2;  // [K;Q] tile, K-major, 128 rows
-constexpr uint32_t UT_OFF = 0, WK_OFF = 16384, P_OFF = 32768, GAM_OFF = 40960;
+// Record of one (chunk, value head): U^T tile | Wk^T tile | P tile | decay
+// factors e^{gamma_r} [64], e^{gamma_C - gamma_r} [64], e^{gamma_C}.
+constexpr uint32_t UT_OFF = 0, WK_OFF = 16384, P_OFF = 32768, EXP_OFF = 40960;
 constexpr uint32_t VH_REC = 41984;           // per (chunk, value head)
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;   // suspending try_wait iterations
+constexpr uint32_t SPIN_LIMIT = 1u << 26;   // non-blocking test_wait iterations
 constexpr float LOG2E = 1.4426950408889634f;
 
 __device__ __forceinline__ float silu_fast(float z) {
@@ -84,17 +87,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  float a[16], b[16];
-  tmem_ld16(taddr, a);
-  tmem_ld16(taddr + 16, b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = a[i];
-    v[16 + i] = b[i];
-  }
 }
 
 // Bulk async copies (no tensor map): global -> shared with mbarrier
@@ -172,16 +164,16 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const GdnPrefillArgs 
 struct PrepSmem {
   static constexpr uint32_t KQ = 0;          // 32768  [K;Q] K-major, 128 rows x 128
   static constexpr uint32_t V = 32768;       // 2 x 16384, MN-major (64 rows s x 128 j)
-  static constexpr uint32_t BU = 65536;      // 2 x 8192, K-major (64 rows r x 64 s)
-  static constexpr uint32_t BW = 81920;      // 2 x 8192
-  static constexpr uint32_t A = 98304;       // 2 x fp32 [64][65]
-  static constexpr uint32_t T = 131584;      // 2 x fp32 [64][65]
-  static constexpr uint32_t R = 164864;      // 2 x fp32 [3][16][16]
-  static constexpr uint32_t GAM = 171008;    // fp32 [2][64] (log2 units)
-  static constexpr uint32_t BETA = 171520;   // fp32 [2][64]
-  static constexpr uint32_t BAR = 172032;    // 2 mbarriers + tmem address
-  static constexpr uint32_t SIZE = 172032 + 64;
-  static constexpr int AST = 65;             // fp32 row stride of A and T
+  static constexpr uint32_t A = 65536;       // 2 x fp32 [64][68]; later BU | BW tiles
+  static constexpr uint32_t AH = 17408;      // bytes per head of A and of T
+  static constexpr uint32_t T = 100352;      // 2 x fp32 [64][68]
+  static constexpr uint32_t R = 135168;      // 2 x fp32 [3][16][16]
+  static constexpr uint32_t GAM = 141312;    // fp32 [2][64], log2 units
+  static constexpr uint32_t BETA = 141824;   // fp32 [2][64]
+  static constexpr uint32_t EG = 142336;     // fp32 [2][64], e^{gamma}
+  static constexpr uint32_t BAR = 142848;    // 2 mbarriers + tmem address
+  static constexpr uint32_t SIZE = BAR + 64;
+  static constexpr int AST = 68;             // fp32 row stride of A and T
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, int32_t gc) {
@@ -299,6 +291,8 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
     }
   }
   // ---- gates of the two value heads (warps 14, 15) ----
+  unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
+  float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
   if (warp >= 14) {
     const int g = warp - 14;
     const int h = 2 * hk + g;
@@ -324,11 +318,21 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       const float n = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += n;
     }
-    const float exc = inc - pair;
-    gam[g * 64 + 2 * lane] = (exc + gv[0]) * LOG2E;
-    gam[g * 64 + 2 * lane + 1] = (exc + gv[0] + gv[1]) * LOG2E;
+    const float g0 = (inc - pair + gv[0]) * LOG2E, g1 = inc * LOG2E;  // log2 units
+    const float glast = __shfl_sync(0xffffffffu, g1, 31);
+    gam[g * 64 + 2 * lane] = g0;
+    gam[g * 64 + 2 * lane + 1] = g1;
     beta[g * 64 + 2 * lane] = be[0];
     beta[g * 64 + 2 * lane + 1] = be[1];
+    const float e0 = fast_exp2(g0), e1 = fast_exp2(g1);
+    eg[g * 64 + 2 * lane] = e0;
+    eg[g * 64 + 2 * lane + 1] = e1;
+    float* rec = reinterpret_cast<float*>(vrec0 + g * VH_REC + EXP_OFF);
+    rec[2 * lane] = e0;
+    rec[2 * lane + 1] = e1;
+    rec[64 + 2 * lane] = fast_exp2(glast - g0);
+    rec[64 + 2 * lane + 1] = fast_exp2(glast - g1);
+    if (lane == 0) rec[128] = fast_exp2(glast);
   }
   fence_async_smem();
   tc_fence_before();
@@ -342,53 +346,45 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
                ks > 0);
     mma_commit(&bar[0]);
   }
-  unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
-  // ---- A (lanes 0..63: K K^T) and P (lanes 64..127: Q K^T) ----
-  if (warp < 4) {
-    const bool ok = mbar_wait(&bar[0], 0, WAIT_LIMIT);
+  constexpr int S = PrepSmem::AST;
+  // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); all warps ----
+  {
+    const int q = warp & 3, g = (warp >> 2) & 1, sh = warp >> 3;
+    const int m = 32 * q + lane;
+    const bool ok = mbar_spin(&bar[0], 0, SPIN_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
-    float d[64];
-    if (ok) {
-      float t16[16];
+    float d[32];
+    if (ok) tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * sh, d);
+    else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 16 * q, t16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) d[16 * q + e] = t16[e];
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) d[e] = 0.f;
+      for (int e = 0; e < 32; ++e) d[e] = 0.f;
     }
-    if (tid < 64) {
-      const int r = tid;
+    const float* gm = gam + g * 64;
+    if (m < 64) {
+      const int r = m;
+      float* A = reinterpret_cast<float*>(sm + PrepSmem::A + g * PrepSmem::AH);
+      const float gr = gm[r], br = beta[g * 64 + r];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        float* A = reinterpret_cast<float*>(sm + PrepSmem::A) + g * 64 * PrepSmem::AST;
-        const float gr = gam[g * 64 + r], br = beta[g * 64 + r];
-#pragma unroll
-        for (int s = 0; s < 64; ++s)
-          A[r * PrepSmem::AST + s] = s < r ? br * exp2f(gr - gam[g * 64 + s]) * d[s] : 0.f;
+      for (int e = 0; e < 32; ++e) {
+        const int s = 32 * sh + e;
+        A[r * S + s] = s < r ? br * fast_exp2(gr - gm[s]) * d[e] : 0.f;
       }
     } else {
-      const int r = tid - 64;
+      const int r = m - 64;
+      const float gr = gm[r];
+      unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const float gr = gam[g * 64 + r];
-        unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
+      for (int ck = 0; ck < 4; ++ck) {
+        float pv[8];
 #pragma unroll
-        for (int ck = 0; ck < 8; ++ck) {
-          float pv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = 8 * ck + e;
-            pv[e] = s <= r ? exp2f(gr - gam[g * 64 + s]) * d[s] : 0.f;
-          }
-          uint4 pk = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
-                                pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
-          *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 8 * ck)) = pk;
+        for (int e = 0; e < 8; ++e) {
+          const int s = 32 * sh + 8 * ck + e;
+          pv[e] = s <= r ? fast_exp2(gr - gm[s]) * d[8 * ck + e] : 0.f;
         }
+        *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * sh + 8 * ck)) =
+            make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                       pack_bf16(pv[6], pv[7]));
       }
     }
   }
@@ -397,10 +393,9 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   // ---- T = (I + A)^-1 per value head: 8 warps per head ----
   {
     const int g = warp >> 3, gt = tid & 255;
-    const float* A = reinterpret_cast<const float*>(sm + PrepSmem::A) + g * 64 * PrepSmem::AST;
-    float* T = reinterpret_cast<float*>(sm + PrepSmem::T) + g * 64 * PrepSmem::AST;
+    const float* A = reinterpret_cast<const float*>(sm + PrepSmem::A + g * PrepSmem::AH);
+    float* T = reinterpret_cast<float*>(sm + PrepSmem::T + g * PrepSmem::AH);
     float* Rt = reinterpret_cast<float*>(sm + PrepSmem::R) + g * 768;
-    constexpr int S = PrepSmem::AST;
     if (gt < 64) {  // 16x16 diagonal blocks: one column each, forward substitution
       const int kb = gt >> 4, jj = gt & 15, o = kb * 16;
       float tc[16];
@@ -416,46 +411,63 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       for (int rr = 0; rr < 16; ++rr) T[(o + rr) * S + o + jj] = tc[rr];
     }
     named_bar(1 + g, 256);
-    const int rr = gt >> 4, cc = gt & 15;
+    // block rows 1..3: T[bi][bj] = -T[bi][bi] sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj];
+    // each thread owns a 1x4 strip (row rr, columns 4cg..4cg+3) of one block.
+    const int e = gt & 63, rr = e >> 2, cg = e & 3, bj = gt >> 6;
     for (int bi = 1; bi < 4; ++bi) {
-      for (int bj = 0; bj < bi; ++bj) {  // R = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj]
-        float acc = 0.f;
-        for (int bk = bj; bk < bi; ++bk) {
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            acc = fmaf(A[(bi * 16 + rr) * S + bk * 16 + m], T[(bk * 16 + m) * S + bj * 16 + cc], acc);
+      const bool act = bj < bi;
+      if (act) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* arow = A + (16 * bi + rr) * S;
+        for (int k = 16 * bj; k < 16 * bi; ++k) {
+          const float av = arow[k];
+          const float4 t4 = *reinterpret_cast<const float4*>(T + k * S + 16 * bj + 4 * cg);
+          acc.x = fmaf(av, t4.x, acc.x);
+          acc.y = fmaf(av, t4.y, acc.y);
+          acc.z = fmaf(av, t4.z, acc.z);
+          acc.w = fmaf(av, t4.w, acc.w);
         }
-        Rt[bj * 256 + rr * 16 + cc] = acc;
+        *reinterpret_cast<float4*>(Rt + bj * 256 + rr * 16 + 4 * cg) = acc;
       }
       named_bar(1 + g, 256);
-      for (int bj = 0; bj < bi; ++bj) {  // T[bi][bj] = -T[bi][bi] R
-        float acc = 0.f;
+      if (act) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* trow = T + (16 * bi + rr) * S + 16 * bi;
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc = fmaf(T[(bi * 16 + rr) * S + bi * 16 + m], Rt[bj * 256 + m * 16 + cc], acc);
-        T[(bi * 16 + rr) * S + bj * 16 + cc] = -acc;
+        for (int m2 = 0; m2 < 16; ++m2) {
+          const float tv = trow[m2];
+          const float4 r4 = *reinterpret_cast<const float4*>(Rt + bj * 256 + m2 * 16 + 4 * cg);
+          acc.x = fmaf(tv, r4.x, acc.x);
+          acc.y = fmaf(tv, r4.y, acc.y);
+          acc.z = fmaf(tv, r4.z, acc.z);
+          acc.w = fmaf(tv, r4.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(T + (16 * bi + rr) * S + 16 * bj + 4 * cg) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       named_bar(1 + g, 256);
     }
-    // B operands of the U / Wk products: (T diag(beta)) and (T diag(beta e^gamma))
+    // B operands of the U / Wk products, (T diag(beta)) and (T diag(beta e^gamma)),
+    // written over this head's A (no longer read).
+    const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH, bw = bu + 8192;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int chunk = gt + 256 * q;
       const int r = chunk >> 3, s0 = 8 * (chunk & 7);
-      float bu[8], bw[8];
+      float vu[8], vw[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s = s0 + e;
-        const float t = s <= r ? T[r * S + s] : 0.f;
-        bu[e] = t * beta[g * 64 + s];
-        bw[e] = bu[e] * exp2f(gam[g * 64 + s]);
+      for (int k = 0; k < 8; ++k) {
+        const int sc = s0 + k;
+        const float t = sc <= r ? T[r * S + sc] : 0.f;
+        vu[k] = t * beta[g * 64 + sc];
+        vw[k] = vu[k] * eg[g * 64 + sc];
       }
-      st_shared_v4(s_base + PrepSmem::BU + g * 8192 + kmaj_off(64, r, s0),
-                   make_uint4(pack_bf16(bu[0], bu[1]), pack_bf16(bu[2], bu[3]),
-                              pack_bf16(bu[4], bu[5]), pack_bf16(bu[6], bu[7])));
-      st_shared_v4(s_base + PrepSmem::BW + g * 8192 + kmaj_off(64, r, s0),
-                   make_uint4(pack_bf16(bw[0], bw[1]), pack_bf16(bw[2], bw[3]),
-                              pack_bf16(bw[4], bw[5]), pack_bf16(bw[6], bw[7])));
+      st_shared_v4(bu + kmaj_off(64, r, s0),
+                   make_uint4(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]),
+                              pack_bf16(vu[4], vu[5]), pack_bf16(vu[6], vu[7])));
+      st_shared_v4(bw + kmaj_off(64, r, s0),
+                   make_uint4(pack_bf16(vw[0], vw[1]), pack_bf16(vw[2], vw[3]),
+                              pack_bf16(vw[4], vw[5]), pack_bf16(vw[6], vw[7])));
     }
   }
   fence_async_smem();
@@ -465,27 +477,22 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   if (tid == 0) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
+      const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH, bw = bu + 8192;
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
-                 sdesc_kmaj(s_base + PrepSmem::BU + 8192 * g, 64, ks),
-                 idesc_bf16(128, 64, true, false), ks > 0);
+                 sdesc_kmaj(bu, 64, ks), idesc_bf16(128, 64, true, false), ks > 0);
       for (int ks = 0; ks < 4; ++ks)  // Wk^T_g -> TMEM columns [128+64g, +64)
         mma_bf16(tmem + 128 + 64 * g, sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks),
-                 sdesc_kmaj(s_base + PrepSmem::BW + 8192 * g, 64, ks),
-                 idesc_bf16(128, 64, true, false), ks > 0);
+                 sdesc_kmaj(bw, 64, ks), idesc_bf16(128, 64, true, false), ks > 0);
     }
     mma_commit(&bar[1]);
   }
   if (tid == 32) {  // the [K;Q] tile, already in its final image, to the workspace
     bulk_s2g(a.kq_ws + ((size_t)gc * a.h_k + hk) * KQ_BYTES, s_base + PrepSmem::KQ, KQ_BYTES);
   }
-  if (tid >= 64 && tid < 192) {  // gamma (log2 units) of both heads
-    const int g = (tid - 64) >> 6, r = (tid - 64) & 63;
-    reinterpret_cast<float*>(vrec0 + g * VH_REC + GAM_OFF)[r] = gam[g * 64 + r];
-  }
   // ---- U^T and Wk^T from TMEM to the workspace ----
   {
-    const bool ok = mbar_wait(&bar[1], 0, WAIT_LIMIT);
+    const bool ok = mbar_spin(&bar[1], 0, SPIN_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const int q = warp >> 2;             // 0,1: U^T of head q; 2,3: Wk^T of head q-2
@@ -515,15 +522,15 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// scan: one CTA (320 threads) per (sequence, value head).
+// scan: one CTA (576 threads) per (sequence, value head).
 //   warp 0: bulk loads of chunk inputs (two buffers)
 //   warp 1: MMA issue
-//   warps 2..9: epilogue; warp w owns TMEM lanes 32*(w%4).., group (w-2)/4
-//               takes one half of the columns.
+//   warps 2..17: epilogue; warp w owns TMEM lanes 32*(w%4).., and group
+//               (w-2)/4 takes one quarter of the columns.
 
 struct ScanSmem {
-  static constexpr uint32_t BUF = 74752;      // KQ 32768 | UT 16384 | Wk 16384 | P 8192 | gam 1024
-  static constexpr uint32_t B_KQ = 0, B_UT = 32768, B_WK = 49152, B_P = 65536, B_GAM = 73728;
+  static constexpr uint32_t BUF = 74752;      // KQ 32768 | UT 16384 | Wk 16384 | P 8192 | exp 1024
+  static constexpr uint32_t B_KQ = 0, B_UT = 32768, B_WK = 49152, B_P = 65536, B_EXP = 73728;
   static constexpr uint32_t HT = 2 * BUF;     // 32768, K-major 128 x 128
   static constexpr uint32_t WT = HT + 32768;  // 16384, K-major 128 x 64
   static constexpr uint32_t WTT = WT + 16384; // 16384
@@ -532,8 +539,10 @@ struct ScanSmem {
 };
 // TMEM columns
 constexpr uint32_t TX = 0, TO1 = 64, TO2 = 128, TDH = 256;
+constexpr int SCAN_THREADS = 576;
+constexpr uint32_t EPI_THREADS = 512;
 
-__global__ void __launch_bounds__(320, 1) scan_kernel(const GdnPrefillArgs a) {
+__global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -575,9 +584,9 @@ __global__ void __launch_bounds__(320, 1) scan_kernel(const GdnPrefillArgs a) {
     mbar_init(bar_x, 1);
     mbar_init(bar_dh, 1);
     mbar_init(bar_o, 1);
-    mbar_init(wready, 256);
-    mbar_init(hready, 256);
-    mbar_init(ofree, 256);
+    mbar_init(wready, EPI_THREADS);
+    mbar_init(hready, EPI_THREADS);
+    mbar_init(ofree, EPI_THREADS);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -610,88 +619,100 @@ __global__ void __launch_bounds__(320, 1) scan_kernel(const GdnPrefillArgs a) {
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
+      constexpr uint32_t ID64 = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t ID64_BMN = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t ID128_BMN = idesc_bf16(128, 128, false, true);
+      const uint64_t d_ht = sdesc_kmaj(s_base + ScanSmem::HT, 128, 0);
+      const uint64_t d_wt = sdesc_kmaj(s_base + ScanSmem::WT, 128, 0);
+      const uint64_t d_wtt = sdesc_kmaj(s_base + ScanSmem::WTT, 128, 0);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t buf = s_base + s * ScanSmem::BUF;
-        if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) ||
-            !mbar_wait(hready, c & 1, WAIT_LIMIT)) { fail(); break; }
+        const uint64_t d_wk = sdesc_mnmaj(buf + ScanSmem::B_WK, 128, 0);
+        const uint64_t d_q = sdesc_kmaj(buf + ScanSmem::B_KQ + 64 * 128, 128, 0);
+        const uint64_t d_kmn = sdesc_mnmaj(buf + ScanSmem::B_KQ, 128, 0);
+        const uint64_t d_p = sdesc_kmaj(buf + ScanSmem::B_P, 64, 0);
+        if (!mbar_spin(&full[s], (c >> 1) & 1, SPIN_LIMIT) ||
+            !mbar_spin(hready, c & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // X = H^T Wk^T
-          mma_bf16(tmem + TX, sdesc_kmaj(s_base + ScanSmem::HT, 128, ks),
-                   sdesc_mnmaj(buf + ScanSmem::B_WK, 128, ks), idesc_bf16(128, 64, false, true),
-                   ks > 0);
+          mma_bf16(tmem + TX, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc_add(d_wk, ks * 2048), ID64_BMN, ks > 0);
         mma_commit(bar_x);
-        if (c > 0 && !mbar_wait(ofree, (c - 1) & 1, WAIT_LIMIT)) { fail(); break; }
+        if (c > 0 && !mbar_spin(ofree, (c - 1) & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T
-          mma_bf16(tmem + TO1, sdesc_kmaj(s_base + ScanSmem::HT, 128, ks),
-                   sdesc_kmaj(buf + ScanSmem::B_KQ + 64 * 128, 128, ks),
-                   idesc_bf16(128, 64, false, false), ks > 0);
-        if (!mbar_wait(wready, c & 1, WAIT_LIMIT)) { fail(); break; }
+          mma_bf16(tmem + TO1, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc_add(d_q, (ks >> 2) * 16384 + (ks & 3) * 32), ID64, ks > 0);
+        if (!mbar_spin(wready, c & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
-          mma_bf16(tmem + TDH, sdesc_kmaj(s_base + ScanSmem::WTT, 128, ks),
-                   sdesc_mnmaj(buf + ScanSmem::B_KQ, 128, ks), idesc_bf16(128, 128, false, true),
+          mma_bf16(tmem + TDH, sdesc_add(d_wtt, ks * 32), sdesc_add(d_kmn, ks * 2048), ID128_BMN,
                    ks > 0);
         mma_commit(bar_dh);
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
-          mma_bf16(tmem + TO2, sdesc_kmaj(s_base + ScanSmem::WT, 128, ks),
-                   sdesc_kmaj(buf + ScanSmem::B_P, 64, ks), idesc_bf16(128, 64, false, false),
-                   ks > 0);
+          mma_bf16(tmem + TO2, sdesc_add(d_wt, ks * 32), sdesc_add(d_p, ks * 32), ID64, ks > 0);
         mma_commit(bar_o);
         mma_commit(&empty[s]);
       }
     }
   } else {
     // ---------------- epilogue ----------------
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;            // 0..3
     const uint32_t lbase = (uint32_t)(32 * (warp & 3)) << 16;
     const int j = 32 * (warp & 3) + lane;       // TMEM lane = value index
-    float H[64];                                // H^T[j][64*grp + i]
+    float H[32];                                // H^T[j][32*grp + i], fp32
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      H[i] = init ? gstate[(size_t)(64 * grp + i) * D + j] : 0.f;
-    auto write_ht = [&]() {
+    for (int i = 0; i < 32; ++i)
+      H[i] = init ? gstate[(size_t)(32 * grp + i) * D + j] : 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(s_base + ScanSmem::HT + kmaj_off(128, j, 64 * grp + 8 * q),
-                     make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
-                                pack_bf16(H[8 * q + 4], H[8 * q + 5]),
-                                pack_bf16(H[8 * q + 6], H[8 * q + 7])));
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(hready);
-    };
-    write_ht();
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q),
+                   make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
+                              pack_bf16(H[8 * q + 4], H[8 * q + 5]),
+                              pack_bf16(H[8 * q + 6], H[8 * q + 7])));
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(hready);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o);
     for (int c = 0; c < nch; ++c) {
       if (*s_abort) break;
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
-      const float* gam = reinterpret_cast<const float*>(sm + s * ScanSmem::BUF + ScanSmem::B_GAM);
+      const float* ex = reinterpret_cast<const float*>(sm + s * ScanSmem::BUF + ScanSmem::B_EXP);
       const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
-      if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) || !mbar_wait(bar_x, c & 1, WAIT_LIMIT)) {
+      if (!mbar_spin(&full[s], (c >> 1) & 1, SPIN_LIMIT) || !mbar_spin(bar_x, c & 1, SPIN_LIMIT)) {
         fail();
         break;
       }
       tc_fence_after();
-      const float glast = gam[63];
-      float eg[32];                                   // e^{gamma_r} for this group's r
+      // W^T = U^T - X and Wt^T = W^T diag(e^{gamma_C - gamma}), r in this group's quarter
+      float eg[16];
+      const float dec = ex[128];
       {
-        float X[32];
-        tmem_ld32(tmem + lbase + TX + 32 * grp, X);
+        float X[16];
+        tmem_ld16(tmem + lbase + TX + 16 * grp, X);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r0 = 32 * grp + 8 * q;
+        for (int q = 0; q < 2; ++q) {
+          const int r0 = 16 * grp + 8 * q;
           float u[8];
           bf16x8_to_float(ld_shared_v4(buf + ScanSmem::B_UT + kmaj_off(128, j, r0)), u);
+          const float4 e0 = *reinterpret_cast<const float4*>(ex + r0);
+          const float4 e1 = *reinterpret_cast<const float4*>(ex + r0 + 4);
+          const float4 d0 = *reinterpret_cast<const float4*>(ex + 64 + r0);
+          const float4 d1 = *reinterpret_cast<const float4*>(ex + 64 + r0 + 4);
+          const float ed[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          eg[8 * q + 0] = e0.x; eg[8 * q + 1] = e0.y; eg[8 * q + 2] = e0.z; eg[8 * q + 3] = e0.w;
+          eg[8 * q + 4] = e1.x; eg[8 * q + 5] = e1.y; eg[8 * q + 6] = e1.z; eg[8 * q + 7] = e1.w;
           float wv[8], wt[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float gr = gam[r0 + e];
             wv[e] = u[e] - X[8 * q + e];
-            wt[e] = wv[e] * exp2f(glast - gr);
-            eg[8 * q + e] = exp2f(gr);
+            wt[e] = wv[e] * ed[e];
           }
           st_shared_v4(s_base + ScanSmem::WT + kmaj_off(128, j, r0),
                        make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
@@ -704,31 +725,36 @@ __global__ void __launch_bounds__(320, 1) scan_kernel(const GdnPrefillArgs a) {
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(wready);
-      if (!mbar_wait(bar_dh, c & 1, WAIT_LIMIT)) { fail(); break; }
+      if (!mbar_spin(bar_dh, c & 1, SPIN_LIMIT)) { fail(); break; }
       tc_fence_after();
+      // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
       {
-        const float dec = exp2f(glast);
+        float dH[32];
+        tmem_ld32(tmem + lbase + TDH + 32 * grp, dH);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float dH[32];
-          tmem_ld32(tmem + lbase + TDH + 64 * grp + 32 * hh, dH);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) H[32 * hh + e] = fmaf(dec, H[32 * hh + e], dH[e]);
-        }
+        for (int e = 0; e < 32; ++e) H[e] = fmaf(dec, H[e], dH[e]);
       }
-      write_ht();
-      if (!mbar_wait(bar_o, c & 1, WAIT_LIMIT)) { fail(); break; }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q),
+                     make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
+                                pack_bf16(H[8 * q + 4], H[8 * q + 5]),
+                                pack_bf16(H[8 * q + 6], H[8 * q + 7])));
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(hready);
+      if (!mbar_spin(bar_o, c & 1, SPIN_LIMIT)) { fail(); break; }
       tc_fence_after();
       {
-        float O1[32], O2[32];
-        tmem_ld32(tmem + lbase + TO1 + 32 * grp, O1);
-        tmem_ld32(tmem + lbase + TO2 + 32 * grp, O2);
+        float O1[16], O2[16];
+        tmem_ld16(tmem + lbase + TO1 + 16 * grp, O1);
+        tmem_ld16(tmem + lbase + TO2 + 16 * grp, O2);
         tc_fence_before();
         mbar_arrive(ofree);
         const int64_t t0 = start + (int64_t)c * C;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int r = 32 * grp + e;
+        for (int e = 0; e < 16; ++e) {
+          const int r = 16 * grp + e;
           if (r < L)
             out[((size_t)(t0 + r) * a.h_v + h) * D + j] = __float2bfloat16_rn(fmaf(eg[e], O1[e], O2[e]));
         }
@@ -736,7 +762,7 @@ __global__ void __launch_bounds__(320, 1) scan_kernel(const GdnPrefillArgs a) {
     }
     if (!*s_abort) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) gstate[(size_t)(64 * grp + i) * D + j] = H[i];
+      for (int i = 0; i < 32; ++i) gstate[(size_t)(32 * grp + i) * D + j] = H[i];
     }
   }
   tc_fence_before();
@@ -781,7 +807,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   const int smem = (int)ScanSmem::SIZE + 1024;
   e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  scan_kernel<<<dim3(a.num_seqs, a.h_v), 320, smem, s>>>(a);
+  scan_kernel<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, smem, s>>>(a);
   gdn_trace_count(tr, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return gdn_trace_mark(tr, 2, false, s);
