@@ -239,18 +239,24 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       const float4 f = *reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e));
       w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
     }
+    // All 11 rows (3-token halo + 8 tokens) are loaded unconditionally from a
+    // valid address so the loads issue back to back; masked rows are zeroed
+    // afterwards.  Rows before the sequence start come from the slot's window.
     uint4 xr[11];
+    bool keep[11];
 #pragma unroll
     for (int q = 0; q < 11; ++q) {
       const int rr = r0 - 3 + q;                  // row within the chunk
       const int64_t p = (int64_t)c * C + rr;      // position within the sequence
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (rr < L) {
-        if (p >= 0) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + rr) * cd + ch);
-        else if (init) v = *reinterpret_cast<const uint4*>(win + (size_t)(3 + p) * cd + ch);
-      }
-      xr[q] = v;
+      const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;  // row 0 of the chunk: always valid
+      keep[q] = rr < L && (p >= 0 || init);
+      if (rr < L && p >= 0) src = x + (size_t)(t0 + rr) * cd + ch;
+      else if (rr < L && init) src = win + (size_t)(3 + p) * cd + ch;
+      xr[q] = __ldg(reinterpret_cast<const uint4*>(src));
     }
+#pragma unroll
+    for (int q = 0; q < 11; ++q)
+      if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
     const float qscale = rsqrtf((float)D);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -419,13 +425,17 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       if (act) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float* arow = A + (16 * bi + rr) * S;
-        for (int k = 16 * bj; k < 16 * bi; ++k) {
-          const float av = arow[k];
-          const float4 t4 = *reinterpret_cast<const float4*>(T + k * S + 16 * bj + 4 * cg);
-          acc.x = fmaf(av, t4.x, acc.x);
-          acc.y = fmaf(av, t4.y, acc.y);
-          acc.z = fmaf(av, t4.z, acc.z);
-          acc.w = fmaf(av, t4.w, acc.w);
+        for (int bk = bj; bk < bi; ++bk) {
+#pragma unroll
+          for (int m2 = 0; m2 < 16; ++m2) {
+            const int k = 16 * bk + m2;
+            const float av = arow[k];
+            const float4 t4 = *reinterpret_cast<const float4*>(T + k * S + 16 * bj + 4 * cg);
+            acc.x = fmaf(av, t4.x, acc.x);
+            acc.y = fmaf(av, t4.y, acc.y);
+            acc.z = fmaf(av, t4.z, acc.z);
+            acc.w = fmaf(av, t4.w, acc.w);
+          }
         }
         *reinterpret_cast<float4*>(Rt + bj * 256 + rr * 16 + 4 * cg) = acc;
       }
