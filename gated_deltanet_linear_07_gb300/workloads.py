@@ -52,11 +52,17 @@ QWEN35_4B = Dims(h_k=16, h_v=32, d_k=128, d_v=128, chunk=64, io="bf16")
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even), kept as float32."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    """Round float32 values to the nearest bf16 (ties to even), kept as float32.
+    Works in place on a float32 copy, in slices, with 32-bit integer arithmetic
+    (finite inputs only)."""
+    out = np.array(a, dtype=np.float32, copy=True, order="C")
+    flat = out.reshape(-1).view(np.uint32)
+    step = 1 << 24
+    for i in range(0, flat.size, step):
+        u = flat[i:i + step]
+        u += np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+        u &= np.uint32(0xFFFF0000)
+    return out
 
 
 def _io(a: np.ndarray, dims: Dims) -> np.ndarray:

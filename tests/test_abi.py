@@ -57,8 +57,12 @@ def test_workspace_size_rules(lib):
     w1 = gdn.gdn_prefill_workspace_size(d, 4096, 1)
     w2 = gdn.gdn_prefill_workspace_size(d, 8192, 1)
     assert w1 > 0 and w2 > w1
-    # at least the normalised q, k, v and the two gates per token, in fp32
-    assert w1 >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
+    # tensor-core path (this shape): per chunk slot ([T/64] + B of them) one
+    # 32 KiB [K;Q] tile per key head and a 41 KiB record per value head
+    assert w1 >= (4096 // 64 + 1) * (16 * 32768 + 32 * 41984)
+    # SIMT path (fp32 I/O): normalised q, k, v and the two gates per token, fp32
+    d32 = gdn.make_dims(**dict(D4B, io="fp32"))
+    assert gdn.gdn_prefill_workspace_size(d32, 4096, 1) >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
     for bad in (dict(D4B, d_k=48), dict(D4B, chunk=128), dict(D4B, h_v=33),
                 dict(D4B, conv_w=3), dict(D4B, io=7)):
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**bad), 4096, 1) == 0
