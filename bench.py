@@ -455,18 +455,27 @@ def run_gdn(args):
     ms = max_over_ranks(statistics.mean(pf["step_ms"]))
     value = world * T / (ms / 1e3)
     flops_launch = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
+    # The method's FLOPs by the stage that performs them: the chunk stage does
+    # K K^T, Q K^T, T (beta V), T (beta e^gamma K) (8 C d per token and head),
+    # the scan does P W and Wk S^T, Q S^T, W^T K (2 C d + 6 d^2).
+    stage_flops = {"frontend": 0.0,
+                   "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
+                   "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
     stage = pf["stage_ms"]
     dom = max(stage, key=stage.get) if stage else None
     peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     roof = None
-    if dom:
+    if dom and stage_flops.get(dom):
         dom_ms = max_over_ranks(stage[dom])
-        if dom == "scan":
-            ach = flops_launch / (dom_ms / 1e3) / 1e12
-            roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": ach / peak_tf, "traffic": recorded_traffic("prefill_" + dom),
-                    "kernel": f"prefill stage '{dom}'", "peak_source": f"bf16_tflops ({peak_src})",
-                    "launch_ms": dom_ms, "flops_per_launch": flops_launch}
+        ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": ach / peak_tf, "traffic": recorded_traffic("prefill_" + dom),
+                "kernel": {"chunk": "prep_kernel (prefill stage 'chunk')",
+                           "scan": "scan_kernel (prefill stage 'scan')"}.get(dom, dom),
+                "peak_source": f"bf16_tflops ({peak_src})",
+                "launch_ms": dom_ms, "flops_per_launch": stage_flops[dom]}
+    stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()
+                    if stage_flops.get(k)}
     out = None
     if rank == 0:
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -477,7 +486,8 @@ def run_gdn(args):
             "dtype": prefill_dtype(inp["dims"]), "data": "synthetic", "config": config_of(inp),
             "roofline": roof,
             "tc_roofline_frac_whole_step": flops_launch / (ms / 1e3) / 1e12 / peak_tf,
-            "stages_ms": stage, "gpu_launches": pf["launches"], "clocks": clocks,
+            "stages_ms": stage, "stages_tflops": stage_tflops,
+            "gpu_launches": pf["launches"], "clocks": clocks,
             "device_status": pf["status"],
         }
         if e2e:

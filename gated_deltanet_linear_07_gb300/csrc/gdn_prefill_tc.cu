@@ -40,11 +40,17 @@ using namespace gdn::tc;
 
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // d_k = d_v
-constexpr uint32_t KQ_BYTES = 128 * 128 * 2;  // [K;Q] tile, K-major, 128 rows
-// Record of one (chunk, value head): U^T tile | Wk^T tile | P tile | decay
-// factors e^{gamma_r} [64], e^{gamma_C - gamma_r} [64], e^{gamma_C}.
-constexpr uint32_t UT_OFF = 0, WK_OFF = 16384, P_OFF = 32768, EXP_OFF = 40960;
-constexpr uint32_t VH_REC = 41984;           // per (chunk, value head)
+constexpr uint32_t KQ_BYTES = 128 * 128 * 2;  // [K;Q] tile in the prep, K-major, 128 rows
+constexpr uint32_t Q_REC = 64 * 128 * 2;      // per (chunk, key head): Q tile, K-major, 64 rows
+// Record of one (chunk, value head), every tile a ready shared-memory image:
+//   P    [r][s]  K-major, 64 rows            8 KiB
+//   KT   [i][s]  K-major, 128 rows  (K diag(e^{gamma_C - gamma}))^T   16 KiB
+//   UT   [j][r]  K-major, 128 rows           16 KiB
+//   EXP  e^{gamma_r} [64], e^{gamma_C - gamma_r} [64], e^{gamma_C}     1 KiB
+//   WK   [r][i]  K-major, 64 rows (two 8 KiB K-blocks)                16 KiB
+constexpr uint32_t P_OFF = 0, KT_OFF = 8192, UT_OFF = 24576, EXP_OFF = 40960, WK_OFF = 41984;
+constexpr uint32_t VH_REC = 58368;           // per (chunk, value head)
+constexpr uint32_t VH_HEAD = 41984;          // P | KT | UT | EXP, copied in one piece
 constexpr uint32_t WAIT_LIMIT = 1u << 22;   // suspending try_wait iterations
 constexpr uint32_t SPIN_LIMIT = 1u << 26;   // non-blocking test_wait iterations
 constexpr float LOG2E = 1.4426950408889634f;
@@ -171,7 +177,9 @@ struct PrepSmem {
   static constexpr uint32_t GAM = 141312;    // fp32 [2][64], log2 units
   static constexpr uint32_t BETA = 141824;   // fp32 [2][64]
   static constexpr uint32_t EG = 142336;     // fp32 [2][64], e^{gamma}
-  static constexpr uint32_t BAR = 142848;    // 2 mbarriers + tmem address
+  static constexpr uint32_t BW2 = 143360;    // [T diag(beta e^gamma)] of both heads, K-major 128 rows x 64
+  static constexpr uint32_t DED = 159744;    // 2 x diag(e^{gamma_C - gamma}), K-major 64 x 64
+  static constexpr uint32_t BAR = 176128;    // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
   static constexpr int AST = 68;             // fp32 row stride of A and T
 };
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   const uint32_t s_base = smem_u32(sm);
 
   if (warp == 0) {
-    tmem_alloc(s_tmem, 256);
+    tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
   if (tid == 32) {
@@ -457,20 +465,32 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       }
       named_bar(1 + g, 256);
     }
-    // B operands of the U / Wk products, (T diag(beta)) and (T diag(beta e^gamma)),
-    // written over this head's A (no longer read).
-    const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH, bw = bu + 8192;
+    // B operands: (T diag(beta)) of this head over its A (no longer read),
+    // (T diag(beta e^gamma)) into rows 64g.. of the stacked tile, and the
+    // diagonal tile diag(e^{gamma_C - gamma}).
+    const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH;
+    const uint32_t bw = s_base + PrepSmem::BW2 + 8192 * g;
+    const uint32_t ded = s_base + PrepSmem::DED + 8192 * g;
+    float tv[2][8];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int chunk = gt + 256 * q;
       const int r = chunk >> 3, s0 = 8 * (chunk & 7);
-      float vu[8], vw[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? T[r * S + s0 + k] : 0.f;
+    }
+    const float glast = gam[g * 64 + 63];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int chunk = gt + 256 * q;
+      const int r = chunk >> 3, s0 = 8 * (chunk & 7);
+      float vu[8], vw[8], vd[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int sc = s0 + k;
-        const float t = sc <= r ? T[r * S + sc] : 0.f;
-        vu[k] = t * beta[g * 64 + sc];
+        vu[k] = tv[q][k] * beta[g * 64 + sc];
         vw[k] = vu[k] * eg[g * 64 + sc];
+        vd[k] = sc == r ? fast_exp2(glast - gam[g * 64 + sc]) : 0.f;
       }
       st_shared_v4(bu + kmaj_off(64, r, s0),
                    make_uint4(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]),
@@ -478,6 +498,9 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       st_shared_v4(bw + kmaj_off(64, r, s0),
                    make_uint4(pack_bf16(vw[0], vw[1]), pack_bf16(vw[2], vw[3]),
                               pack_bf16(vw[4], vw[5]), pack_bf16(vw[6], vw[7])));
+      st_shared_v4(ded + kmaj_off(64, r, s0),
+                   make_uint4(pack_bf16(vd[0], vd[1]), pack_bf16(vd[2], vd[3]),
+                              pack_bf16(vd[4], vd[5]), pack_bf16(vd[6], vd[7])));
     }
   }
   fence_async_smem();
@@ -487,68 +510,88 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   if (tid == 0) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
-      const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH, bw = bu + 8192;
+      const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH;
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
                  sdesc_kmaj(bu, 64, ks), idesc_bf16(128, 64, true, false), ks > 0);
-      for (int ks = 0; ks < 4; ++ks)  // Wk^T_g -> TMEM columns [128+64g, +64)
-        mma_bf16(tmem + 128 + 64 * g, sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks),
-                 sdesc_kmaj(bw, 64, ks), idesc_bf16(128, 64, true, false), ks > 0);
+      for (int ks = 0; ks < 4; ++ks)  // K~^T_g = K^T diag(e^{gamma_C-gamma}) -> [256+64g, +64)
+        mma_bf16(tmem + 256 + 64 * g, sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks),
+                 sdesc_kmaj(s_base + PrepSmem::DED + 8192 * g, 64, ks),
+                 idesc_bf16(128, 64, true, false), ks > 0);
     }
+    for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
+      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BW2, 128, ks),
+               sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 128, false, true),
+               ks > 0);
     mma_commit(&bar[1]);
   }
-  if (tid == 32) {  // the [K;Q] tile, already in its final image, to the workspace
-    bulk_s2g(a.kq_ws + ((size_t)gc * a.h_k + hk) * KQ_BYTES, s_base + PrepSmem::KQ, KQ_BYTES);
+  if (tid == 32) {  // the Q rows of the [K;Q] tile (already a tile image) to the workspace
+    unsigned char* qrec = a.kq_ws + ((size_t)gc * a.h_k + hk) * Q_REC;
+    bulk_s2g(qrec, s_base + PrepSmem::KQ + 8192, 8192);
+    bulk_s2g(qrec + 8192, s_base + PrepSmem::KQ + 16384 + 8192, 8192);
   }
-  // ---- U^T and Wk^T from TMEM to the workspace ----
+  // ---- U^T, [Wk_0; Wk_1] and K~^T from TMEM to the workspace ----
   {
     const bool ok = mbar_spin(&bar[1], 0, SPIN_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
-    const int q = warp >> 2;             // 0,1: U^T of head q; 2,3: Wk^T of head q-2
-    const int m = 32 * (warp & 3) + lane;
-    const int g = q & 1;
-    unsigned char* dst = vrec0 + g * VH_REC + (q < 2 ? UT_OFF : WK_OFF);
-    if (ok) {
+    const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
+    // 24 tasks of (lane quarter, 64 columns); warp w takes tasks w and w+16,
+    // whose lane quarter matches its own (TMEM lane access rule).
+    for (int task = warp; task < 24 && ok; task += 16) {
+      const int kind = task >> 2;                // 0,1: U^T_g  2,3: Wk halves  4,5: K~^T_g
+      const uint32_t col = kind < 2 ? 64 * kind : (kind < 4 ? 128 + 64 * (kind - 2) : 256 + 64 * (kind - 4));
+      float v[2][32];
+      tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col, v[0]);
+      tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32, v[1]);
+      unsigned char* dst;
+      int row, R, c0;
+      if (kind < 2) {            // U^T_g row j = m
+        dst = vrec0 + kind * VH_REC + UT_OFF; row = m; R = 128; c0 = 0;
+      } else if (kind < 4) {     // Wk of head m/64, row r = m%64, columns i in this half
+        dst = vrec0 + (m >> 6) * VH_REC + WK_OFF; row = m & 63; R = 64; c0 = 64 * (kind - 2);
+      } else {                   // K~^T_g row i = m
+        dst = vrec0 + (kind - 4) * VH_REC + KT_OFF; row = m; R = 128; c0 = 0;
+      }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * q + 32 * h2, v);
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
-          uint4 pk = make_uint4(pack_bf16(v[8 * ck], v[8 * ck + 1]),
-                                pack_bf16(v[8 * ck + 2], v[8 * ck + 3]),
-                                pack_bf16(v[8 * ck + 4], v[8 * ck + 5]),
-                                pack_bf16(v[8 * ck + 6], v[8 * ck + 7]));
-          *reinterpret_cast<uint4*>(dst + kmaj_off(128, m, 32 * h2 + 8 * ck)) = pk;
+          const float* f = &v[h2][8 * ck];
+          uint4 pk = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+          *reinterpret_cast<uint4*>(dst + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck)) = pk;
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 32) bulk_wait_read();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (tid == 32) bulk_wait_all();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
 // scan: one CTA (576 threads) per (sequence, value head).
 //   warp 0: bulk loads of chunk inputs (two buffers)
-//   warp 1: MMA issue
+//   warp 1: MMA issue, two groups per chunk:
+//             [X | O1]  = H^T [Wk; Q]^T      (N = 128, TMEM double-buffered)
+//             [O2 | dH] = W^T [P; K~^T]^T    (N = 192)
 //   warps 2..17: epilogue; warp w owns TMEM lanes 32*(w%4).., and group
 //               (w-2)/4 takes one quarter of the columns.
 
 struct ScanSmem {
-  static constexpr uint32_t BUF = 74752;      // KQ 32768 | UT 16384 | Wk 16384 | P 8192 | exp 1024
-  static constexpr uint32_t B_KQ = 0, B_UT = 32768, B_WK = 49152, B_P = 65536, B_EXP = 73728;
+  // per buffer: B2 = [P; K~^T] (K-major, 192 rows x 64) | UT | EXP | B1 = [Wk; Q] (K-major 128 x 128)
+  static constexpr uint32_t BUF = 74752;
+  static constexpr uint32_t B_B2 = 0, B_UT = 24576, B_EXP = 40960, B_B1 = 41984;
   static constexpr uint32_t HT = 2 * BUF;     // 32768, K-major 128 x 128
   static constexpr uint32_t WT = HT + 32768;  // 16384, K-major 128 x 64
-  static constexpr uint32_t WTT = WT + 16384; // 16384
-  static constexpr uint32_t BAR = WTT + 16384;
+  static constexpr uint32_t OST = WT + 16384; // 16384, output staging [r][j] bf16
+  static constexpr uint32_t BAR = OST + 16384;
   static constexpr uint32_t SIZE = BAR + 256;
 };
-// TMEM columns
-constexpr uint32_t TX = 0, TO1 = 64, TO2 = 128, TDH = 256;
+// TMEM columns: [X | O1] x 2 buffers, then [O2 | dH]
+constexpr uint32_t TXO = 0, TOD = 256;
 constexpr int SCAN_THREADS = 576;
 constexpr uint32_t EPI_THREADS = 512;
 
@@ -575,12 +618,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   uint64_t* empty = full + 2;                                             // [2]
   uint64_t* bar_x = full + 4;
   uint64_t* bar_dh = full + 5;
-  uint64_t* bar_o = full + 6;
-  uint64_t* wready = full + 7;
-  uint64_t* hready = full + 8;
-  uint64_t* ofree = full + 9;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 10);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(full + 11);
+  uint64_t* wready = full + 6;
+  uint64_t* hready = full + 7;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 8);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(full + 9);
 
   if (warp == 0) {
     tmem_alloc(s_tmem, 512);
@@ -593,10 +634,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     mbar_init(&empty[1], 1);
     mbar_init(bar_x, 1);
     mbar_init(bar_dh, 1);
-    mbar_init(bar_o, 1);
     mbar_init(wready, EPI_THREADS);
     mbar_init(hready, EPI_THREADS);
-    mbar_init(ofree, EPI_THREADS);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -619,54 +658,42 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         if (c >= 2 && !mbar_wait(&empty[s], ((c >> 1) - 1) & 1, WAIT_LIMIT)) { fail(); break; }
         if (*s_abort) break;
         const uint32_t dst = s_base + s * ScanSmem::BUF;
+        const unsigned char* vrec = a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC;
+        const unsigned char* qrec = a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * Q_REC;
         mbar_expect_tx(&full[s], ScanSmem::BUF);
-        bulk_g2s(dst + ScanSmem::B_KQ, a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * KQ_BYTES,
-                 KQ_BYTES, &full[s]);
-        bulk_g2s(dst + ScanSmem::B_UT, a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC,
-                 VH_REC, &full[s]);
+        bulk_g2s(dst, vrec, VH_HEAD, &full[s]);                                   // P|KT|UT|EXP
+        bulk_g2s(dst + ScanSmem::B_B1, vrec + WK_OFF, 8192, &full[s]);             // Wk K-block 0
+        bulk_g2s(dst + ScanSmem::B_B1 + 16384, vrec + WK_OFF + 8192, 8192, &full[s]);  // block 1
+        bulk_g2s(dst + ScanSmem::B_B1 + 8192, qrec, 8192, &full[s]);               // Q K-block 0
+        bulk_g2s(dst + ScanSmem::B_B1 + 24576, qrec + 8192, 8192, &full[s]);       // block 1
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t ID64 = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t ID64_BMN = idesc_bf16(128, 64, false, true);
-      constexpr uint32_t ID128_BMN = idesc_bf16(128, 128, false, true);
+      constexpr uint32_t ID_XO = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_OD = idesc_bf16(128, 192, false, false);
       const uint64_t d_ht = sdesc_kmaj(s_base + ScanSmem::HT, 128, 0);
       const uint64_t d_wt = sdesc_kmaj(s_base + ScanSmem::WT, 128, 0);
-      const uint64_t d_wtt = sdesc_kmaj(s_base + ScanSmem::WTT, 128, 0);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t buf = s_base + s * ScanSmem::BUF;
-        const uint64_t d_wk = sdesc_mnmaj(buf + ScanSmem::B_WK, 128, 0);
-        const uint64_t d_q = sdesc_kmaj(buf + ScanSmem::B_KQ + 64 * 128, 128, 0);
-        const uint64_t d_kmn = sdesc_mnmaj(buf + ScanSmem::B_KQ, 128, 0);
-        const uint64_t d_p = sdesc_kmaj(buf + ScanSmem::B_P, 64, 0);
-        if (!mbar_spin(&full[s], (c >> 1) & 1, SPIN_LIMIT) ||
-            !mbar_spin(hready, c & 1, SPIN_LIMIT)) { fail(); break; }
+        const uint64_t d_b1 = sdesc_kmaj(buf + ScanSmem::B_B1, 128, 0);
+        const uint64_t d_b2 = sdesc_kmaj(buf + ScanSmem::B_B2, 192, 0);
+        if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) ||
+            !mbar_wait(hready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // X = H^T Wk^T
-          mma_bf16(tmem + TX, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc_add(d_wk, ks * 2048), ID64_BMN, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)  // [X | O1] = H^T [Wk; Q]^T
+          mma_bf16(tmem + TXO + 128 * s, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(bar_x);
-        if (c > 0 && !mbar_spin(ofree, (c - 1) & 1, SPIN_LIMIT)) { fail(); break; }
+        if (!mbar_wait(wready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T
-          mma_bf16(tmem + TO1, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc_add(d_q, (ks >> 2) * 16384 + (ks & 3) * 32), ID64, ks > 0);
-        if (!mbar_spin(wready, c & 1, SPIN_LIMIT)) { fail(); break; }
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
-          mma_bf16(tmem + TDH, sdesc_add(d_wtt, ks * 32), sdesc_add(d_kmn, ks * 2048), ID128_BMN,
-                   ks > 0);
+        for (int ks = 0; ks < 4; ++ks)  // [O2 | dH] = W^T [P; K~^T]^T
+          mma_bf16(tmem + TOD, sdesc_add(d_wt, ks * 32), sdesc_add(d_b2, ks * 32), ID_OD, ks > 0);
         mma_commit(bar_dh);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
-          mma_bf16(tmem + TO2, sdesc_add(d_wt, ks * 32), sdesc_add(d_p, ks * 32), ID64, ks > 0);
-        mma_commit(bar_o);
         mma_commit(&empty[s]);
       }
     }
@@ -694,18 +721,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
       const float* ex = reinterpret_cast<const float*>(sm + s * ScanSmem::BUF + ScanSmem::B_EXP);
+      const uint32_t txo = tmem + lbase + TXO + 128 * s;
       const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
-      if (!mbar_spin(&full[s], (c >> 1) & 1, SPIN_LIMIT) || !mbar_spin(bar_x, c & 1, SPIN_LIMIT)) {
+      if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) || !mbar_wait(bar_x, c & 1, WAIT_LIMIT)) {
         fail();
         break;
       }
       tc_fence_after();
-      // W^T = U^T - X and Wt^T = W^T diag(e^{gamma_C - gamma}), r in this group's quarter
+      // W^T = U^T - X for r in this group's quarter
       float eg[16];
       const float dec = ex[128];
       {
         float X[16];
-        tmem_ld16(tmem + lbase + TX + 16 * grp, X);
+        tmem_ld16(txo + 16 * grp, X);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int r0 = 16 * grp + 8 * q;
@@ -713,34 +741,25 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
           bf16x8_to_float(ld_shared_v4(buf + ScanSmem::B_UT + kmaj_off(128, j, r0)), u);
           const float4 e0 = *reinterpret_cast<const float4*>(ex + r0);
           const float4 e1 = *reinterpret_cast<const float4*>(ex + r0 + 4);
-          const float4 d0 = *reinterpret_cast<const float4*>(ex + 64 + r0);
-          const float4 d1 = *reinterpret_cast<const float4*>(ex + 64 + r0 + 4);
-          const float ed[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
           eg[8 * q + 0] = e0.x; eg[8 * q + 1] = e0.y; eg[8 * q + 2] = e0.z; eg[8 * q + 3] = e0.w;
           eg[8 * q + 4] = e1.x; eg[8 * q + 5] = e1.y; eg[8 * q + 6] = e1.z; eg[8 * q + 7] = e1.w;
-          float wv[8], wt[8];
+          float wv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            wv[e] = u[e] - X[8 * q + e];
-            wt[e] = wv[e] * ed[e];
-          }
+          for (int e = 0; e < 8; ++e) wv[e] = u[e] - X[8 * q + e];
           st_shared_v4(s_base + ScanSmem::WT + kmaj_off(128, j, r0),
                        make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
                                   pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7])));
-          st_shared_v4(s_base + ScanSmem::WTT + kmaj_off(128, j, r0),
-                       make_uint4(pack_bf16(wt[0], wt[1]), pack_bf16(wt[2], wt[3]),
-                                  pack_bf16(wt[4], wt[5]), pack_bf16(wt[6], wt[7])));
         }
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(wready);
-      if (!mbar_spin(bar_dh, c & 1, SPIN_LIMIT)) { fail(); break; }
+      if (!mbar_wait(bar_dh, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
       // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
       {
         float dH[32];
-        tmem_ld32(tmem + lbase + TDH + 32 * grp, dH);
+        tmem_ld32(tmem + lbase + TOD + 64 + 32 * grp, dH);
 #pragma unroll
         for (int e = 0; e < 32; ++e) H[e] = fmaf(dec, H[e], dH[e]);
       }
@@ -752,23 +771,32 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
                                 pack_bf16(H[8 * q + 6], H[8 * q + 7])));
       fence_async_smem();
       tc_fence_before();
+      // o = e^{gamma} O1 + O2 (read before arriving, so the next chunk's MMAs
+      // cannot overwrite O2 / this buffer's O1 while they are read)
+      float O1[16], O2[16];
+      tmem_ld16(txo + 64 + 16 * grp, O1);
+      tmem_ld16(tmem + lbase + TOD + 16 * grp, O2);
+      tc_fence_before();
       mbar_arrive(hready);
-      if (!mbar_spin(bar_o, c & 1, SPIN_LIMIT)) { fail(); break; }
-      tc_fence_after();
+      // Stage this warp's 16 x 32 block of o in its own 1 KiB of shared
+      // memory, then write it as 16-byte pieces (8 values of one row each).
+      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + ScanSmem::OST + (warp - 2) * 1024);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ost[e * 32 + lane] = __float2bfloat16_rn(fmaf(eg[e], O1[e], O2[e]));
+      __syncwarp();
       {
-        float O1[16], O2[16];
-        tmem_ld16(tmem + lbase + TO1 + 16 * grp, O1);
-        tmem_ld16(tmem + lbase + TO2 + 16 * grp, O2);
-        tc_fence_before();
-        mbar_arrive(ofree);
         const int64_t t0 = start + (int64_t)c * C;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int q = 0; q < 2; ++q) {
+          const int piece = lane + 32 * q;       // 16 rows x 4 pieces
+          const int e = piece >> 2, k = piece & 3;
           const int r = 16 * grp + e;
           if (r < L)
-            out[((size_t)(t0 + r) * a.h_v + h) * D + j] = __float2bfloat16_rn(fmaf(eg[e], O1[e], O2[e]));
+            *reinterpret_cast<uint4*>(out + ((size_t)(t0 + r) * a.h_v + h) * D + 32 * (warp & 3) + 8 * k) =
+                *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * k);
         }
       }
+      __syncwarp();  // staging reusable by the next chunk
     }
     if (!*s_abort) {
 #pragma unroll
@@ -789,7 +817,7 @@ bool gdn_tc_prefill_supported(int h_k, int h_v, int d_k, int d_v, int chunk, int
   return d_k == 128 && d_v == 128 && chunk == 64 && io == GDN_BF16 && h_v == 2 * h_k;
 }
 
-size_t gdn_tc_kq_bytes() { return gdn::tcp::KQ_BYTES; }
+size_t gdn_tc_kq_bytes() { return gdn::tcp::Q_REC; }
 size_t gdn_tc_vh_bytes() { return gdn::tcp::VH_REC; }
 
 cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {

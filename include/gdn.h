@@ -213,7 +213,7 @@ int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
  * calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Returns GDN_EWORKSPACE, with nothing enqueued, when the call would need
  *     more than GDN_NOALLOC_SCRATCH_BYTES of workspace
- *     (gdn_prefill_workspace_size() > GDN_NOALLOC_SCRATCH_BYTES; about 2000
+ *     (gdn_prefill_workspace_size() > GDN_NOALLOC_SCRATCH_BYTES; about 1900
  *     tokens at the Qwen3.5-4B layer shape).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that

@@ -49,9 +49,9 @@ def test_noalloc_prefill_matches_prefill_on_two_calls_in_a_row(gpu_lib, dims, le
 
 def test_noalloc_refuses_requests_beyond_its_scratch(gpu_lib):
     d = QWEN35_4B
-    per_token = gdn.gdn_prefill_workspace_size(d, 1000, 1) / 1000.0
-    T = int(gdn.GDN_NOALLOC_SCRATCH_BYTES / per_token) + 64
-    assert gdn.gdn_prefill_workspace_size(d, T, 1) > gdn.GDN_NOALLOC_SCRATCH_BYTES
+    T = 64
+    while gdn.gdn_prefill_workspace_size(d, T, 1) <= gdn.GDN_NOALLOC_SCRATCH_BYTES:
+        T += 64   # the smallest multiple of 64 tokens that no longer fits
     inp = workloads.layer_inputs(d, [T], seed=5, init="zero", num_slots=1)
     run = PrefillRun(inp)
     o_before = run.o.clone()
