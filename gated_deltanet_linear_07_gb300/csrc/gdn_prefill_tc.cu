@@ -170,18 +170,18 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const GdnPrefillArgs 
 struct PrepSmem {
   static constexpr uint32_t KQ = 0;          // 32768  [K;Q] K-major, 128 rows x 128
   static constexpr uint32_t V = 32768;       // 2 x 16384, MN-major (64 rows s x 128 j)
-  static constexpr uint32_t A = 65536;       // 2 x fp32 [64][68]; later BU | BW tiles
-  static constexpr uint32_t AH = 17408;      // bytes per head of A and of T
-  static constexpr uint32_t T = 100352;      // 2 x fp32 [64][68]
-  static constexpr uint32_t R = 135168;      // 2 x fp32 [3][16][16]
-  static constexpr uint32_t GAM = 141312;    // fp32 [2][64], log2 units
-  static constexpr uint32_t BETA = 141824;   // fp32 [2][64]
-  static constexpr uint32_t EG = 142336;     // fp32 [2][64], e^{gamma}
-  static constexpr uint32_t BW2 = 143360;    // [T diag(beta e^gamma)] of both heads, K-major 128 rows x 64
-  static constexpr uint32_t DED = 159744;    // 2 x diag(e^{gamma_C - gamma}), K-major 64 x 64
-  static constexpr uint32_t BAR = 176128;    // 2 mbarriers + tmem address
+  static constexpr uint32_t AT = 65536;      // 2 x fp32 [64][68]: A, then T in place; finally
+                                             // BU_0 | BU_1 | [BW_0; BW_1] bf16 tiles
+  static constexpr uint32_t AH = 17408;      // bytes per head of A / T
+  static constexpr uint32_t R = 100352;      // 2 x fp32 [3][16][16]
+  static constexpr uint32_t GAM = 106496;    // fp32 [2][64], log2 units
+  static constexpr uint32_t BETA = 107008;   // fp32 [2][64]
+  static constexpr uint32_t EG = 107520;     // fp32 [2][64], e^{gamma}
+  static constexpr uint32_t ED = 108032;     // fp32 [2][64], e^{gamma_C - gamma}
+  static constexpr uint32_t BAR = 108544;    // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
   static constexpr int AST = 68;             // fp32 row stride of A and T
+  static constexpr int THREADS = 256;
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, int32_t gc) {
@@ -193,7 +193,9 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, 
   return lo;
 }
 
-__global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
+// Two CTAs per SM: 256 threads, <= 128 registers, ~107 KB shared memory and
+// 256 TMEM columns each, so one CTA's latency-bound phases overlap the other's.
+__global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -213,15 +215,19 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   const bool init = a.has_init ? a.has_init[b] != 0 : false;
   const int cd = a.conv_dim;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int S = PrepSmem::AST;
 
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + PrepSmem::BAR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + PrepSmem::BAR + 16);
   float* gam = reinterpret_cast<float*>(sm + PrepSmem::GAM);
   float* beta = reinterpret_cast<float*>(sm + PrepSmem::BETA);
+  float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
+  float* ed = reinterpret_cast<float*>(sm + PrepSmem::ED);
   const uint32_t s_base = smem_u32(sm);
+  unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
   if (warp == 0) {
-    tmem_alloc(s_tmem, 512);
+    tmem_alloc(s_tmem, 256);
     tmem_relinquish();
   }
   if (tid == 32) {
@@ -230,62 +236,56 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
     fence_mbar_init();
   }
 
-  // ---- front end: conv + SiLU + L2 norm, one warp per (segment, 8 tokens) ----
+  // ---- front end: conv + SiLU + L2 norm; warp = (segment, 16 tokens) ----
   {
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* win =
         reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * cd;
-    const int seg = warp >> 3;          // 0: q | k, 1: v of both value heads
-    const int r0 = (warp & 7) * 8;
+    const int seg = warp >> 2;          // 0: q | k, 1: v of both value heads
+    const int r0 = (warp & 3) * 16;
     const int half = lane >> 4, l16 = lane & 15;
     int ch;
     if (seg == 0) ch = half == 0 ? hk * D + 8 * l16 : a.h_k * D + hk * D + 8 * l16;
     else ch = 2 * a.h_k * D + (2 * hk + half) * D + 8 * l16;
-    float w[8][4];
+    // 19 rows (3-token halo + 16 tokens), loaded unconditionally from valid
+    // addresses so the loads issue back to back; masked rows zeroed after.
+    uint4 xr[19];
+    bool keep[19];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 f = *reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e));
-      w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
-    }
-    // All 11 rows (3-token halo + 8 tokens) are loaded unconditionally from a
-    // valid address so the loads issue back to back; masked rows are zeroed
-    // afterwards.  Rows before the sequence start come from the slot's window.
-    uint4 xr[11];
-    bool keep[11];
-#pragma unroll
-    for (int q = 0; q < 11; ++q) {
-      const int rr = r0 - 3 + q;                  // row within the chunk
-      const int64_t p = (int64_t)c * C + rr;      // position within the sequence
-      const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;  // row 0 of the chunk: always valid
+    for (int q = 0; q < 19; ++q) {
+      const int rr = r0 - 3 + q;
+      const int64_t p = (int64_t)c * C + rr;
+      const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;
       keep[q] = rr < L && (p >= 0 || init);
       if (rr < L && p >= 0) src = x + (size_t)(t0 + rr) * cd + ch;
       else if (rr < L && init) src = win + (size_t)(3 + p) * cd + ch;
       xr[q] = __ldg(reinterpret_cast<const uint4*>(src));
     }
+    float w[8][4];
 #pragma unroll
-    for (int q = 0; q < 11; ++q)
+    for (int e = 0; e < 8; ++e) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e)));
+      w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 19; ++q)
       if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
     const float qscale = rsqrtf((float)D);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const int r = r0 + i;
       float y[8];
-      if (r < L) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+      for (int e = 0; e < 8; ++e) y[e] = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float xv[8];
-          bf16x8_to_float(xr[i + k], xv);
+      for (int k = 0; k < 4; ++k) {
+        float xv[8];
+        bf16x8_to_float(xr[i + k], xv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = fmaf(w[e][k], xv[e], y[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = silu_fast(y[e]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+        for (int e = 0; e < 8; ++e) y[e] = fmaf(w[e][k], xv[e], y[e]);
       }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = r < L ? silu_fast(y[e]) : 0.f;
       if (seg == 0) {
         float ss = 0.f;
 #pragma unroll
@@ -294,21 +294,19 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
         for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const float inv = (r < L ? rsqrtf(ss + a.l2_eps) : 0.f) * (half == 0 ? qscale : 1.0f);
         const int row = half == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
-        uint4 pk = make_uint4(pack_bf16(y[0] * inv, y[1] * inv), pack_bf16(y[2] * inv, y[3] * inv),
-                              pack_bf16(y[4] * inv, y[5] * inv), pack_bf16(y[6] * inv, y[7] * inv));
-        st_shared_v4(s_base + PrepSmem::KQ + kmaj_off(128, row, 8 * l16), pk);
+        st_shared_v4(s_base + PrepSmem::KQ + kmaj_off(128, row, 8 * l16),
+                     make_uint4(pack_bf16(y[0] * inv, y[1] * inv), pack_bf16(y[2] * inv, y[3] * inv),
+                                pack_bf16(y[4] * inv, y[5] * inv), pack_bf16(y[6] * inv, y[7] * inv)));
       } else {
-        uint4 pk = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                              pack_bf16(y[6], y[7]));
-        st_shared_v4(s_base + PrepSmem::V + half * 16384 + mnmaj_off(64, 8 * l16, r), pk);
+        st_shared_v4(s_base + PrepSmem::V + half * 16384 + mnmaj_off(64, 8 * l16, r),
+                     make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                                pack_bf16(y[6], y[7])));
       }
     }
   }
-  // ---- gates of the two value heads (warps 14, 15) ----
-  unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
-  float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
-  if (warp >= 14) {
-    const int g = warp - 14;
+  // ---- gates of the two value heads (warps 6, 7) ----
+  if (warp >= 6) {
+    const int g = warp - 6;
     const int h = 2 * hk + g;
     const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(a.a);
     const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(a.b);
@@ -334,18 +332,21 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
     }
     const float g0 = (inc - pair + gv[0]) * LOG2E, g1 = inc * LOG2E;  // log2 units
     const float glast = __shfl_sync(0xffffffffu, g1, 31);
+    const float e0 = fast_exp2(g0), e1 = fast_exp2(g1);
+    const float d0 = fast_exp2(glast - g0), d1 = fast_exp2(glast - g1);
     gam[g * 64 + 2 * lane] = g0;
     gam[g * 64 + 2 * lane + 1] = g1;
     beta[g * 64 + 2 * lane] = be[0];
     beta[g * 64 + 2 * lane + 1] = be[1];
-    const float e0 = fast_exp2(g0), e1 = fast_exp2(g1);
     eg[g * 64 + 2 * lane] = e0;
     eg[g * 64 + 2 * lane + 1] = e1;
+    ed[g * 64 + 2 * lane] = d0;
+    ed[g * 64 + 2 * lane + 1] = d1;
     float* rec = reinterpret_cast<float*>(vrec0 + g * VH_REC + EXP_OFF);
     rec[2 * lane] = e0;
     rec[2 * lane + 1] = e1;
-    rec[64 + 2 * lane] = fast_exp2(glast - g0);
-    rec[64 + 2 * lane + 1] = fast_exp2(glast - g1);
+    rec[64 + 2 * lane] = d0;
+    rec[64 + 2 * lane + 1] = d1;
     if (lane == 0) rec[128] = fast_exp2(glast);
   }
   fence_async_smem();
@@ -354,49 +355,53 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   if (tid == 0) {
-    for (int ks = 0; ks < 8; ++ks)
+    for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
                sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 64, false, false),
                ks > 0);
     mma_commit(&bar[0]);
   }
-  constexpr int S = PrepSmem::AST;
-  // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); all warps ----
+  // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); warp = (head, lanes) ----
   {
-    const int q = warp & 3, g = (warp >> 2) & 1, sh = warp >> 3;
+    const int q = warp & 3, g = warp >> 2;
     const int m = 32 * q + lane;
-    const bool ok = mbar_spin(&bar[0], 0, SPIN_LIMIT);
+    const bool ok = mbar_wait(&bar[0], 0, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
-    float d[32];
-    if (ok) tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * sh, d);
-    else {
+    float d[64];
+    if (ok) {
+      float t32[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * q) << 16), t32);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) d[e] = 0.f;
+      for (int e = 0; e < 32; ++e) d[e] = t32[e];
+      tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32, t32);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) d[32 + e] = t32[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) d[e] = 0.f;
     }
     const float* gm = gam + g * 64;
     if (m < 64) {
       const int r = m;
-      float* A = reinterpret_cast<float*>(sm + PrepSmem::A + g * PrepSmem::AH);
+      float* A = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
       const float gr = gm[r], br = beta[g * 64 + r];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int s = 32 * sh + e;
-        A[r * S + s] = s < r ? br * fast_exp2(gr - gm[s]) * d[e] : 0.f;
-      }
+      for (int s2 = 0; s2 < 64; ++s2)
+        A[r * S + s2] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[s2] : 0.f;
     } else {
       const int r = m - 64;
       const float gr = gm[r];
       unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
 #pragma unroll
-      for (int ck = 0; ck < 4; ++ck) {
+      for (int ck = 0; ck < 8; ++ck) {
         float pv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int s = 32 * sh + 8 * ck + e;
-          pv[e] = s <= r ? fast_exp2(gr - gm[s]) * d[8 * ck + e] : 0.f;
+          const int s2 = 8 * ck + e;
+          pv[e] = s2 <= r ? fast_exp2(gr - gm[s2]) * d[s2] : 0.f;
         }
-        *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * sh + 8 * ck)) =
+        *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 8 * ck)) =
             make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
                        pack_bf16(pv[6], pv[7]));
       }
@@ -404,41 +409,45 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  // ---- T = (I + A)^-1 per value head: 8 warps per head ----
+  // ---- T = (I + A)^-1 in place, per value head: 4 warps per head ----
+  float tv[4][8];   // this thread's T entries for the B operands (read before they are overwritten)
   {
-    const int g = warp >> 3, gt = tid & 255;
-    const float* A = reinterpret_cast<const float*>(sm + PrepSmem::A + g * PrepSmem::AH);
-    float* T = reinterpret_cast<float*>(sm + PrepSmem::T + g * PrepSmem::AH);
+    const int g = warp >> 2, gt = tid & 127;
+    float* AT = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
     float* Rt = reinterpret_cast<float*>(sm + PrepSmem::R) + g * 768;
-    if (gt < 64) {  // 16x16 diagonal blocks: one column each, forward substitution
-      const int kb = gt >> 4, jj = gt & 15, o = kb * 16;
-      float tc[16];
+    // 16x16 diagonal blocks: one column each by forward substitution (reads
+    // A's block, then writes T's block over it)
+    float tc[16];
+    const int kb = gt >> 4, jj = gt & 15, o = kb * 16;
+    if (gt < 64) {
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         float acc = 0.f;
 #pragma unroll
         for (int ss = 0; ss < rr; ++ss)
-          if (ss >= jj) acc = fmaf(A[(o + rr) * S + o + ss], tc[ss], acc);
+          if (ss >= jj) acc = fmaf(AT[(o + rr) * S + o + ss], tc[ss], acc);
         tc[rr] = rr < jj ? 0.f : (rr == jj ? 1.f : -acc);
       }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) T[(o + rr) * S + o + jj] = tc[rr];
     }
-    named_bar(1 + g, 256);
-    // block rows 1..3: T[bi][bj] = -T[bi][bi] sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj];
-    // each thread owns a 1x4 strip (row rr, columns 4cg..4cg+3) of one block.
-    const int e = gt & 63, rr = e >> 2, cg = e & 3, bj = gt >> 6;
+    named_bar(1 + g, 128);
+    if (gt < 64) {
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) AT[(o + rr) * S + o + jj] = tc[rr];
+    }
+    named_bar(1 + g, 128);
+    // block rows 1..3: T[bi][bj] = -T[bi][bi] sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],
+    // written over A[bi][bj]; a thread owns 1x4 strips (row rr, columns 4cg..).
     for (int bi = 1; bi < 4; ++bi) {
-      const bool act = bj < bi;
-      if (act) {
+      for (int strip = gt; strip < 64 * bi; strip += 128) {
+        const int bj = strip >> 6, e = strip & 63, rr = e >> 2, cg = e & 3;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = A + (16 * bi + rr) * S;
+        const float* arow = AT + (16 * bi + rr) * S;
         for (int bk = bj; bk < bi; ++bk) {
 #pragma unroll
           for (int m2 = 0; m2 < 16; ++m2) {
             const int k = 16 * bk + m2;
             const float av = arow[k];
-            const float4 t4 = *reinterpret_cast<const float4*>(T + k * S + 16 * bj + 4 * cg);
+            const float4 t4 = *reinterpret_cast<const float4*>(AT + k * S + 16 * bj + 4 * cg);
             acc.x = fmaf(av, t4.x, acc.x);
             acc.y = fmaf(av, t4.y, acc.y);
             acc.z = fmaf(av, t4.z, acc.z);
@@ -447,50 +456,47 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
         }
         *reinterpret_cast<float4*>(Rt + bj * 256 + rr * 16 + 4 * cg) = acc;
       }
-      named_bar(1 + g, 256);
-      if (act) {
+      named_bar(1 + g, 128);
+      for (int strip = gt; strip < 64 * bi; strip += 128) {
+        const int bj = strip >> 6, e = strip & 63, rr = e >> 2, cg = e & 3;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* trow = T + (16 * bi + rr) * S + 16 * bi;
+        const float* trow = AT + (16 * bi + rr) * S + 16 * bi;
 #pragma unroll
         for (int m2 = 0; m2 < 16; ++m2) {
-          const float tv = trow[m2];
+          const float t1 = trow[m2];
           const float4 r4 = *reinterpret_cast<const float4*>(Rt + bj * 256 + m2 * 16 + 4 * cg);
-          acc.x = fmaf(tv, r4.x, acc.x);
-          acc.y = fmaf(tv, r4.y, acc.y);
-          acc.z = fmaf(tv, r4.z, acc.z);
-          acc.w = fmaf(tv, r4.w, acc.w);
+          acc.x = fmaf(t1, r4.x, acc.x);
+          acc.y = fmaf(t1, r4.y, acc.y);
+          acc.z = fmaf(t1, r4.z, acc.z);
+          acc.w = fmaf(t1, r4.w, acc.w);
         }
-        *reinterpret_cast<float4*>(T + (16 * bi + rr) * S + 16 * bj + 4 * cg) =
+        *reinterpret_cast<float4*>(AT + (16 * bi + rr) * S + 16 * bj + 4 * cg) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
-      named_bar(1 + g, 256);
+      named_bar(1 + g, 128);
     }
-    // B operands: (T diag(beta)) of this head over its A (no longer read),
-    // (T diag(beta e^gamma)) into rows 64g.. of the stacked tile, and the
-    // diagonal tile diag(e^{gamma_C - gamma}).
-    const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH;
-    const uint32_t bw = s_base + PrepSmem::BW2 + 8192 * g;
-    const uint32_t ded = s_base + PrepSmem::DED + 8192 * g;
-    float tv[2][8];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int chunk = gt + 256 * q;
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = gt + 128 * q;
       const int r = chunk >> 3, s0 = 8 * (chunk & 7);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? T[r * S + s0 + k] : 0.f;
+      for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? AT[r * S + s0 + k] : 0.f;
     }
-    const float glast = gam[g * 64 + 63];
+  }
+  __syncthreads();  // both heads' T read: the B-operand tiles overwrite the whole region
+  {
+    const int g = warp >> 2, gt = tid & 127;
+    const uint32_t bu = s_base + PrepSmem::AT + 8192 * g;
+    const uint32_t bw = s_base + PrepSmem::AT + 16384 + 8192 * g;  // rows 64g.. of [BW_0; BW_1]
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int chunk = gt + 256 * q;
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = gt + 128 * q;
       const int r = chunk >> 3, s0 = 8 * (chunk & 7);
-      float vu[8], vw[8], vd[8];
+      float vu[8], vw[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int sc = s0 + k;
-        vu[k] = tv[q][k] * beta[g * 64 + sc];
-        vw[k] = vu[k] * eg[g * 64 + sc];
-        vd[k] = sc == r ? fast_exp2(glast - gam[g * 64 + sc]) : 0.f;
+        vu[k] = tv[q][k] * beta[g * 64 + s0 + k];
+        vw[k] = vu[k] * eg[g * 64 + s0 + k];
       }
       st_shared_v4(bu + kmaj_off(64, r, s0),
                    make_uint4(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]),
@@ -498,9 +504,6 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       st_shared_v4(bw + kmaj_off(64, r, s0),
                    make_uint4(pack_bf16(vw[0], vw[1]), pack_bf16(vw[2], vw[3]),
                               pack_bf16(vw[4], vw[5]), pack_bf16(vw[6], vw[7])));
-      st_shared_v4(ded + kmaj_off(64, r, s0),
-                   make_uint4(pack_bf16(vd[0], vd[1]), pack_bf16(vd[2], vd[3]),
-                              pack_bf16(vd[4], vd[5]), pack_bf16(vd[6], vd[7])));
     }
   }
   fence_async_smem();
@@ -509,18 +512,13 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   tc_fence_after();
   if (tid == 0) {
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const uint32_t bu = s_base + PrepSmem::A + g * PrepSmem::AH;
+    for (int g = 0; g < 2; ++g)
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
-                 sdesc_kmaj(bu, 64, ks), idesc_bf16(128, 64, true, false), ks > 0);
-      for (int ks = 0; ks < 4; ++ks)  // K~^T_g = K^T diag(e^{gamma_C-gamma}) -> [256+64g, +64)
-        mma_bf16(tmem + 256 + 64 * g, sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks),
-                 sdesc_kmaj(s_base + PrepSmem::DED + 8192 * g, 64, ks),
+                 sdesc_kmaj(s_base + PrepSmem::AT + 8192 * g, 64, ks),
                  idesc_bf16(128, 64, true, false), ks > 0);
-    }
     for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
-      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BW2, 128, ks),
+      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::AT + 16384, 128, ks),
                sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 128, false, true),
                ks > 0);
     mma_commit(&bar[1]);
@@ -530,17 +528,34 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
     bulk_s2g(qrec, s_base + PrepSmem::KQ + 8192, 8192);
     bulk_s2g(qrec + 8192, s_base + PrepSmem::KQ + 16384 + 8192, 8192);
   }
-  // ---- U^T, [Wk_0; Wk_1] and K~^T from TMEM to the workspace ----
+  // K~^T_g[i][s] = K[s][i] e^{gamma_C - gamma_s} (fp32 factor), row i per thread
   {
-    const bool ok = mbar_spin(&bar[1], 0, SPIN_LIMIT);
+    const int g = tid >> 7, i = tid & 127;
+    const __nv_bfloat16* kq = reinterpret_cast<const __nv_bfloat16*>(sm + PrepSmem::KQ);
+    unsigned char* dst = vrec0 + g * VH_REC + KT_OFF;
+#pragma unroll
+    for (int ck = 0; ck < 8; ++ck) {
+      float kv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int s2 = 8 * ck + e;
+        kv[e] = __bfloat162float(kq[kmaj_off(128, s2, i) >> 1]) * ed[g * 64 + s2];
+      }
+      *reinterpret_cast<uint4*>(dst + kmaj_off(128, i, 8 * ck)) =
+          make_uint4(pack_bf16(kv[0], kv[1]), pack_bf16(kv[2], kv[3]), pack_bf16(kv[4], kv[5]),
+                     pack_bf16(kv[6], kv[7]));
+    }
+  }
+  // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
+  {
+    const bool ok = mbar_wait(&bar[1], 0, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
-    // 24 tasks of (lane quarter, 64 columns); warp w takes tasks w and w+16,
-    // whose lane quarter matches its own (TMEM lane access rule).
-    for (int task = warp; task < 24 && ok; task += 16) {
-      const int kind = task >> 2;                // 0,1: U^T_g  2,3: Wk halves  4,5: K~^T_g
-      const uint32_t col = kind < 2 ? 64 * kind : (kind < 4 ? 128 + 64 * (kind - 2) : 256 + 64 * (kind - 4));
+    // 16 tasks of (lane quarter, 64 columns); warp w takes tasks w and w+8.
+    for (int task = warp; task < 16 && ok; task += 8) {
+      const int kind = task >> 2;                // 0,1: U^T_g   2,3: Wk column halves
+      const uint32_t col = 64 * kind;
       float v[2][32];
       tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col, v[0]);
       tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32, v[1]);
@@ -548,19 +563,17 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
       int row, R, c0;
       if (kind < 2) {            // U^T_g row j = m
         dst = vrec0 + kind * VH_REC + UT_OFF; row = m; R = 128; c0 = 0;
-      } else if (kind < 4) {     // Wk of head m/64, row r = m%64, columns i in this half
+      } else {                   // Wk of head m/64, row r = m%64, columns i in this half
         dst = vrec0 + (m >> 6) * VH_REC + WK_OFF; row = m & 63; R = 64; c0 = 64 * (kind - 2);
-      } else {                   // K~^T_g row i = m
-        dst = vrec0 + (kind - 4) * VH_REC + KT_OFF; row = m; R = 128; c0 = 0;
       }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
           const float* f = &v[h2][8 * ck];
-          uint4 pk = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-          *reinterpret_cast<uint4*>(dst + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck)) = pk;
+          *reinterpret_cast<uint4*>(dst + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck)) =
+              make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                         pack_bf16(f[6], f[7]));
         }
       }
     }
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(512, 1) prep_kernel(const GdnPrefillArgs a) {
   tc_fence_before();
   __syncthreads();
   if (tid == 32) bulk_wait_all();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -834,7 +847,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
     const int smem = (int)PrepSmem::SIZE + 1024;
     e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    prep_kernel<<<dim3((unsigned)a.max_chunks, a.h_k), 512, smem, s>>>(a);
+    prep_kernel<<<dim3((unsigned)a.max_chunks, a.h_k), PrepSmem::THREADS, smem, s>>>(a);
     gdn_trace_count(tr, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
