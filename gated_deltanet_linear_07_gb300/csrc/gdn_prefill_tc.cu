@@ -41,16 +41,16 @@ using namespace gdn::tc;
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // d_k = d_v
 constexpr uint32_t KQ_BYTES = 128 * 128 * 2;  // [K;Q] tile in the prep, K-major, 128 rows
-constexpr uint32_t Q_REC = 64 * 128 * 2;      // per (chunk, key head): Q tile, K-major, 64 rows
+constexpr uint32_t Q_REC = 2 * 64 * 128 * 2;  // per (chunk, key head): Q tile | K tile, K-major, 64 rows each
+constexpr uint32_t K_IN_QREC = 64 * 128 * 2;
 // Record of one (chunk, value head), every tile a ready shared-memory image:
 //   P    [r][s]  K-major, 64 rows            8 KiB
-//   KT   [i][s]  K-major, 128 rows  (K diag(e^{gamma_C - gamma}))^T   16 KiB
 //   UT   [j][r]  K-major, 128 rows           16 KiB
 //   EXP  e^{gamma_r} [64], e^{gamma_C - gamma_r} [64], e^{gamma_C}     1 KiB
 //   WK   [r][i]  K-major, 64 rows (two 8 KiB K-blocks)                16 KiB
-constexpr uint32_t P_OFF = 0, KT_OFF = 8192, UT_OFF = 24576, EXP_OFF = 40960, WK_OFF = 41984;
-constexpr uint32_t VH_REC = 58368;           // per (chunk, value head)
-constexpr uint32_t VH_HEAD = 41984;          // P | KT | UT | EXP, copied in one piece
+constexpr uint32_t P_OFF = 0, UT_OFF = 8192, EXP_OFF = 24576, WK_OFF = 25600;
+constexpr uint32_t VH_REC = 41984;           // per (chunk, value head)
+constexpr uint32_t VH_HEAD = 25600;          // P | UT | EXP, copied in one piece
 constexpr uint32_t WAIT_LIMIT = 1u << 22;   // suspending try_wait iterations
 constexpr uint32_t SPIN_LIMIT = 1u << 26;   // non-blocking test_wait iterations
 constexpr float LOG2E = 1.4426950408889634f;
@@ -177,8 +177,7 @@ struct PrepSmem {
   static constexpr uint32_t GAM = 106496;    // fp32 [2][64], log2 units
   static constexpr uint32_t BETA = 107008;   // fp32 [2][64]
   static constexpr uint32_t EG = 107520;     // fp32 [2][64], e^{gamma}
-  static constexpr uint32_t ED = 108032;     // fp32 [2][64], e^{gamma_C - gamma}
-  static constexpr uint32_t BAR = 108544;    // 2 mbarriers + tmem address
+  static constexpr uint32_t BAR = 108032;    // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
   static constexpr int AST = 68;             // fp32 row stride of A and T
   static constexpr int THREADS = 256;
@@ -222,7 +221,6 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   float* gam = reinterpret_cast<float*>(sm + PrepSmem::GAM);
   float* beta = reinterpret_cast<float*>(sm + PrepSmem::BETA);
   float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
-  float* ed = reinterpret_cast<float*>(sm + PrepSmem::ED);
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
@@ -271,21 +269,26 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
     for (int q = 0; q < 19; ++q)
       if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
     const float qscale = rsqrtf((float)D);
+    float xf[4][8];   // rolling window of the last four rows, converted once each
+#pragma unroll
+    for (int q = 0; q < 3; ++q) bf16x8_to_float(xr[q], xf[q + 1]);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int r = r0 + i;
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xf[q][e] = xf[q + 1][e];
+      bf16x8_to_float(xr[i + 3], xf[3]);
       float y[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float xv[8];
-        bf16x8_to_float(xr[i + k], xv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = fmaf(w[e][k], xv[e], y[e]);
+      for (int e = 0; e < 8; ++e) {
+        float z = w[e][0] * xf[0][e];
+        z = fmaf(w[e][1], xf[1][e], z);
+        z = fmaf(w[e][2], xf[2][e], z);
+        z = fmaf(w[e][3], xf[3][e], z);
+        y[e] = r < L ? silu_fast(z) : 0.f;
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = r < L ? silu_fast(y[e]) : 0.f;
       if (seg == 0) {
         float ss = 0.f;
 #pragma unroll
@@ -340,8 +343,6 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
     beta[g * 64 + 2 * lane + 1] = be[1];
     eg[g * 64 + 2 * lane] = e0;
     eg[g * 64 + 2 * lane + 1] = e1;
-    ed[g * 64 + 2 * lane] = d0;
-    ed[g * 64 + 2 * lane + 1] = d1;
     float* rec = reinterpret_cast<float*>(vrec0 + g * VH_REC + EXP_OFF);
     rec[2 * lane] = e0;
     rec[2 * lane + 1] = e1;
@@ -523,28 +524,12 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
                ks > 0);
     mma_commit(&bar[1]);
   }
-  if (tid == 32) {  // the Q rows of the [K;Q] tile (already a tile image) to the workspace
+  if (tid == 32) {  // Q rows then K rows of the [K;Q] tile (tile images) to the workspace
     unsigned char* qrec = a.kq_ws + ((size_t)gc * a.h_k + hk) * Q_REC;
     bulk_s2g(qrec, s_base + PrepSmem::KQ + 8192, 8192);
     bulk_s2g(qrec + 8192, s_base + PrepSmem::KQ + 16384 + 8192, 8192);
-  }
-  // K~^T_g[i][s] = K[s][i] e^{gamma_C - gamma_s} (fp32 factor), row i per thread
-  {
-    const int g = tid >> 7, i = tid & 127;
-    const __nv_bfloat16* kq = reinterpret_cast<const __nv_bfloat16*>(sm + PrepSmem::KQ);
-    unsigned char* dst = vrec0 + g * VH_REC + KT_OFF;
-#pragma unroll
-    for (int ck = 0; ck < 8; ++ck) {
-      float kv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s2 = 8 * ck + e;
-        kv[e] = __bfloat162float(kq[kmaj_off(128, s2, i) >> 1]) * ed[g * 64 + s2];
-      }
-      *reinterpret_cast<uint4*>(dst + kmaj_off(128, i, 8 * ck)) =
-          make_uint4(pack_bf16(kv[0], kv[1]), pack_bf16(kv[2], kv[3]), pack_bf16(kv[4], kv[5]),
-                     pack_bf16(kv[6], kv[7]));
-    }
+    bulk_s2g(qrec + K_IN_QREC, s_base + PrepSmem::KQ, 8192);
+    bulk_s2g(qrec + K_IN_QREC + 8192, s_base + PrepSmem::KQ + 16384, 8192);
   }
   // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
   {
@@ -587,24 +572,26 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
 // ---------------------------------------------------------------------------
 // scan: one CTA (576 threads) per (sequence, value head).
 //   warp 0: bulk loads of chunk inputs (two buffers)
-//   warp 1: MMA issue, two groups per chunk:
-//             [X | O1]  = H^T [Wk; Q]^T      (N = 128, TMEM double-buffered)
-//             [O2 | dH] = W^T [P; K~^T]^T    (N = 192)
+//   warp 1: MMA issue, three groups per chunk:
+//             [X | O1] = H^T [Wk; Q]^T       (N = 128, TMEM double-buffered)
+//             dH       = Wt^T K              (N = 128; Wt = diag(e^{gamma_C-gamma}) W)
+//             O2       = W^T P^T             (N = 64)
 //   warps 2..17: epilogue; warp w owns TMEM lanes 32*(w%4).., and group
 //               (w-2)/4 takes one quarter of the columns.
 
 struct ScanSmem {
-  // per buffer: B2 = [P; K~^T] (K-major, 192 rows x 64) | UT | EXP | B1 = [Wk; Q] (K-major 128 x 128)
+  // per buffer: P (K-major 64 x 64) | UT | EXP | K (K-major 64 x 128, used MN-major) |
+  //             B1 = [Wk; Q] (K-major 128 x 128)
   static constexpr uint32_t BUF = 74752;
-  static constexpr uint32_t B_B2 = 0, B_UT = 24576, B_EXP = 40960, B_B1 = 41984;
+  static constexpr uint32_t B_P = 0, B_UT = 8192, B_EXP = 24576, B_K = 25600, B_B1 = 41984;
   static constexpr uint32_t HT = 2 * BUF;     // 32768, K-major 128 x 128
-  static constexpr uint32_t WT = HT + 32768;  // 16384, K-major 128 x 64
-  static constexpr uint32_t OST = WT + 16384; // 16384, output staging [r][j] bf16
-  static constexpr uint32_t BAR = OST + 16384;
+  static constexpr uint32_t WT = HT + 32768;  // 16384, K-major 128 x 64: W^T
+  static constexpr uint32_t WTT = WT + 16384; // 16384: W^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t BAR = WTT + 16384;
   static constexpr uint32_t SIZE = BAR + 256;
 };
-// TMEM columns: [X | O1] x 2 buffers, then [O2 | dH]
-constexpr uint32_t TXO = 0, TOD = 256;
+// TMEM columns: [X | O1] x 2 buffers, dH, O2
+constexpr uint32_t TXO = 0, TDH = 256, TO2 = 384;
 constexpr int SCAN_THREADS = 576;
 constexpr uint32_t EPI_THREADS = 512;
 
@@ -633,8 +620,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   uint64_t* bar_dh = full + 5;
   uint64_t* wready = full + 6;
   uint64_t* hready = full + 7;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 8);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(full + 9);
+  uint64_t* bar_o = full + 8;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 9);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(full + 10);
 
   if (warp == 0) {
     tmem_alloc(s_tmem, 512);
@@ -643,10 +631,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   if (tid == 32) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    mbar_init(&empty[0], 1);
-    mbar_init(&empty[1], 1);
+    // a buffer is free once its MMAs are done and every epilogue warp has
+    // finished staging its output in the buffer's (consumed) U tile
+    mbar_init(&empty[0], 1 + EPI_THREADS / 32);
+    mbar_init(&empty[1], 1 + EPI_THREADS / 32);
     mbar_init(bar_x, 1);
     mbar_init(bar_dh, 1);
+    mbar_init(bar_o, 1);
     mbar_init(wready, EPI_THREADS);
     mbar_init(hready, EPI_THREADS);
     *s_abort = 0;
@@ -674,7 +665,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         const unsigned char* vrec = a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC;
         const unsigned char* qrec = a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * Q_REC;
         mbar_expect_tx(&full[s], ScanSmem::BUF);
-        bulk_g2s(dst, vrec, VH_HEAD, &full[s]);                                   // P|KT|UT|EXP
+        bulk_g2s(dst, vrec, VH_HEAD, &full[s]);                                   // P|UT|EXP
+        bulk_g2s(dst + ScanSmem::B_K, qrec + K_IN_QREC, K_IN_QREC, &full[s]);      // K
         bulk_g2s(dst + ScanSmem::B_B1, vrec + WK_OFF, 8192, &full[s]);             // Wk K-block 0
         bulk_g2s(dst + ScanSmem::B_B1 + 16384, vrec + WK_OFF + 8192, 8192, &full[s]);  // block 1
         bulk_g2s(dst + ScanSmem::B_B1 + 8192, qrec, 8192, &full[s]);               // Q K-block 0
@@ -685,14 +677,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t ID_XO = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_OD = idesc_bf16(128, 192, false, false);
+      constexpr uint32_t ID_DH = idesc_bf16(128, 128, false, true);
+      constexpr uint32_t ID_O2 = idesc_bf16(128, 64, false, false);
       const uint64_t d_ht = sdesc_kmaj(s_base + ScanSmem::HT, 128, 0);
       const uint64_t d_wt = sdesc_kmaj(s_base + ScanSmem::WT, 128, 0);
+      const uint64_t d_wtt = sdesc_kmaj(s_base + ScanSmem::WTT, 128, 0);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t buf = s_base + s * ScanSmem::BUF;
         const uint64_t d_b1 = sdesc_kmaj(buf + ScanSmem::B_B1, 128, 0);
-        const uint64_t d_b2 = sdesc_kmaj(buf + ScanSmem::B_B2, 192, 0);
+        const uint64_t d_k = sdesc_mnmaj(buf + ScanSmem::B_K, 64, 0);
+        const uint64_t d_p = sdesc_kmaj(buf + ScanSmem::B_P, 64, 0);
         if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) ||
             !mbar_wait(hready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
@@ -704,9 +699,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         if (!mbar_wait(wready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // [O2 | dH] = W^T [P; K~^T]^T
-          mma_bf16(tmem + TOD, sdesc_add(d_wt, ks * 32), sdesc_add(d_b2, ks * 32), ID_OD, ks > 0);
+        for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
+          mma_bf16(tmem + TDH, sdesc_add(d_wtt, ks * 32), sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
         mma_commit(bar_dh);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
+          mma_bf16(tmem + TO2, sdesc_add(d_wt, ks * 32), sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
+        mma_commit(bar_o);
         mma_commit(&empty[s]);
       }
     }
@@ -719,9 +718,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       H[i] = init ? gstate[(size_t)(32 * grp + i) * D + j] : 0.f;
+    // Shared-memory addresses of this thread's rows, fixed for the whole scan.
+    uint32_t a_ut[2], a_wt[2], a_ht[4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      a_ut[q] = ScanSmem::B_UT + kmaj_off(128, j, 16 * grp + 8 * q);   // + buffer base
+      a_wt[q] = s_base + ScanSmem::WT + kmaj_off(128, j, 16 * grp + 8 * q);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a_ht[q] = s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q);
+    constexpr uint32_t WTT_OFF = ScanSmem::WTT - ScanSmem::WT;
+    // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
+    const size_t o_lane = ((size_t)(16 * grp + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) + 8 * (lane & 3);
+    const size_t o_row = (size_t)a.h_v * D;   // elements between consecutive tokens
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      st_shared_v4(s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q),
+      st_shared_v4(a_ht[q],
                    make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
                               pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                               pack_bf16(H[8 * q + 6], H[8 * q + 7])));
@@ -742,7 +754,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       }
       tc_fence_after();
       // W^T = U^T - X for r in this group's quarter
-      float eg[16];
       const float dec = ex[128];
       {
         float X[16];
@@ -751,17 +762,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         for (int q = 0; q < 2; ++q) {
           const int r0 = 16 * grp + 8 * q;
           float u[8];
-          bf16x8_to_float(ld_shared_v4(buf + ScanSmem::B_UT + kmaj_off(128, j, r0)), u);
-          const float4 e0 = *reinterpret_cast<const float4*>(ex + r0);
-          const float4 e1 = *reinterpret_cast<const float4*>(ex + r0 + 4);
-          eg[8 * q + 0] = e0.x; eg[8 * q + 1] = e0.y; eg[8 * q + 2] = e0.z; eg[8 * q + 3] = e0.w;
-          eg[8 * q + 4] = e1.x; eg[8 * q + 5] = e1.y; eg[8 * q + 6] = e1.z; eg[8 * q + 7] = e1.w;
-          float wv[8];
+          bf16x8_to_float(ld_shared_v4(buf + a_ut[q]), u);
+          const float4 d0 = *reinterpret_cast<const float4*>(ex + 64 + r0);
+          const float4 d1 = *reinterpret_cast<const float4*>(ex + 64 + r0 + 4);
+          const float edv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          float wv[8], wt[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) wv[e] = u[e] - X[8 * q + e];
-          st_shared_v4(s_base + ScanSmem::WT + kmaj_off(128, j, r0),
+          for (int e = 0; e < 8; ++e) {
+            wv[e] = u[e] - X[8 * q + e];
+            wt[e] = wv[e] * edv[e];
+          }
+          st_shared_v4(a_wt[q],
                        make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
                                   pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7])));
+          st_shared_v4(a_wt[q] + WTT_OFF,
+                       make_uint4(pack_bf16(wt[0], wt[1]), pack_bf16(wt[2], wt[3]),
+                                  pack_bf16(wt[4], wt[5]), pack_bf16(wt[6], wt[7])));
         }
       }
       fence_async_smem();
@@ -772,13 +788,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
       {
         float dH[32];
-        tmem_ld32(tmem + lbase + TOD + 64 + 32 * grp, dH);
+        tmem_ld32(tmem + lbase + TDH + 32 * grp, dH);
 #pragma unroll
         for (int e = 0; e < 32; ++e) H[e] = fmaf(dec, H[e], dH[e]);
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        st_shared_v4(s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q),
+        st_shared_v4(a_ht[q],
                      make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
                                 pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                                 pack_bf16(H[8 * q + 6], H[8 * q + 7])));
@@ -786,30 +802,34 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       tc_fence_before();
       // o = e^{gamma} O1 + O2 (read before arriving, so the next chunk's MMAs
       // cannot overwrite O2 / this buffer's O1 while they are read)
+      if (!mbar_wait(bar_o, c & 1, WAIT_LIMIT)) { fail(); break; }
+      tc_fence_after();
       float O1[16], O2[16];
       tmem_ld16(txo + 64 + 16 * grp, O1);
-      tmem_ld16(tmem + lbase + TOD + 16 * grp, O2);
+      tmem_ld16(tmem + lbase + TO2 + 16 * grp, O2);
       tc_fence_before();
       mbar_arrive(hready);
-      // Stage this warp's 16 x 32 block of o in its own 1 KiB of shared
-      // memory, then write it as 16-byte pieces (8 values of one row each).
-      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + ScanSmem::OST + (warp - 2) * 1024);
+      // Stage this warp's 16 x 32 block of o in its own 1 KiB of the buffer's
+      // U tile (read in the W phase, free now), then write it as 16-byte
+      // pieces (8 values of one row each).
+      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + s * ScanSmem::BUF + ScanSmem::B_UT +
+                                                            (warp - 2) * 1024);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) ost[e * 32 + lane] = __float2bfloat16_rn(fmaf(eg[e], O1[e], O2[e]));
+      for (int e = 0; e < 16; ++e)   // e^{gamma_r}: the buffer is still ours (released after staging)
+        ost[e * 32 + lane] = __float2bfloat16_rn(fmaf(ex[16 * grp + e], O1[e], O2[e]));
       __syncwarp();
       {
-        const int64_t t0 = start + (int64_t)c * C;
+        __nv_bfloat16* ob = out + (size_t)(start + (int64_t)c * C) * o_row + o_lane;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int piece = lane + 32 * q;       // 16 rows x 4 pieces
-          const int e = piece >> 2, k = piece & 3;
-          const int r = 16 * grp + e;
-          if (r < L)
-            *reinterpret_cast<uint4*>(out + ((size_t)(t0 + r) * a.h_v + h) * D + 32 * (warp & 3) + 8 * k) =
-                *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * k);
+        for (int q = 0; q < 2; ++q) {            // rows e = lane/4 and lane/4 + 8
+          const int e = (lane >> 2) + 8 * q;
+          if (16 * grp + e < L)
+            *reinterpret_cast<uint4*>(ob + (size_t)(8 * q) * o_row) =
+                *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * (lane & 3));
         }
       }
-      __syncwarp();  // staging reusable by the next chunk
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with buffer s
     }
     if (!*s_abort) {
 #pragma unroll
