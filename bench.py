@@ -462,6 +462,10 @@ def run_gdn(args):
                    "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
                    "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
     stage = pf["stage_ms"]
+    if "scan" in stage and "chunk" not in stage:
+        # Overlapped launch: the chunk work runs beside the scan inside the
+        # scan stage's interval, so that interval carries both FLOP shares.
+        stage_flops["scan"] += stage_flops["chunk"]
     dom = max(stage, key=stage.get) if stage else None
     peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     roof = None
@@ -471,7 +475,9 @@ def run_gdn(args):
         roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": ach / peak_tf, "traffic": recorded_traffic("prefill_" + dom),
                 "kernel": {"chunk": "prep_kernel (prefill stage 'chunk')",
-                           "scan": "scan_kernel (prefill stage 'scan')"}.get(dom, dom),
+                           "scan": ("scan_kernel (prefill stage 'scan')" if "chunk" in stage else
+                                   "prep_persistent_kernel + scan_kernel, overlapped "
+                                   "(prefill stage 'scan')")}.get(dom, dom),
                 "peak_source": f"bf16_tflops ({peak_src})",
                 "launch_ms": dom_ms, "flops_per_launch": stage_flops[dom]}
     stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()

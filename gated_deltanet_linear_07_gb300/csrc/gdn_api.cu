@@ -54,7 +54,7 @@ struct PrefillLayout {
   // SIMT path
   size_t flag, q, k, v, g, beta;
   // tensor-core path
-  size_t chunk_off, kq, vh;
+  size_t chunk_off, ready, kq, vh;
   int64_t max_chunks;
   size_t total;
 };
@@ -67,6 +67,7 @@ PrefillLayout prefill_layout(const gdn_dims* d, int64_t T, int64_t B) {
   if (use_tc(d)) {
     L.max_chunks = (T + d->chunk - 1) / d->chunk + B;
     L.chunk_off = o; o += align_up((size_t)(B + 1) * sizeof(int32_t));
+    L.ready = o; o += align_up((size_t)L.max_chunks * d->h_k * sizeof(int32_t));
     o = (o + 1023) / 1024 * 1024;
     L.kq = o; o += (size_t)L.max_chunks * d->h_k * gdn_tc_kq_bytes();
     L.vh = o; o += (size_t)L.max_chunks * d->h_v * gdn_tc_vh_bytes();
@@ -175,6 +176,8 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   p.ws_beta = reinterpret_cast<float*>(ws + L.beta);
   if (use_tc(dims)) {
     p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
+    p.chunk_ready = reinterpret_cast<int32_t*>(ws + L.ready);
+    p.work_counter = reinterpret_cast<int32_t*>(ws + L.flag + 64);
     p.max_chunks = L.max_chunks;
     p.kq_ws = reinterpret_cast<uint8_t*>(ws + L.kq);
     p.vh_ws = reinterpret_cast<uint8_t*>(ws + L.vh);

@@ -53,6 +53,7 @@ constexpr uint32_t VH_REC = 41984;           // per (chunk, value head)
 constexpr uint32_t VH_HEAD = 25600;          // P | UT | EXP, copied in one piece
 constexpr uint32_t WAIT_LIMIT = 1u << 22;   // suspending try_wait iterations
 constexpr uint32_t SPIN_LIMIT = 1u << 26;   // non-blocking test_wait iterations
+constexpr uint32_t FLAG_LIMIT = 1u << 25;   // polls of a global ready flag (64 ns apart)
 constexpr float LOG2E = 1.4426950408889634f;
 
 __device__ __forceinline__ float silu_fast(float z) {
@@ -122,6 +123,18 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Order this thread's async-proxy global accesses with its generic ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // ---------------------------------------------------------------------------
 // chunk table: chunk_off[b] = sum_{b'<b} ceil(len_b' / C); one CTA.
@@ -162,6 +175,9 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const GdnPrefillArgs 
     run += (a.cu_seqlens[b + 1] - a.cu_seqlens[b] + C - 1) / C;
   }
   if (tid == 1023) a.chunk_off[B] = run;
+  // per-(chunk, key head) ready flags and the prep work counter start at zero
+  for (int64_t i = tid; i < a.max_chunks * a.h_k; i += 1024) a.chunk_ready[i] = 0;
+  if (tid == 0) *a.work_counter = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -194,18 +210,13 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, 
 
 // Two CTAs per SM: 256 threads, <= 128 registers, ~107 KB shared memory and
 // 256 TMEM columns each, so one CTA's latency-bound phases overlap the other's.
-__global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  if (!a.ws_flag[0]) return;
-  const int32_t gc = blockIdx.x;
-  const int hk = blockIdx.y;
-  const int32_t nch = a.chunk_off[a.num_seqs];
-  if (gc >= nch) return;
-  const int b = find_seq(a.chunk_off, a.num_seqs, gc);
-  const int slot = a.slot_idx[b];
-  if (slot < 0 || slot >= a.num_slots) return;  // the scan reports it
+// One (chunk, key head) work item, run by a group of 256 threads (thread
+// index tid) on its own shared memory `sm`, its own two mbarriers (completing
+// once per item; parity ph) and 256 TMEM columns from `tmem`.  Named barrier
+// nb spans the group, nb+1 and nb+2 its two 128-thread halves.
+__device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
+                                          int slot, unsigned char* sm, int tid, int nb,
+                                          uint64_t* bar, uint32_t ph, uint32_t tmem) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -213,26 +224,13 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
   const bool init = a.has_init ? a.has_init[b] != 0 : false;
   const int cd = a.conv_dim;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int warp = tid >> 5, lane = tid & 31;
   constexpr int S = PrepSmem::AST;
-
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + PrepSmem::BAR);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + PrepSmem::BAR + 16);
   float* gam = reinterpret_cast<float*>(sm + PrepSmem::GAM);
   float* beta = reinterpret_cast<float*>(sm + PrepSmem::BETA);
   float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
-
-  if (warp == 0) {
-    tmem_alloc(s_tmem, 256);
-    tmem_relinquish();
-  }
-  if (tid == 32) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
 
   // ---- front end: conv + SiLU + L2 norm; warp = (segment, 16 tokens) ----
   {
@@ -245,13 +243,23 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
     int ch;
     if (seg == 0) ch = half == 0 ? hk * D + 8 * l16 : a.h_k * D + hk * D + 8 * l16;
     else ch = 2 * a.h_k * D + (2 * hk + half) * D + 8 * l16;
-    // 19 rows (3-token halo + 16 tokens), loaded unconditionally from valid
-    // addresses so the loads issue back to back; masked rows zeroed after.
-    uint4 xr[19];
-    bool keep[19];
+    float w[8][4];
 #pragma unroll
-    for (int q = 0; q < 19; ++q) {
-      const int rr = r0 - 3 + q;
+    for (int e = 0; e < 8; ++e) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e)));
+      w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
+    }
+    const float qscale = rsqrtf((float)D);
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+    const int rb = r0 + 8 * hh;
+    // 11 rows (3-token halo + 8 tokens), loaded unconditionally from valid
+    // addresses so the loads issue back to back; masked rows zeroed after.
+    uint4 xr[11];
+    bool keep[11];
+#pragma unroll
+    for (int q = 0; q < 11; ++q) {
+      const int rr = rb - 3 + q;
       const int64_t p = (int64_t)c * C + rr;
       const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;
       keep[q] = rr < L && (p >= 0 || init);
@@ -259,22 +267,15 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
       else if (rr < L && init) src = win + (size_t)(3 + p) * cd + ch;
       xr[q] = __ldg(reinterpret_cast<const uint4*>(src));
     }
-    float w[8][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e)));
-      w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
-    }
-#pragma unroll
-    for (int q = 0; q < 19; ++q)
+    for (int q = 0; q < 11; ++q)
       if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
-    const float qscale = rsqrtf((float)D);
     float xf[4][8];   // rolling window of the last four rows, converted once each
 #pragma unroll
     for (int q = 0; q < 3; ++q) bf16x8_to_float(xr[q], xf[q + 1]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int r = r0 + i;
+    for (int i = 0; i < 8; ++i) {
+      const int r = rb + i;
 #pragma unroll
       for (int q = 0; q < 3; ++q)
 #pragma unroll
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
                      make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
                                 pack_bf16(y[6], y[7])));
       }
+    }
     }
   }
   // ---- gates of the two value heads (warps 6, 7) ----
@@ -352,9 +354,8 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   }
   fence_async_smem();
   tc_fence_before();
-  __syncthreads();
+  named_bar(nb, 256);
   tc_fence_after();
-  const uint32_t tmem = *s_tmem;
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   {
     const int q = warp & 3, g = warp >> 2;
     const int m = 32 * q + lane;
-    const bool ok = mbar_wait(&bar[0], 0, WAIT_LIMIT);
+    const bool ok = mbar_wait(&bar[0], ph, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     float d[64];
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
     }
   }
   tc_fence_before();
-  __syncthreads();
+  named_bar(nb, 256);
   // ---- T = (I + A)^-1 in place, per value head: 4 warps per head ----
   float tv[4][8];   // this thread's T entries for the B operands (read before they are overwritten)
   {
@@ -430,12 +431,12 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
         tc[rr] = rr < jj ? 0.f : (rr == jj ? 1.f : -acc);
       }
     }
-    named_bar(1 + g, 128);
+    named_bar(nb + 1 + g, 128);
     if (gt < 64) {
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) AT[(o + rr) * S + o + jj] = tc[rr];
     }
-    named_bar(1 + g, 128);
+    named_bar(nb + 1 + g, 128);
     // block rows 1..3: T[bi][bj] = -T[bi][bi] sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],
     // written over A[bi][bj]; a thread owns 1x4 strips (row rr, columns 4cg..).
     for (int bi = 1; bi < 4; ++bi) {
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
         }
         *reinterpret_cast<float4*>(Rt + bj * 256 + rr * 16 + 4 * cg) = acc;
       }
-      named_bar(1 + g, 128);
+      named_bar(nb + 1 + g, 128);
       for (int strip = gt; strip < 64 * bi; strip += 128) {
         const int bj = strip >> 6, e = strip & 63, rr = e >> 2, cg = e & 3;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
         *reinterpret_cast<float4*>(AT + (16 * bi + rr) * S + 16 * bj + 4 * cg) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
-      named_bar(1 + g, 128);
+      named_bar(nb + 1 + g, 128);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
       for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? AT[r * S + s0 + k] : 0.f;
     }
   }
-  __syncthreads();  // both heads' T read: the B-operand tiles overwrite the whole region
+  named_bar(nb, 256);  // both heads' T read: the B-operand tiles overwrite the whole region
   {
     const int g = warp >> 2, gt = tid & 127;
     const uint32_t bu = s_base + PrepSmem::AT + 8192 * g;
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   }
   fence_async_smem();
   tc_fence_before();
-  __syncthreads();
+  named_bar(nb, 256);
   tc_fence_after();
   if (tid == 0) {
 #pragma unroll
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
   }
   // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
   {
-    const bool ok = mbar_wait(&bar[1], 0, WAIT_LIMIT);
+    const bool ok = mbar_wait(&bar[1], ph, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
@@ -563,10 +564,69 @@ __global__ void __launch_bounds__(256, 2) prep_kernel(const GdnPrefillArgs a) {
       }
     }
   }
+  // Publish the item: every record byte written (generic stores made visible
+  // device-wide, bulk stores completed), then the ready flag with release.
+  tc_fence_before();
+  if (tid == 32) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+  }
+  __threadfence();
+  named_bar(nb, 256);
+  if (tid == 0) st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
+}
+
+// Persistent prep: one CTA per SM runs two independent 256-thread item
+// pipelines (two halves of shared memory and TMEM), each pulling (chunk, key
+// head) items in chunk-major order from an atomic counter.  It lets dependent
+// grids (the scan) launch at once.
+constexpr uint32_t PREP_HALF = (PrepSmem::SIZE + 1023) / 1024 * 1024;
+
+__global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefillArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm0 = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ int s_item[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_bar[4];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!a.ws_flag[0]) return;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int i = 0; i < 4; ++i) mbar_init(&s_bar[i], 1);
+    fence_mbar_init();
+  }
   tc_fence_before();
   __syncthreads();
-  if (tid == 32) bulk_wait_all();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  tc_fence_after();
+  const int k = tid >> 8, lt = tid & 255;
+  unsigned char* sm = sm0 + k * PREP_HALF;
+  const uint32_t tmem = s_tmem + 256 * k;
+  const int nb = 1 + 3 * k;
+  const int32_t nch = a.chunk_off[a.num_seqs];
+  const int n_items = nch * a.h_k;
+  uint32_t ph = 0;
+  for (;;) {
+    if (lt == 0) s_item[k] = atomicAdd(a.work_counter, 1);
+    named_bar(nb, 256);
+    const int item = s_item[k];
+    named_bar(nb, 256);
+    if (item >= n_items) break;
+    const int32_t gc = item / a.h_k;
+    const int hk = item % a.h_k;
+    const int b = find_seq(a.chunk_off, a.num_seqs, gc);
+    const int slot = a.slot_idx[b];
+    if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
+    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem);
+    ph ^= 1u;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(s_tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -662,6 +722,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         if (c >= 2 && !mbar_wait(&empty[s], ((c >> 1) - 1) & 1, WAIT_LIMIT)) { fail(); break; }
         if (*s_abort) break;
         const uint32_t dst = s_base + s * ScanSmem::BUF;
+        {  // the chunk's records are published by the prep (possibly still running)
+          const int32_t* fl = a.chunk_ready + (size_t)(gc0 + c) * a.h_k + hk;
+          uint32_t it = 0;
+          while (ld_acquire_gpu(fl) == 0 && ++it < FLAG_LIMIT) __nanosleep(64);
+          if (it >= FLAG_LIMIT) { fail(); break; }
+          fence_proxy_async_global();
+        }
         const unsigned char* vrec = a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC;
         const unsigned char* qrec = a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * Q_REC;
         mbar_expect_tx(&full[s], ScanSmem::BUF);
@@ -839,6 +906,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  // Launched as a dependent of the prep, finish only after it (a no-op otherwise).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace tcp
@@ -856,30 +925,62 @@ size_t gdn_tc_vh_bytes() { return gdn::tcp::VH_REC; }
 cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
   using namespace gdn::tcp;
   cudaError_t e = cudaSuccess;
+  int dev = 0, n_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  // With few (sequence, head) chains the scan leaves most SMs idle: run the
+  // prep on the other SMs at the same time and let the scan consume chunks
+  // as they are published.  Otherwise the prep gets every SM first.
+  const int64_t n_scan = (int64_t)a.num_seqs * a.h_v;
+  const bool overlap = n_scan <= n_sm / 2;
+  const int workers = overlap ? n_sm - (int)n_scan : n_sm;
+  const int psmem = (int)(2 * PREP_HALF) + 1024;
+  const int ssmem = (int)ScanSmem::SIZE + 1024;
+  if ((e = cudaFuncSetAttribute(prep_persistent_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ssmem)) != cudaSuccess)
+    return e;
+
   if ((e = gdn_trace_mark(tr, 0, true, s)) != cudaSuccess) return e;
   if ((e = gdn_launch_check(a, s, tr)) != cudaSuccess) return e;
   chunk_table_kernel<<<1, 1024, 0, s>>>(a);
   gdn_trace_count(tr, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 0, false, s)) != cudaSuccess) return e;
-  if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
-  if (a.max_chunks > 0) {
-    const int smem = (int)PrepSmem::SIZE + 1024;
-    e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    prep_kernel<<<dim3((unsigned)a.max_chunks, a.h_k), PrepSmem::THREADS, smem, s>>>(a);
+
+  if (!overlap) {
+    if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
+    prep_persistent_kernel<<<workers, 512, psmem, s>>>(a);
     gdn_trace_count(tr, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
+    if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
+    scan_kernel<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, ssmem, s>>>(a);
+    gdn_trace_count(tr, 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    // stage 2 covers prep and scan together: no event may sit between them
+    if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
+    prep_persistent_kernel<<<workers, 512, psmem, s>>>(a);
+    gdn_trace_count(tr, 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_seqs, a.h_v);
+    cfg.blockDim = dim3(SCAN_THREADS);
+    cfg.dynamicSmemBytes = ssmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, scan_kernel, a)) != cudaSuccess) return e;
+    gdn_trace_count(tr, 1);
   }
   // conv windows are rewritten only after the prep has read them
   if ((e = gdn_launch_window(a, GDN_BF16, s, tr)) != cudaSuccess) return e;
-  if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
-  if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
-  const int smem = (int)ScanSmem::SIZE + 1024;
-  e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  scan_kernel<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, smem, s>>>(a);
-  gdn_trace_count(tr, 1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return gdn_trace_mark(tr, 2, false, s);
 }
