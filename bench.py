@@ -231,18 +231,25 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
         for x in [e["s"], e["e"], *e["b"], *e["f"]]:
             x.record(stream)
     torch.cuda.synchronize()
+    # Timed pass: the plain call, events only around each step.
+    for e in ev:
+        flush.fill_(1.0)
+        e["s"].record(stream)
+        run()
+        e["e"].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [e["s"].elapsed_time(e["e"]) for e in ev]
+    # Attribution pass: the same steps with stage events and a launch count
+    # (the events sit between kernels, so this pass is not the headline).
     launches = 0
     traces = []
     for e in ev:
         flush.fill_(1.0)
-        e["s"].record(stream)
         tr = gdn.make_trace(e["b"], e["f"])
         run(trace=tr)
-        e["e"].record(stream)
         launches += tr.launches
         traces.append(tr)
     torch.cuda.synchronize()
-    step_ms = [e["s"].elapsed_time(e["e"]) for e in ev]
     stage_ms = {}
     for i, name in enumerate(ns):
         vals = []

@@ -177,7 +177,6 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   if (use_tc(dims)) {
     p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
     p.chunk_ready = reinterpret_cast<int32_t*>(ws + L.ready);
-    p.work_counter = reinterpret_cast<int32_t*>(ws + L.flag + 64);
     p.max_chunks = L.max_chunks;
     p.kq_ws = reinterpret_cast<uint8_t*>(ws + L.kq);
     p.vh_ws = reinterpret_cast<uint8_t*>(ws + L.vh);

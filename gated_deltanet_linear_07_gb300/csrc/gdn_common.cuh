@@ -127,7 +127,6 @@ struct GdnPrefillArgs {
   uint8_t* kq_ws;       // [max_chunks][h_k] [K;Q] tile images
   uint8_t* vh_ws;       // [max_chunks][h_v] P | U^T | decay factors | Wk records
   int32_t* chunk_ready; // [max_chunks][h_k] set to 1 when the prep published the chunk
-  int32_t* work_counter;  // next prep work item
 };
 
 // Launchers (defined in the kernel translation units); return cudaError_t.

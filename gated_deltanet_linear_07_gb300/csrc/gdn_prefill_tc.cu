@@ -92,6 +92,19 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -137,13 +150,29 @@ __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
 }
 
 // ---------------------------------------------------------------------------
-// chunk table: chunk_off[b] = sum_{b'<b} ceil(len_b' / C); one CTA.
+// Setup, one CTA: validate cu_seqlens (cu[0] = 0, non-decreasing, last =
+// total tokens; sets the workspace flag, or the device status bit and no
+// flag), then the chunk table chunk_off[b] = sum_{b'<b} ceil(len_b' / C), and
+// zero the ready flags.
 
-__global__ void __launch_bounds__(1024) chunk_table_kernel(const GdnPrefillArgs a) {
+__global__ void __launch_bounds__(1024) setup_kernel(const GdnPrefillArgs a) {
   __shared__ int32_t s_warp[32];
-  if (!a.ws_flag[0]) return;
+  __shared__ int s_bad;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int B = a.num_seqs;
   const int tid = threadIdx.x;
+  if (tid == 0) s_bad = (a.cu_seqlens[0] != 0) || ((int64_t)a.cu_seqlens[B] != a.total_tokens);
+  __syncthreads();
+  for (int i = tid; i < B; i += 1024)
+    if (a.cu_seqlens[i + 1] < a.cu_seqlens[i]) s_bad = 1;
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      a.ws_flag[0] = 0;
+      set_status(a.d_status, GDN_DEV_BAD_CU_SEQLENS);
+    }
+    return;
+  }
   const int per = (B + 1023) / 1024;
   const int b0 = tid * per;
   int32_t local = 0;
@@ -175,13 +204,58 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const GdnPrefillArgs 
     run += (a.cu_seqlens[b + 1] - a.cu_seqlens[b] + C - 1) / C;
   }
   if (tid == 1023) a.chunk_off[B] = run;
-  // per-(chunk, key head) ready flags and the prep work counter start at zero
+  // per-(chunk, key head) ready flags start at zero
   for (int64_t i = tid; i < a.max_chunks * a.h_k; i += 1024) a.chunk_ready[i] = 0;
-  if (tid == 0) *a.work_counter = 0;
+  if (tid == 0) a.ws_flag[0] = 1;
 }
 
 // ---------------------------------------------------------------------------
 // prep: one CTA (512 threads) per (chunk, key head).
+
+// Warp-level TF32 tensor-core product for the 16 x 16 blocks of the chunk
+// inverse: fragments of mma.m16n8k8 (row.col), fp32 accumulate.
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// d (16 x 16, as two 16 x 8 accumulator fragments) += P Q for 16 x 16 fp32
+// blocks P (row stride sp) and Q (row stride sq) in shared memory.
+__device__ __forceinline__ void mma16x16(float (&d)[2][4], const float* P, int sp, const float* Q,
+                                         int sq, int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int kt = 0; kt < 2; ++kt) {
+    const uint32_t a[4] = {f2tf32(P[gid * sp + 8 * kt + tig]), f2tf32(P[(gid + 8) * sp + 8 * kt + tig]),
+                           f2tf32(P[gid * sp + 8 * kt + tig + 4]),
+                           f2tf32(P[(gid + 8) * sp + 8 * kt + tig + 4])};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t b[2] = {f2tf32(Q[(8 * kt + tig) * sq + 8 * nt + gid]),
+                             f2tf32(Q[(8 * kt + tig + 4) * sq + 8 * nt + gid])};
+      mma_tf32(d[nt], a, b);
+    }
+  }
+}
+// Store sign * d into a 16 x 16 fp32 block (row stride st).
+__device__ __forceinline__ void store16x16(float* Dst, int st, const float (&d)[2][4], float sign,
+                                           int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2*>(Dst + gid * st + 8 * nt + 2 * tig) =
+        make_float2(sign * d[nt][0], sign * d[nt][1]);
+    *reinterpret_cast<float2*>(Dst + (gid + 8) * st + 8 * nt + 2 * tig) =
+        make_float2(sign * d[nt][2], sign * d[nt][3]);
+  }
+}
 
 struct PrepSmem {
   static constexpr uint32_t KQ = 0;          // 32768  [K;Q] K-major, 128 rows x 128
@@ -189,11 +263,12 @@ struct PrepSmem {
   static constexpr uint32_t AT = 65536;      // 2 x fp32 [64][68]: A, then T in place; finally
                                              // BU_0 | BU_1 | [BW_0; BW_1] bf16 tiles
   static constexpr uint32_t AH = 17408;      // bytes per head of A / T
-  static constexpr uint32_t R = 100352;      // 2 x fp32 [3][16][16]
-  static constexpr uint32_t GAM = 106496;    // fp32 [2][64], log2 units
-  static constexpr uint32_t BETA = 107008;   // fp32 [2][64]
-  static constexpr uint32_t EG = 107520;     // fp32 [2][64], e^{gamma}
-  static constexpr uint32_t BAR = 108032;    // 2 mbarriers + tmem address
+  static constexpr uint32_t R = 100352;      // 2 x fp32 [4][16][RST]: inverse products
+  static constexpr int RST = 24;             // fp32 row stride of those blocks
+  static constexpr uint32_t GAM = R + 2 * 4 * 16 * RST * 4;   // fp32 [2][64], log2 units
+  static constexpr uint32_t BETA = GAM + 512;                 // fp32 [2][64]
+  static constexpr uint32_t EG = BETA + 512;                  // fp32 [2][64], e^{gamma}
+  static constexpr uint32_t BAR = EG + 512;                   // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
   static constexpr int AST = 68;             // fp32 row stride of A and T
   static constexpr int THREADS = 256;
@@ -208,15 +283,46 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, 
   return lo;
 }
 
-// Two CTAs per SM: 256 threads, <= 128 registers, ~107 KB shared memory and
-// 256 TMEM columns each, so one CTA's latency-bound phases overlap the other's.
+// L2 prefetch of one work item's inputs: the x rows of its q, k and two v
+// segments including the 3-token halo, and its a / b rows, one 128-byte line
+// per request, spread over n threads (thread index i).  Every address lies
+// inside the item's own rows.
+__device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item, int i, int n) {
+  const int32_t gc = item / a.h_k;
+  const int hk = item % a.h_k;
+  const int b = find_seq(a.chunk_off, a.num_seqs, gc);
+  const int64_t start = a.cu_seqlens[b];
+  const int64_t t0 = start + (int64_t)(gc - a.chunk_off[b]) * C;
+  const int64_t t1 = min(t0 + C, (int64_t)a.cu_seqlens[b + 1]);
+  const int64_t r0 = t0 - 3 > start ? t0 - 3 : start;
+  const size_t cd2 = (size_t)a.conv_dim * 2;
+  const unsigned char* x = reinterpret_cast<const unsigned char*>(a.x);
+  const size_t seg_q = (size_t)hk * D * 2, seg_k = (size_t)(a.h_k + hk) * D * 2,
+               seg_v = (size_t)(2 * a.h_k + 2 * hk) * D * 2;
+  const int nl = (int)(t1 - r0) * 8;   // 2 + 2 + 4 lines per row
+  for (int l = i; l < nl; l += n) {
+    const int r = l >> 3, q = l & 7;
+    const size_t off = q < 2 ? seg_q + 128 * q : (q < 4 ? seg_k + 128 * (q - 2) : seg_v + 128 * (q - 4));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + (size_t)(r0 + r) * cd2 + off) : "memory");
+  }
+  const size_t g0 = (size_t)t0 * a.h_v * 2, g1 = (size_t)t1 * a.h_v * 2;  // bytes of a / b rows
+  for (size_t o = (g0 & ~(size_t)127) + 128 * (size_t)i; o < g1; o += 128 * (size_t)n) {
+    const size_t q = o < g0 ? g0 : o;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const unsigned char*>(a.a) + q) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const unsigned char*>(a.b) + q) : "memory");
+  }
+}
+
+// Two item groups per SM: 256 threads, <= 128 registers, ~107 KB shared memory
+// and 256 TMEM columns each, so one group's latency-bound phases overlap the
+// other's.
 // One (chunk, key head) work item, run by a group of 256 threads (thread
 // index tid) on its own shared memory `sm`, its own two mbarriers (completing
 // once per item; parity ph) and 256 TMEM columns from `tmem`.  Named barrier
 // nb spans the group, nb+1 and nb+2 its two 128-thread halves.
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
                                           int slot, unsigned char* sm, int tid, int nb,
-                                          uint64_t* bar, uint32_t ph, uint32_t tmem) {
+                                          uint64_t* bar, uint32_t ph, uint32_t tmem, int next) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -309,6 +415,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     }
     }
   }
+  // Warps 4 and 5 (v, no norm) finish first: they prefetch the group's next item.
+  if (next >= 0 && (warp == 4 || warp == 5)) prefetch_item(a, next, tid - 128, 64);
   // ---- gates of the two value heads (warps 6, 7) ----
   if (warp >= 6) {
     const int g = warp - 6;
@@ -412,71 +520,67 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   tc_fence_before();
   named_bar(nb, 256);
   // ---- T = (I + A)^-1 in place, per value head: 4 warps per head ----
+  // With 16 x 16 blocks b: T_bb = (I + A_bb)^-1 by forward substitution (fp32),
+  // then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then the lower-left
+  // 32 x 32 block -T_[23][23] A_[23][01] T_[01][01] (products on the tensor
+  // cores in TF32).  Only products of exact blocks, no matrix powers: finite
+  // for fully correlated keys.
   float tv[4][8];   // this thread's T entries for the B operands (read before they are overwritten)
   {
-    const int g = warp >> 2, gt = tid & 127;
+    const int g = warp >> 2, gt = tid & 127, wb = warp & 3;
     float* AT = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
-    float* Rt = reinterpret_cast<float*>(sm + PrepSmem::R) + g * 768;
-    // 16x16 diagonal blocks: one column each by forward substitution (reads
-    // A's block, then writes T's block over it)
-    float tc[16];
-    const int kb = gt >> 4, jj = gt & 15, o = kb * 16;
-    if (gt < 64) {
+    constexpr int RS = PrepSmem::RST;
+    float* Rt = reinterpret_cast<float*>(sm + PrepSmem::R) + g * (4 * 16 * RS);
+    {  // diagonal block wb: lane j (< 16) computes column j
+      const int o = 16 * wb, j = lane & 15;
+      float x[16];
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
+      for (int r = 0; r < 16; ++r) {
+        float arow[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = *reinterpret_cast<const float4*>(AT + (o + r) * S + o + 4 * q);
+          arow[4 * q] = f.x; arow[4 * q + 1] = f.y; arow[4 * q + 2] = f.z; arow[4 * q + 3] = f.w;
+        }
         float acc = 0.f;
 #pragma unroll
-        for (int ss = 0; ss < rr; ++ss)
-          if (ss >= jj) acc = fmaf(AT[(o + rr) * S + o + ss], tc[ss], acc);
-        tc[rr] = rr < jj ? 0.f : (rr == jj ? 1.f : -acc);
+        for (int s2 = 0; s2 < r; ++s2) acc = fmaf(arow[s2], x[s2], acc);
+        x[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
+      }
+      __syncwarp();
+      if (lane < 16) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) AT[(o + r) * S + o + j] = x[r];
       }
     }
     named_bar(nb + 1 + g, 128);
-    if (gt < 64) {
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) AT[(o + rr) * S + o + jj] = tc[rr];
+    if (wb < 2) {  // T_10 (warp 0) and T_32 (warp 1)
+      const int i = 1 + 2 * wb;   // block row; column block i - 1
+      float* Rw = Rt + wb * 16 * RS;
+      float d[2][4] = {};
+      mma16x16(d, AT + 16 * i * S + 16 * (i - 1), S, AT + 16 * (i - 1) * S + 16 * (i - 1), S, lane);
+      store16x16(Rw, RS, d, 1.f, lane);
+      __syncwarp();
+      float e[2][4] = {};
+      mma16x16(e, AT + 16 * i * S + 16 * i, S, Rw, RS, lane);
+      store16x16(AT + 16 * i * S + 16 * (i - 1), S, e, -1.f, lane);
     }
     named_bar(nb + 1 + g, 128);
-    // block rows 1..3: T[bi][bj] = -T[bi][bi] sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],
-    // written over A[bi][bj]; a thread owns 1x4 strips (row rr, columns 4cg..).
-    for (int bi = 1; bi < 4; ++bi) {
-      for (int strip = gt; strip < 64 * bi; strip += 128) {
-        const int bj = strip >> 6, e = strip & 63, rr = e >> 2, cg = e & 3;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = AT + (16 * bi + rr) * S;
-        for (int bk = bj; bk < bi; ++bk) {
-#pragma unroll
-          for (int m2 = 0; m2 < 16; ++m2) {
-            const int k = 16 * bk + m2;
-            const float av = arow[k];
-            const float4 t4 = *reinterpret_cast<const float4*>(AT + k * S + 16 * bj + 4 * cg);
-            acc.x = fmaf(av, t4.x, acc.x);
-            acc.y = fmaf(av, t4.y, acc.y);
-            acc.z = fmaf(av, t4.z, acc.z);
-            acc.w = fmaf(av, t4.w, acc.w);
-          }
-        }
-        *reinterpret_cast<float4*>(Rt + bj * 256 + rr * 16 + 4 * cg) = acc;
-      }
-      named_bar(nb + 1 + g, 128);
-      for (int strip = gt; strip < 64 * bi; strip += 128) {
-        const int bj = strip >> 6, e = strip & 63, rr = e >> 2, cg = e & 3;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* trow = AT + (16 * bi + rr) * S + 16 * bi;
-#pragma unroll
-        for (int m2 = 0; m2 < 16; ++m2) {
-          const float t1 = trow[m2];
-          const float4 r4 = *reinterpret_cast<const float4*>(Rt + bj * 256 + m2 * 16 + 4 * cg);
-          acc.x = fmaf(t1, r4.x, acc.x);
-          acc.y = fmaf(t1, r4.y, acc.y);
-          acc.z = fmaf(t1, r4.z, acc.z);
-          acc.w = fmaf(t1, r4.w, acc.w);
-        }
-        *reinterpret_cast<float4*>(AT + (16 * bi + rr) * S + 16 * bj + 4 * cg) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-      }
-      named_bar(nb + 1 + g, 128);
+    const int bi = 2 + (wb >> 1), bj = wb & 1;   // this warp's block of the lower-left 32 x 32
+    {  // R_ij = A_i0 T_0j + A_i1 T_1j  (T_01 = 0)
+      float d[2][4] = {};
+      if (bj == 0) mma16x16(d, AT + 16 * bi * S, S, AT, S, lane);
+      mma16x16(d, AT + 16 * bi * S + 16, S, AT + 16 * S + 16 * bj, S, lane);
+      store16x16(Rt + wb * 16 * RS, RS, d, 1.f, lane);
     }
+    named_bar(nb + 1 + g, 128);
+    {  // T_ij = -(sum_{k = 2..i} T_ik R_kj)
+      float d[2][4] = {};
+      if (bi == 3) mma16x16(d, AT + 48 * S + 32, S, Rt + bj * 16 * RS, RS, lane);
+      mma16x16(d, AT + 16 * bi * S + 16 * bi, S, Rt + ((bi - 2) * 2 + bj) * 16 * RS, RS, lane);
+      store16x16(AT + 16 * bi * S + 16 * bj, S, d, -1.f, lane);
+    }
+    named_bar(nb + 1 + g, 128);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int chunk = gt + 128 * q;
@@ -586,11 +690,8 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm0 = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ int s_item[2];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_bar[4];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (!a.ws_flag[0]) return;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(&s_tmem, 512);
@@ -603,6 +704,14 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The setup kernel's results (flag, chunk table, zeroed counters) are
+  // visible after this wait; only then may dependent grids (the scan) start.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!a.ws_flag[0]) {
+    if (warp == 0) tmem_dealloc(s_tmem, 512);
+    return;
+  }
   const int k = tid >> 8, lt = tid & 255;
   unsigned char* sm = sm0 + k * PREP_HALF;
   const uint32_t tmem = s_tmem + 256 * k;
@@ -610,18 +719,18 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   const int32_t nch = a.chunk_off[a.num_seqs];
   const int n_items = nch * a.h_k;
   uint32_t ph = 0;
-  for (;;) {
-    if (lt == 0) s_item[k] = atomicAdd(a.work_counter, 1);
-    named_bar(nb, 256);
-    const int item = s_item[k];
-    named_bar(nb, 256);
-    if (item >= n_items) break;
+  // Static round-robin over the (chunk, key head) items in chunk-major order:
+  // group g takes items g, g + G, g + 2G, ... (G groups), so each wave of
+  // items finishes the earliest chunks first.
+  const int n_groups = 2 * (int)gridDim.x;
+  for (int item = 2 * (int)blockIdx.x + k; item < n_items; item += n_groups) {
     const int32_t gc = item / a.h_k;
     const int hk = item % a.h_k;
     const int b = find_seq(a.chunk_off, a.num_seqs, gc);
     const int slot = a.slot_idx[b];
     if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
-    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem);
+    const int next = item + n_groups < n_items ? item + n_groups : -1;
+    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem, next);
     ph ^= 1u;
   }
   tc_fence_before();
@@ -681,6 +790,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   uint64_t* wready = full + 6;
   uint64_t* hready = full + 7;
   uint64_t* bar_o = full + 8;
+  uint64_t* wtready = full + 11;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 9);
   volatile int* s_abort = reinterpret_cast<volatile int*>(full + 10);
 
@@ -698,8 +808,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     mbar_init(bar_x, 1);
     mbar_init(bar_dh, 1);
     mbar_init(bar_o, 1);
-    mbar_init(wready, EPI_THREADS);
-    mbar_init(hready, EPI_THREADS);
+    mbar_init(wtready, EPI_THREADS / 32);
+    // one arrival per epilogue warp, after the warp's writes are fenced
+    mbar_init(wready, EPI_THREADS / 32);
+    mbar_init(hready, EPI_THREADS / 32);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -743,7 +855,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t ID_XO = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_XO = idesc_bf16(128, 64, false, false);
       constexpr uint32_t ID_DH = idesc_bf16(128, 128, false, true);
       constexpr uint32_t ID_O2 = idesc_bf16(128, 64, false, false);
       const uint64_t d_ht = sdesc_kmaj(s_base + ScanSmem::HT, 128, 0);
@@ -759,16 +871,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
             !mbar_wait(hready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // [X | O1] = H^T [Wk; Q]^T
+        for (int ks = 0; ks < 8; ++ks)  // X = H^T Wk^T first: it is on the chain
           mma_bf16(tmem + TXO + 128 * s, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
                    sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(bar_x);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T (completes with bar_o)
+          mma_bf16(tmem + TXO + 128 * s + 64, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
+                   sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         if (!mbar_wait(wready, c & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
           mma_bf16(tmem + TDH, sdesc_add(d_wtt, ks * 32), sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
         mma_commit(bar_dh);
+        if (!mbar_wait(wtready, c & 1, WAIT_LIMIT)) { fail(); break; }
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
           mma_bf16(tmem + TO2, sdesc_add(d_wt, ks * 32), sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
@@ -796,6 +914,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     for (int q = 0; q < 4; ++q) a_ht[q] = s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q);
     constexpr uint32_t WTT_OFF = ScanSmem::WTT - ScanSmem::WT;
     // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
+    // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
     const size_t o_lane = ((size_t)(16 * grp + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) + 8 * (lane & 3);
     const size_t o_row = (size_t)a.h_v * D;   // elements between consecutive tokens
 #pragma unroll
@@ -806,58 +925,75 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
                               pack_bf16(H[8 * q + 6], H[8 * q + 7])));
     fence_async_smem();
     tc_fence_before();
-    mbar_arrive(hready);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(hready);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o);
     for (int c = 0; c < nch; ++c) {
       if (*s_abort) break;
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
-      const float* ex = reinterpret_cast<const float*>(sm + s * ScanSmem::BUF + ScanSmem::B_EXP);
+      const uint32_t ex = buf + ScanSmem::B_EXP;   // e^{gamma} [64] | e^{gamma_C - gamma} [64] | e^{gamma_C}
       const uint32_t txo = tmem + lbase + TXO + 128 * s;
       const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
-      if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) || !mbar_wait(bar_x, c & 1, WAIT_LIMIT)) {
-        fail();
-        break;
+      if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
+      // Everything the W step reads from shared memory, loaded while X is computed.
+      const uint4 ut0 = ld_shared_v4(buf + a_ut[0]), ut1 = ld_shared_v4(buf + a_ut[1]);
+      float edv[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = ld_shared_f4(ex + 4 * (64 + 16 * grp + 4 * q));
+        edv[4 * q] = f.x; edv[4 * q + 1] = f.y; edv[4 * q + 2] = f.z; edv[4 * q + 3] = f.w;
       }
+      const float dec = ld_shared_f32(ex + 4 * 128);
+      if (!mbar_wait(bar_x, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
       // W^T = U^T - X for r in this group's quarter
-      const float dec = ex[128];
       {
         float X[16];
         tmem_ld16(txo + 16 * grp, X);
+        uint4 wpk[2];   // W^T in bf16, stored after the chain's tile
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int r0 = 16 * grp + 8 * q;
           float u[8];
-          bf16x8_to_float(ld_shared_v4(buf + a_ut[q]), u);
-          const float4 d0 = *reinterpret_cast<const float4*>(ex + 64 + r0);
-          const float4 d1 = *reinterpret_cast<const float4*>(ex + 64 + r0 + 4);
-          const float edv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          bf16x8_to_float(q == 0 ? ut0 : ut1, u);
           float wv[8], wt[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             wv[e] = u[e] - X[8 * q + e];
-            wt[e] = wv[e] * edv[e];
+            wt[e] = wv[e] * edv[8 * q + e];
           }
-          st_shared_v4(a_wt[q],
-                       make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
-                                  pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7])));
+          wpk[q] = make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
+                              pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7]));
           st_shared_v4(a_wt[q] + WTT_OFF,
                        make_uint4(pack_bf16(wt[0], wt[1]), pack_bf16(wt[2], wt[3]),
                                   pack_bf16(wt[4], wt[5]), pack_bf16(wt[6], wt[7])));
         }
+        // (the X read is ordered before later MMAs into this buffer by the
+        // tcgen05 fence ahead of the next hready arrival)
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wready);
+        st_shared_v4(a_wt[0], wpk[0]);
+        st_shared_v4(a_wt[1], wpk[1]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wtready);
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(wready);
+
       if (!mbar_wait(bar_dh, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
       // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
       {
         float dH[32];
         tmem_ld32(tmem + lbase + TDH + 32 * grp, dH);
+        const float2 dd = make_float2(dec, dec);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) H[e] = fmaf(dec, H[e], dH[e]);
+        for (int e = 0; e < 16; ++e) {
+          const float2 r2 = __ffma2_rn(dd, make_float2(H[2 * e], H[2 * e + 1]),
+                                       make_float2(dH[2 * e], dH[2 * e + 1]));
+          H[2 * e] = r2.x;
+          H[2 * e + 1] = r2.y;
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -866,24 +1002,31 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
                                 pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                                 pack_bf16(H[8 * q + 6], H[8 * q + 7])));
       fence_async_smem();
-      tc_fence_before();
-      // o = e^{gamma} O1 + O2 (read before arriving, so the next chunk's MMAs
-      // cannot overwrite O2 / this buffer's O1 while they are read)
       if (!mbar_wait(bar_o, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
       float O1[16], O2[16];
-      tmem_ld16(txo + 64 + 16 * grp, O1);
-      tmem_ld16(tmem + lbase + TO2 + 16 * grp, O2);
+      tmem_ld16x2(txo + 64 + 16 * grp, O1, tmem + lbase + TO2 + 16 * grp, O2);
       tc_fence_before();
-      mbar_arrive(hready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hready);
       // Stage this warp's 16 x 32 block of o in its own 1 KiB of the buffer's
       // U tile (read in the W phase, free now), then write it as 16-byte
       // pieces (8 values of one row each).
       __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + s * ScanSmem::BUF + ScanSmem::B_UT +
                                                             (warp - 2) * 1024);
+      float eg[16];   // e^{gamma_r} of this group's rows
 #pragma unroll
-      for (int e = 0; e < 16; ++e)   // e^{gamma_r}: the buffer is still ours (released after staging)
-        ost[e * 32 + lane] = __float2bfloat16_rn(fmaf(ex[16 * grp + e], O1[e], O2[e]));
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = ld_shared_f4(ex + 4 * (16 * grp + 4 * q));
+        eg[4 * q] = f.x; eg[4 * q + 1] = f.y; eg[4 * q + 2] = f.z; eg[4 * q + 3] = f.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const float2 o2 = __ffma2_rn(make_float2(eg[e], eg[e + 1]), make_float2(O1[e], O1[e + 1]),
+                                     make_float2(O2[e], O2[e + 1]));
+        ost[e * 32 + lane] = __float2bfloat16_rn(o2.x);
+        ost[(e + 1) * 32 + lane] = __float2bfloat16_rn(o2.y);
+      }
       __syncwarp();
       {
         __nv_bfloat16* ob = out + (size_t)(start + (int64_t)c * C) * o_row + o_lane;
@@ -945,17 +1088,27 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
     return e;
 
   if ((e = gdn_trace_mark(tr, 0, true, s)) != cudaSuccess) return e;
-  if ((e = gdn_launch_check(a, s, tr)) != cudaSuccess) return e;
-  chunk_table_kernel<<<1, 1024, 0, s>>>(a);
+  setup_kernel<<<1, 1024, 0, s>>>(a);
   gdn_trace_count(tr, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 0, false, s)) != cudaSuccess) return e;
+  // the prep is a programmatic dependent of the setup (it waits for it on
+  // the device) and the scan, when overlapped, of the prep
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3(workers);
+  pcfg.blockDim = dim3(512);
+  pcfg.dynamicSmemBytes = psmem;
+  pcfg.stream = s;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = tr ? 0 : 1;   // a stage event between the two ends the overlap anyway
 
   if (!overlap) {
     if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
-    prep_persistent_kernel<<<workers, 512, psmem, s>>>(a);
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
     scan_kernel<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, ssmem, s>>>(a);
@@ -964,17 +1117,13 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   } else {
     // stage 2 covers prep and scan together: no event may sit between them
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
-    prep_persistent_kernel<<<workers, 512, psmem, s>>>(a);
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_seqs, a.h_v);
     cfg.blockDim = dim3(SCAN_THREADS);
     cfg.dynamicSmemBytes = ssmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, scan_kernel, a)) != cudaSuccess) return e;
