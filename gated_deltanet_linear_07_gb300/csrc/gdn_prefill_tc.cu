@@ -349,22 +349,30 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     int ch;
     if (seg == 0) ch = half == 0 ? hk * D + 8 * l16 : a.h_k * D + hk * D + 8 * l16;
     else ch = 2 * a.h_k * D + (2 * hk + half) * D + 8 * l16;
-    float w[8][4];
+    // Conv taps as channel pairs, w2[k][p] = (w[ch + 2p][k], w[ch + 2p + 1][k]);
+    // the arithmetic below runs on packed fp32 pairs.
+    float2 w2[4][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + e)));
-      w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
+    for (int p2 = 0; p2 < 4; ++p2) {
+      const float4 f0 = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + 2 * p2)));
+      const float4 f1 =
+          __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + 2 * p2 + 1)));
+      w2[0][p2] = make_float2(f0.x, f1.x);
+      w2[1][p2] = make_float2(f0.y, f1.y);
+      w2[2][p2] = make_float2(f0.z, f1.z);
+      w2[3][p2] = make_float2(f0.w, f1.w);
     }
     const float qscale = rsqrtf((float)D);
+    const float2 half2 = make_float2(0.5f, 0.5f);
 #pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-    const int rb = r0 + 8 * hh;
+    for (int hh = 0; hh < 4; ++hh) {
+    const int rb = r0 + 4 * hh;
     // 11 rows (3-token halo + 8 tokens), loaded unconditionally from valid
     // addresses so the loads issue back to back; masked rows zeroed after.
-    uint4 xr[11];
-    bool keep[11];
+    uint4 xr[7];
+    bool keep[7];
 #pragma unroll
-    for (int q = 0; q < 11; ++q) {
+    for (int q = 0; q < 7; ++q) {
       const int rr = rb - 3 + q;
       const int64_t p = (int64_t)c * C + rr;
       const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;
@@ -374,43 +382,67 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       xr[q] = __ldg(reinterpret_cast<const uint4*>(src));
     }
 #pragma unroll
-    for (int q = 0; q < 11; ++q)
+    for (int q = 0; q < 7; ++q)
       if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
-    float xf[4][8];   // rolling window of the last four rows, converted once each
+    float2 xf[4][4];   // rolling window of the last four rows as channel pairs
+    auto unpack = [](const uint4& u, float2 (&f)[4]) {
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int q = 0; q < 3; ++q) bf16x8_to_float(xr[q], xf[q + 1]);
+      for (int p2 = 0; p2 < 4; ++p2)
+        f[p2] = make_float2(__uint_as_float(w4[p2] << 16), __uint_as_float(w4[p2] & 0xffff0000u));
+    };
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int q = 0; q < 3; ++q) unpack(xr[q], xf[q + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
       const int r = rb + i;
 #pragma unroll
       for (int q = 0; q < 3; ++q)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xf[q][e] = xf[q + 1][e];
-      bf16x8_to_float(xr[i + 3], xf[3]);
-      float y[8];
+        for (int p2 = 0; p2 < 4; ++p2) xf[q][p2] = xf[q + 1][p2];
+      unpack(xr[i + 3], xf[3]);
+      float2 y[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float z = w[e][0] * xf[0][e];
-        z = fmaf(w[e][1], xf[1][e], z);
-        z = fmaf(w[e][2], xf[2][e], z);
-        z = fmaf(w[e][3], xf[3][e], z);
-        y[e] = r < L ? silu_fast(z) : 0.f;
+      for (int p2 = 0; p2 < 4; ++p2) {
+        float2 z = __fmul2_rn(w2[0][p2], xf[0][p2]);
+        z = __ffma2_rn(w2[1][p2], xf[1][p2], z);
+        z = __ffma2_rn(w2[2][p2], xf[2][p2], z);
+        z = __ffma2_rn(w2[3][p2], xf[3][p2], z);
+        // SiLU: z sigmoid(z) = h + h tanh(h), h = z / 2
+        const float2 h2 = __fmul2_rn(z, half2);
+        float2 t;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t.x) : "f"(h2.x));
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
+        y[p2] = __ffma2_rn(h2, t, h2);
       }
       if (seg == 0) {
-        float ss = 0.f;
+        float2 s2 = __fmul2_rn(y[0], y[0]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
+        for (int p2 = 1; p2 < 4; ++p2) s2 = __ffma2_rn(y[p2], y[p2], s2);
+        float ss = s2.x + s2.y;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        // rows past the chunk end get inv = 0, so their q / k are zero
         const float inv = (r < L ? rsqrtf(ss + a.l2_eps) : 0.f) * (half == 0 ? qscale : 1.0f);
+        const float2 inv2 = make_float2(inv, inv);
+        uint32_t pk[4];
+#pragma unroll
+        for (int p2 = 0; p2 < 4; ++p2) {
+          const __nv_bfloat162 v = __float22bfloat162_rn(__fmul2_rn(y[p2], inv2));
+          pk[p2] = *reinterpret_cast<const uint32_t*>(&v);
+        }
         const int row = half == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
         st_shared_v4(s_base + PrepSmem::KQ + kmaj_off(128, row, 8 * l16),
-                     make_uint4(pack_bf16(y[0] * inv, y[1] * inv), pack_bf16(y[2] * inv, y[3] * inv),
-                                pack_bf16(y[4] * inv, y[5] * inv), pack_bf16(y[6] * inv, y[7] * inv)));
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
       } else {
-        st_shared_v4(s_base + PrepSmem::V + half * 16384 + mnmaj_off(64, 8 * l16, r),
-                     make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                                pack_bf16(y[6], y[7])));
+        uint32_t pk[4];
+#pragma unroll
+        for (int p2 = 0; p2 < 4; ++p2) {
+          const __nv_bfloat162 v = __float22bfloat162_rn(y[p2]);
+          pk[p2] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        const uint4 val = r < L ? make_uint4(pk[0], pk[1], pk[2], pk[3]) : make_uint4(0, 0, 0, 0);
+        st_shared_v4(s_base + PrepSmem::V + half * 16384 + mnmaj_off(64, 8 * l16, r), val);
       }
     }
     }
@@ -478,42 +510,45 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     const bool ok = mbar_wait(&bar[0], ph, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
-    float d[64];
-    if (ok) {
-      float t32[32];
-      tmem_ld32(tmem + ((uint32_t)(32 * q) << 16), t32);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) d[e] = t32[e];
-      tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32, t32);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) d[32 + e] = t32[e];
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) d[e] = 0.f;
-    }
     const float* gm = gam + g * 64;
-    if (m < 64) {
-      const int r = m;
-      float* A = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
-      const float gr = gm[r], br = beta[g * 64 + r];
+    const int r = m & 63;
+    const float gr = gm[r];
+    const float br = beta[g * 64 + r];
+    float* Arow = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH) + r * S;
+    unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
 #pragma unroll
-      for (int s2 = 0; s2 < 64; ++s2)
-        A[r * S + s2] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[s2] : 0.f;
-    } else {
-      const int r = m - 64;
-      const float gr = gm[r];
-      unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
+    for (int hf = 0; hf < 2; ++hf) {   // 32 columns s at a time
+      float d[32];
+      if (ok) {
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, d);
+      } else {
 #pragma unroll
-      for (int ck = 0; ck < 8; ++ck) {
-        float pv[8];
+        for (int e = 0; e < 32; ++e) d[e] = 0.f;
+      }
+      if (m < 64) {   // A[r][s] = beta_r e^{gamma_r - gamma_s} (k_r . k_s), s < r
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s2 = 8 * ck + e;
-          pv[e] = s2 <= r ? fast_exp2(gr - gm[s2]) * d[s2] : 0.f;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float av[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s2 = 32 * hf + 4 * c4 + e;
+            av[e] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[4 * c4 + e] : 0.f;
+          }
+          *reinterpret_cast<float4*>(Arow + 32 * hf + 4 * c4) = make_float4(av[0], av[1], av[2], av[3]);
         }
-        *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 8 * ck)) =
-            make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                       pack_bf16(pv[6], pv[7]));
+      } else {        // P[r][s] = e^{gamma_r - gamma_s} (q_r . k_s), s <= r
+#pragma unroll
+        for (int ck = 0; ck < 4; ++ck) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s2 = 32 * hf + 8 * ck + e;
+            pv[e] = s2 <= r ? fast_exp2(gr - gm[s2]) * d[8 * ck + e] : 0.f;
+          }
+          *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * hf + 8 * ck)) =
+              make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                         pack_bf16(pv[6], pv[7]));
+        }
       }
     }
   }
@@ -646,9 +681,6 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     for (int task = warp; task < 16 && ok; task += 8) {
       const int kind = task >> 2;                // 0,1: U^T_g   2,3: Wk column halves
       const uint32_t col = 64 * kind;
-      float v[2][32];
-      tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col, v[0]);
-      tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32, v[1]);
       unsigned char* dst;
       int row, R, c0;
       if (kind < 2) {            // U^T_g row j = m
@@ -658,9 +690,11 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32 * h2, v);
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
-          const float* f = &v[h2][8 * ck];
+          const float* f = &v[8 * ck];
           *reinterpret_cast<uint4*>(dst + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck)) =
               make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                          pack_bf16(f[6], f[7]));
@@ -670,14 +704,18 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   }
   // Publish the item: every record byte written (generic stores made visible
   // device-wide, bulk stores completed), then the ready flag with release.
+  // One gpu-scope fence after the group barrier covers every thread's stores
+  // (cumulativity), so only thread 0 waits for them.
   tc_fence_before();
   if (tid == 32) {
     bulk_wait_all();
     fence_proxy_async_global();
   }
-  __threadfence();
   named_bar(nb, 256);
-  if (tid == 0) st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
+  if (tid == 0) {
+    __threadfence();
+    st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
+  }
 }
 
 // Persistent prep: one CTA per SM runs two independent 256-thread item
