@@ -156,6 +156,7 @@ KERNEL_SOURCES = {
     "decode_step": ("gdn_decode.cu", "gdn_common.cuh"),
     "prefill_scan": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "prefill_chunk": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
+    "prefill_overlap": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
 }
 
 
@@ -469,7 +470,8 @@ def run_gdn(args):
                    "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
                    "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
     stage = pf["stage_ms"]
-    if "scan" in stage and "chunk" not in stage:
+    overlapped = "scan" in stage and "chunk" not in stage
+    if overlapped:
         # Overlapped launch: the chunk work runs beside the scan inside the
         # scan stage's interval, so that interval carries both FLOP shares.
         stage_flops["scan"] += stage_flops["chunk"]
@@ -480,7 +482,8 @@ def run_gdn(args):
         dom_ms = max_over_ranks(stage[dom])
         ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": ach / peak_tf, "traffic": recorded_traffic("prefill_" + dom),
+                "frac": ach / peak_tf,
+                "traffic": recorded_traffic("prefill_overlap" if overlapped else "prefill_" + dom),
                 "kernel": {"chunk": "prep_kernel (prefill stage 'chunk')",
                            "scan": ("scan_kernel (prefill stage 'scan')" if "chunk" in stage else
                                    "prep_persistent_kernel + scan_kernel, overlapped "
