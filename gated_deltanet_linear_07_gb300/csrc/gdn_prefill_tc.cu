@@ -83,6 +83,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -338,22 +341,23 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
-  // ---- front end: conv + SiLU + L2 norm; warp = (segment, 16 tokens) ----
+  // ---- front end: conv + SiLU + L2 norm; warp = (segment, 32 tokens), lane = 4 channels ----
   {
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* win =
         reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * cd;
-    const int seg = warp >> 2;          // 0: q | k, 1: v of both value heads
-    const int r0 = (warp & 3) * 16;
-    const int half = lane >> 4, l16 = lane & 15;
+    const int seg = warp >> 1;          // 0: q, 1: k, 2 / 3: v of value head 2 hk / 2 hk + 1
+    const int r0 = (warp & 1) * 32;
     int ch;
-    if (seg == 0) ch = half == 0 ? hk * D + 8 * l16 : a.h_k * D + hk * D + 8 * l16;
-    else ch = 2 * a.h_k * D + (2 * hk + half) * D + 8 * l16;
+    if (seg == 0) ch = hk * D;
+    else if (seg == 1) ch = (a.h_k + hk) * D;
+    else ch = 2 * a.h_k * D + (2 * hk + seg - 2) * D;
+    ch += 4 * lane;
     // Conv taps as channel pairs, w2[k][p] = (w[ch + 2p][k], w[ch + 2p + 1][k]);
     // the arithmetic below runs on packed fp32 pairs.
-    float2 w2[4][4];
+    float2 w2[4][2];
 #pragma unroll
-    for (int p2 = 0; p2 < 4; ++p2) {
+    for (int p2 = 0; p2 < 2; ++p2) {
       const float4 f0 = __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + 2 * p2)));
       const float4 f1 =
           __ldg(reinterpret_cast<const float4*>(a.conv_weight + 4 * (size_t)(ch + 2 * p2 + 1)));
@@ -362,89 +366,87 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       w2[2][p2] = make_float2(f0.z, f1.z);
       w2[3][p2] = make_float2(f0.w, f1.w);
     }
-    const float qscale = rsqrtf((float)D);
+    const float scale = seg == 0 ? rsqrtf((float)D) : 1.0f;
     const float2 half2 = make_float2(0.5f, 0.5f);
-#pragma unroll 1
-    for (int hh = 0; hh < 4; ++hh) {
-    const int rb = r0 + 4 * hh;
-    // 11 rows (3-token halo + 8 tokens), loaded unconditionally from valid
-    // addresses so the loads issue back to back; masked rows zeroed after.
-    uint4 xr[7];
-    bool keep[7];
-#pragma unroll
-    for (int q = 0; q < 7; ++q) {
-      const int rr = rb - 3 + q;
-      const int64_t p = (int64_t)c * C + rr;
-      const __nv_bfloat16* src = x + (size_t)t0 * cd + ch;
-      keep[q] = rr < L && (p >= 0 || init);
-      if (rr < L && p >= 0) src = x + (size_t)(t0 + rr) * cd + ch;
-      else if (rr < L && init) src = win + (size_t)(3 + p) * cd + ch;
-      xr[q] = __ldg(reinterpret_cast<const uint4*>(src));
-    }
-#pragma unroll
-    for (int q = 0; q < 7; ++q)
-      if (!keep[q]) xr[q] = make_uint4(0, 0, 0, 0);
-    float2 xf[4][4];   // rolling window of the last four rows as channel pairs
-    auto unpack = [](const uint4& u, float2 (&f)[4]) {
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int p2 = 0; p2 < 4; ++p2)
-        f[p2] = make_float2(__uint_as_float(w4[p2] << 16), __uint_as_float(w4[p2] & 0xffff0000u));
+    auto unpack = [](const uint2& u, float2 (&f)[2]) {
+      f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+      f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
     };
-#pragma unroll
-    for (int q = 0; q < 3; ++q) unpack(xr[q], xf[q + 1]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rb + i;
-#pragma unroll
-      for (int q = 0; q < 3; ++q)
-#pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) xf[q][p2] = xf[q + 1][p2];
-      unpack(xr[i + 3], xf[3]);
-      float2 y[4];
-#pragma unroll
-      for (int p2 = 0; p2 < 4; ++p2) {
-        float2 z = __fmul2_rn(w2[0][p2], xf[0][p2]);
-        z = __ffma2_rn(w2[1][p2], xf[1][p2], z);
-        z = __ffma2_rn(w2[2][p2], xf[2][p2], z);
-        z = __ffma2_rn(w2[3][p2], xf[3][p2], z);
-        // SiLU: z sigmoid(z) = h + h tanh(h), h = z / 2
-        const float2 h2 = __fmul2_rn(z, half2);
-        float2 t;
-        asm("tanh.approx.f32 %0, %1;" : "=f"(t.x) : "f"(h2.x));
-        asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
-        y[p2] = __ffma2_rn(h2, t, h2);
-      }
-      if (seg == 0) {
-        float2 s2 = __fmul2_rn(y[0], y[0]);
-#pragma unroll
-        for (int p2 = 1; p2 < 4; ++p2) s2 = __ffma2_rn(y[p2], y[p2], s2);
-        float ss = s2.x + s2.y;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        // rows past the chunk end get inv = 0, so their q / k are zero
-        const float inv = (r < L ? rsqrtf(ss + a.l2_eps) : 0.f) * (half == 0 ? qscale : 1.0f);
-        const float2 inv2 = make_float2(inv, inv);
-        uint32_t pk[4];
-#pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const __nv_bfloat162 v = __float22bfloat162_rn(__fmul2_rn(y[p2], inv2));
-          pk[p2] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        const int row = half == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
-        st_shared_v4(s_base + PrepSmem::KQ + kmaj_off(128, row, 8 * l16),
-                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
-      } else {
-        uint32_t pk[4];
-#pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const __nv_bfloat162 v = __float22bfloat162_rn(y[p2]);
-          pk[p2] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        const uint4 val = r < L ? make_uint4(pk[0], pk[1], pk[2], pk[3]) : make_uint4(0, 0, 0, 0);
-        st_shared_v4(s_base + PrepSmem::V + half * 16384 + mnmaj_off(64, 8 * l16, r), val);
-      }
+    // Row rr of the chunk (rr < 0: the 3-token history), or zeros where masked.
+    auto load_row = [&](int rr) -> uint2 {
+      const int64_t p = (int64_t)c * C + rr;
+      uint2 v = make_uint2(0, 0);
+      if (rr < L && p >= 0) v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + rr) * cd + ch));
+      else if (rr < L && init) v = __ldg(reinterpret_cast<const uint2*>(win + (size_t)(3 + p) * cd + ch));
+      return v;
+    };
+    // Each row is loaded once: the rolling window carries the last three rows
+    // from one 4-token step to the next, and the next step's 4 rows are in
+    // flight while the current ones are computed.
+    float2 xf[4][2];
+    {
+      const uint2 h0 = load_row(r0 - 3), h1 = load_row(r0 - 2), h2 = load_row(r0 - 1);
+      unpack(h0, xf[1]);
+      unpack(h1, xf[2]);
+      unpack(h2, xf[3]);
     }
+    uint2 cur[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[i] = load_row(r0 + i);
+#pragma unroll 1
+    for (int hh = 0; hh < 8; ++hh) {
+      const int rb = r0 + 4 * hh;
+      uint2 nxt[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nxt[i] = hh < 7 ? load_row(rb + 4 + i) : make_uint2(0, 0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = rb + i;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          xf[q][0] = xf[q + 1][0];
+          xf[q][1] = xf[q + 1][1];
+        }
+        unpack(cur[i], xf[3]);
+        float2 y[2];
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          float2 z = __fmul2_rn(w2[0][p2], xf[0][p2]);
+          z = __ffma2_rn(w2[1][p2], xf[1][p2], z);
+          z = __ffma2_rn(w2[2][p2], xf[2][p2], z);
+          z = __ffma2_rn(w2[3][p2], xf[3][p2], z);
+          // SiLU: z sigmoid(z) = h + h tanh(h), h = z / 2
+          const float2 h2 = __fmul2_rn(z, half2);
+          float2 t;
+          asm("tanh.approx.f32 %0, %1;" : "=f"(t.x) : "f"(h2.x));
+          asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
+          y[p2] = __ffma2_rn(h2, t, h2);
+        }
+        if (seg < 2) {
+          const float2 s2 = __ffma2_rn(y[1], y[1], __fmul2_rn(y[0], y[0]));
+          float ss = s2.x + s2.y;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          // rows past the chunk end get inv = 0, so their q / k are zero
+          const float inv = (r < L ? rsqrtf(ss + a.l2_eps) : 0.f) * scale;
+          const float2 inv2 = make_float2(inv, inv);
+          const __nv_bfloat162 v0 = __float22bfloat162_rn(__fmul2_rn(y[0], inv2));
+          const __nv_bfloat162 v1 = __float22bfloat162_rn(__fmul2_rn(y[1], inv2));
+          const int row = seg == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
+          st_shared_v2(s_base + PrepSmem::KQ + kmaj_off(128, row, 4 * lane),
+                       make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
+                                  *reinterpret_cast<const uint32_t*>(&v1)));
+        } else {
+          const __nv_bfloat162 v0 = __float22bfloat162_rn(y[0]);
+          const __nv_bfloat162 v1 = __float22bfloat162_rn(y[1]);
+          const uint2 val = r < L ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
+                                               *reinterpret_cast<const uint32_t*>(&v1))
+                                  : make_uint2(0, 0);
+          st_shared_v2(s_base + PrepSmem::V + (seg - 2) * 16384 + mnmaj_off(64, 4 * lane, r), val);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
   }
   // Warps 4 and 5 (v, no norm) finish first: they prefetch the group's next item.
@@ -941,23 +943,23 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       H[i] = init ? gstate[(size_t)(32 * grp + i) * D + j] : 0.f;
-    // Shared-memory addresses of this thread's rows, fixed for the whole scan.
-    uint32_t a_ut[2], a_wt[2], a_ht[4];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      a_ut[q] = ScanSmem::B_UT + kmaj_off(128, j, 16 * grp + 8 * q);   // + buffer base
-      a_wt[q] = s_base + ScanSmem::WT + kmaj_off(128, j, 16 * grp + 8 * q);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) a_ht[q] = s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp + 8 * q);
+    // Shared-memory addresses of this thread's rows, fixed for the whole scan.  In a
+    // 128B-swizzled row the consecutive 16-byte pieces q of one 64-column block sit at
+    // (first piece) ^ 16 q, so only the first address is kept.
+    const uint32_t a_ut0 = ScanSmem::B_UT + kmaj_off(128, j, 16 * grp);   // + buffer base
+    const uint32_t a_wt0 = s_base + ScanSmem::WT + kmaj_off(128, j, 16 * grp);
+    const uint32_t a_ht0 = s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp);
     constexpr uint32_t WTT_OFF = ScanSmem::WTT - ScanSmem::WT;
     // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
-    // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
-    const size_t o_lane = ((size_t)(16 * grp + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) + 8 * (lane & 3);
-    const size_t o_row = (size_t)a.h_v * D;   // elements between consecutive tokens
+    const uint32_t o_row = (uint32_t)a.h_v * D;   // elements between consecutive tokens
+    // this lane's first output element of chunk 0; advanced by C rows per chunk
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                        ((size_t)(start + 16 * grp + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) +
+                        8 * (lane & 3);
+    const int Tbi = (int)Tb;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      st_shared_v4(a_ht[q],
+      st_shared_v4((a_ht0 ^ (16u * q)),
                    make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
                               pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                               pack_bf16(H[8 * q + 6], H[8 * q + 7])));
@@ -965,23 +967,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(hready);
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o);
     for (int c = 0; c < nch; ++c) {
       if (*s_abort) break;
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
       const uint32_t ex = buf + ScanSmem::B_EXP;   // e^{gamma} [64] | e^{gamma_C - gamma} [64] | e^{gamma_C}
       const uint32_t txo = tmem + lbase + TXO + 128 * s;
-      const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
+      const int L = min(C, Tbi - c * C);
       if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
-      // Everything the W step reads from shared memory, loaded while X is computed.
-      const uint4 ut0 = ld_shared_v4(buf + a_ut[0]), ut1 = ld_shared_v4(buf + a_ut[1]);
-      float edv[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 f = ld_shared_f4(ex + 4 * (64 + 16 * grp + 4 * q));
-        edv[4 * q] = f.x; edv[4 * q + 1] = f.y; edv[4 * q + 2] = f.z; edv[4 * q + 3] = f.w;
-      }
+      // U and the decay are loaded while X is computed (the decay factors per row
+      // after X: holding them across the wait costs registers).
+      const uint4 ut0 = ld_shared_v4(buf + a_ut0), ut1 = ld_shared_v4(buf + (a_ut0 ^ 16u));
       const float dec = ld_shared_f32(ex + 4 * 128);
       if (!mbar_wait(bar_x, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
@@ -989,6 +985,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       {
         float X[16];
         tmem_ld16(txo + 16 * grp, X);
+        float edv[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = ld_shared_f4(ex + 4 * (64 + 16 * grp + 4 * q));
+          edv[4 * q] = f.x; edv[4 * q + 1] = f.y; edv[4 * q + 2] = f.z; edv[4 * q + 3] = f.w;
+        }
         uint4 wpk[2];   // W^T in bf16, stored after the chain's tile
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -1002,7 +1004,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
           }
           wpk[q] = make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
                               pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7]));
-          st_shared_v4(a_wt[q] + WTT_OFF,
+          st_shared_v4((a_wt0 ^ (16u * q)) + WTT_OFF,
                        make_uint4(pack_bf16(wt[0], wt[1]), pack_bf16(wt[2], wt[3]),
                                   pack_bf16(wt[4], wt[5]), pack_bf16(wt[6], wt[7])));
         }
@@ -1011,8 +1013,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(wready);
-        st_shared_v4(a_wt[0], wpk[0]);
-        st_shared_v4(a_wt[1], wpk[1]);
+        st_shared_v4(a_wt0, wpk[0]);
+        st_shared_v4(a_wt0 ^ 16u, wpk[1]);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(wtready);
@@ -1035,7 +1037,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        st_shared_v4(a_ht[q],
+        st_shared_v4((a_ht0 ^ (16u * q)),
                      make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
                                 pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                                 pack_bf16(H[8 * q + 6], H[8 * q + 7])));
@@ -1067,17 +1069,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       }
       __syncwarp();
       {
-        __nv_bfloat16* ob = out + (size_t)(start + (int64_t)c * C) * o_row + o_lane;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {            // rows e = lane/4 and lane/4 + 8
           const int e = (lane >> 2) + 8 * q;
           if (16 * grp + e < L)
-            *reinterpret_cast<uint4*>(ob + (size_t)(8 * q) * o_row) =
+            *reinterpret_cast<uint4*>(ob + 8 * q * o_row) =
                 *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * (lane & 3));
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with buffer s
+      ob += (size_t)C * o_row;
     }
     if (!*s_abort) {
 #pragma unroll
