@@ -325,7 +325,8 @@ __device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item,
 // nb spans the group, nb+1 and nb+2 its two 128-thread halves.
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
                                           int slot, unsigned char* sm, int tid, int nb,
-                                          uint64_t* bar, uint32_t ph, uint32_t tmem, int next) {
+                                          uint64_t* bar, uint32_t ph, uint32_t tmem, int next,
+                                          bool& release_partner) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -497,6 +498,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   fence_async_smem();
   tc_fence_before();
   named_bar(nb, 256);
+  if (release_partner) {   // first item of group 0: the other group may start now
+    asm volatile("bar.arrive 7, 512;" ::: "memory");
+    release_partner = false;
+  }
   tc_fence_after();
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
@@ -760,19 +765,25 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   const int n_items = nch * a.h_k;
   uint32_t ph = 0;
   // Static round-robin over the (chunk, key head) items in chunk-major order:
-  // group g takes items g, g + G, g + 2G, ... (G groups), so each wave of
-  // items finishes the earliest chunks first.
+  // in round r, group k of CTA i takes item r G + k n + i (n CTAs, G = 2n
+  // groups), so each round finishes the earliest chunks first.  Group 1 starts
+  // once group 0 has finished its first front end: the two groups then stay
+  // about half an item apart, which spreads their memory traffic, and the
+  // first chunks run on SMs with one busy group.
   const int n_groups = 2 * (int)gridDim.x;
-  for (int item = 2 * (int)blockIdx.x + k; item < n_items; item += n_groups) {
+  bool release_partner = k == 0;
+  if (k == 1) named_bar(7, 512);
+  for (int item = k * (int)gridDim.x + (int)blockIdx.x; item < n_items; item += n_groups) {
     const int32_t gc = item / a.h_k;
     const int hk = item % a.h_k;
     const int b = find_seq(a.chunk_off, a.num_seqs, gc);
     const int slot = a.slot_idx[b];
     if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
     const int next = item + n_groups < n_items ? item + n_groups : -1;
-    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem, next);
+    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem, next, release_partner);
     ph ^= 1u;
   }
+  if (release_partner) asm volatile("bar.arrive 7, 512;" ::: "memory");   // group 0 ran no item
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(s_tmem, 512);
