@@ -108,8 +108,14 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
+// Named CTA barrier over n threads.  The non-aligned form counts each thread
+// on its own, so it stays correct when a warp reaches it diverged (after an
+// `if (tid == 0)` block, say); the aligned form counts whole warps.
 __device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // Bulk async copies (no tensor map): global -> shared with mbarrier
@@ -400,16 +406,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       uint2 nxt[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) nxt[i] = hh < 7 ? load_row(rb + 4 + i) : make_uint2(0, 0);
+      float2 y[4][2];   // SiLU(conv) of the step's 4 tokens, channel pairs
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = rb + i;
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           xf[q][0] = xf[q + 1][0];
           xf[q][1] = xf[q + 1][1];
         }
         unpack(cur[i], xf[3]);
-        float2 y[2];
 #pragma unroll
         for (int p2 = 0; p2 < 2; ++p2) {
           float2 z = __fmul2_rn(w2[0][p2], xf[0][p2]);
@@ -421,25 +426,48 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
           float2 t;
           asm("tanh.approx.f32 %0, %1;" : "=f"(t.x) : "f"(h2.x));
           asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
-          y[p2] = __ffma2_rn(h2, t, h2);
+          y[i][p2] = __ffma2_rn(h2, t, h2);
         }
-        if (seg < 2) {
-          const float2 s2 = __ffma2_rn(y[1], y[1], __fmul2_rn(y[0], y[0]));
-          float ss = s2.x + s2.y;
+      }
+      if (seg < 2) {
+        // Squared norms of the 4 tokens over the warp's 32 lanes with 6
+        // exchanges instead of 20: at xor 16 and xor 8 each lane hands over the
+        // tokens its partner keeps, so afterwards lane l holds token
+        // 2 (l >> 4 & 1) + (l >> 3 & 1); three more levels finish that sum.
+        float ps[4];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-          // rows past the chunk end get inv = 0, so their q / k are zero
-          const float inv = (r < L ? rsqrtf(ss + a.l2_eps) : 0.f) * scale;
+        for (int i = 0; i < 4; ++i) {
+          const float2 s2 = __ffma2_rn(y[i][1], y[i][1], __fmul2_rn(y[i][0], y[i][0]));
+          ps[i] = s2.x + s2.y;
+        }
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
+        const float g0 = __shfl_xor_sync(0xffffffffu, b4 ? ps[0] : ps[2], 16);
+        const float g1 = __shfl_xor_sync(0xffffffffu, b4 ? ps[1] : ps[3], 16);
+        const float q0 = (b4 ? ps[2] : ps[0]) + g0;   // token 2 b4
+        const float q1 = (b4 ? ps[3] : ps[1]) + g1;   // token 2 b4 + 1
+        float tot = (b3 ? q1 : q0) + __shfl_xor_sync(0xffffffffu, b3 ? q0 : q1, 8);
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        const float invl = rsqrtf(tot + a.l2_eps) * scale;   // this lane's token
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = rb + i;
+          // token i's value sits in lane 8 i; rows past the chunk end get 0
+          const float inv = r < L ? __shfl_sync(0xffffffffu, invl, 8 * i) : 0.f;
           const float2 inv2 = make_float2(inv, inv);
-          const __nv_bfloat162 v0 = __float22bfloat162_rn(__fmul2_rn(y[0], inv2));
-          const __nv_bfloat162 v1 = __float22bfloat162_rn(__fmul2_rn(y[1], inv2));
+          const __nv_bfloat162 v0 = __float22bfloat162_rn(__fmul2_rn(y[i][0], inv2));
+          const __nv_bfloat162 v1 = __float22bfloat162_rn(__fmul2_rn(y[i][1], inv2));
           const int row = seg == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
           st_shared_v2(s_base + PrepSmem::KQ + kmaj_off(128, row, 4 * lane),
                        make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
                                   *reinterpret_cast<const uint32_t*>(&v1)));
-        } else {
-          const __nv_bfloat162 v0 = __float22bfloat162_rn(y[0]);
-          const __nv_bfloat162 v1 = __float22bfloat162_rn(y[1]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = rb + i;
+          const __nv_bfloat162 v0 = __float22bfloat162_rn(y[i][0]);
+          const __nv_bfloat162 v1 = __float22bfloat162_rn(y[i][1]);
           const uint2 val = r < L ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
                                                *reinterpret_cast<const uint32_t*>(&v1))
                                   : make_uint2(0, 0);
@@ -499,7 +527,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   tc_fence_before();
   named_bar(nb, 256);
   if (release_partner) {   // first item of group 0: the other group may start now
-    asm volatile("bar.arrive 7, 512;" ::: "memory");
+    named_arrive(7, 512);
     release_partner = false;
   }
   tc_fence_after();
@@ -783,7 +811,7 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
     prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem, next, release_partner);
     ph ^= 1u;
   }
-  if (release_partner) asm volatile("bar.arrive 7, 512;" ::: "memory");   // group 0 ran no item
+  if (release_partner) named_arrive(7, 512);   // group 0 ran no item
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(s_tmem, 512);
