@@ -108,14 +108,28 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
-// Named CTA barrier over n threads.  The non-aligned form counts each thread
-// on its own, so it stays correct when a warp reaches it diverged (after an
-// `if (tid == 0)` block, say); the aligned form counts whole warps.
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void named_arrive(int id, int n) {
-  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Barrier among the warps of an item group (or of one head's four warps) on a
+// shared-memory mbarrier that expects one arrival per warp: the warp
+// reconverges, lane 0 arrives, everyone waits (bounded) for the phase.  Each
+// thread keeps the phase parity it waits for.
+struct WarpSet {
+  uint32_t bar;     // shared-memory address of the mbarrier
+  uint32_t phase;
+};
+__device__ __forceinline__ bool warpset_sync(WarpSet& w, int lane) {
+  __syncwarp();
+  if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(w.bar) : "memory");
+  uint32_t ok = 0;
+  for (uint32_t i = 0; i < WAIT_LIMIT && !ok; ++i)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(w.bar), "r"(w.phase)
+        : "memory");
+  w.phase ^= 1u;
+  return ok != 0;
 }
 
 // Bulk async copies (no tensor map): global -> shared with mbarrier
@@ -326,13 +340,14 @@ __device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item,
 // and 256 TMEM columns each, so one group's latency-bound phases overlap the
 // other's.
 // One (chunk, key head) work item, run by a group of 256 threads (thread
-// index tid) on its own shared memory `sm`, its own two mbarriers (completing
-// once per item; parity ph) and 256 TMEM columns from `tmem`.  Named barrier
-// nb spans the group, nb+1 and nb+2 its two 128-thread halves.
+// index tid) on its own shared memory `sm`, its own two MMA mbarriers
+// (completing once per item; parity ph) and 256 TMEM columns from `tmem`.
+// grp8 synchronises the group's 8 warps, head4 the 4 warps of one value head.
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
-                                          int slot, unsigned char* sm, int tid, int nb,
+                                          int slot, unsigned char* sm, int tid, WarpSet& grp8,
+                                          WarpSet& head4,
                                           uint64_t* bar, uint32_t ph, uint32_t tmem, int next,
-                                          bool& release_partner) {
+                                          bool& release_partner, uint64_t* release_bar) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -525,9 +540,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   }
   fence_async_smem();
   tc_fence_before();
-  named_bar(nb, 256);
+  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   if (release_partner) {   // first item of group 0: the other group may start now
-    named_arrive(7, 512);
+    if (lane == 0) mbar_arrive(release_bar);
     release_partner = false;
   }
   tc_fence_after();
@@ -588,7 +603,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     }
   }
   tc_fence_before();
-  named_bar(nb, 256);
+  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   // ---- T = (I + A)^-1 in place, per value head: 4 warps per head ----
   // With 16 x 16 blocks b: T_bb = (I + A_bb)^-1 by forward substitution (fp32),
   // then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then the lower-left
@@ -623,7 +638,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
         for (int r = 0; r < 16; ++r) AT[(o + r) * S + o + j] = x[r];
       }
     }
-    named_bar(nb + 1 + g, 128);
+    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     if (wb < 2) {  // T_10 (warp 0) and T_32 (warp 1)
       const int i = 1 + 2 * wb;   // block row; column block i - 1
       float* Rw = Rt + wb * 16 * RS;
@@ -635,7 +650,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       mma16x16(e, AT + 16 * i * S + 16 * i, S, Rw, RS, lane);
       store16x16(AT + 16 * i * S + 16 * (i - 1), S, e, -1.f, lane);
     }
-    named_bar(nb + 1 + g, 128);
+    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     const int bi = 2 + (wb >> 1), bj = wb & 1;   // this warp's block of the lower-left 32 x 32
     {  // R_ij = A_i0 T_0j + A_i1 T_1j  (T_01 = 0)
       float d[2][4] = {};
@@ -643,14 +658,14 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       mma16x16(d, AT + 16 * bi * S + 16, S, AT + 16 * S + 16 * bj, S, lane);
       store16x16(Rt + wb * 16 * RS, RS, d, 1.f, lane);
     }
-    named_bar(nb + 1 + g, 128);
+    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     {  // T_ij = -(sum_{k = 2..i} T_ik R_kj)
       float d[2][4] = {};
       if (bi == 3) mma16x16(d, AT + 48 * S + 32, S, Rt + bj * 16 * RS, RS, lane);
       mma16x16(d, AT + 16 * bi * S + 16 * bi, S, Rt + ((bi - 2) * 2 + bj) * 16 * RS, RS, lane);
       store16x16(AT + 16 * bi * S + 16 * bj, S, d, -1.f, lane);
     }
-    named_bar(nb + 1 + g, 128);
+    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int chunk = gt + 128 * q;
@@ -659,7 +674,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? AT[r * S + s0 + k] : 0.f;
     }
   }
-  named_bar(nb, 256);  // both heads' T read: the B-operand tiles overwrite the whole region
+  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);  // both heads' T read: the B-operand tiles overwrite the whole region
   {
     const int g = warp >> 2, gt = tid & 127;
     const uint32_t bu = s_base + PrepSmem::AT + 8192 * g;
@@ -684,7 +699,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   }
   fence_async_smem();
   tc_fence_before();
-  named_bar(nb, 256);
+  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   if (tid == 0) {
 #pragma unroll
@@ -746,7 +761,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     bulk_wait_all();
     fence_proxy_async_global();
   }
-  named_bar(nb, 256);
+  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   if (tid == 0) {
     __threadfence();
     st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
@@ -764,14 +779,23 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   unsigned char* sm0 = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t s_bar[4];
+  // per group: 2 MMA barriers, the 8-warp group barrier, 2 head barriers;
+  // then the barrier group 1 waits on before its first item
+  __shared__ __align__(8) uint64_t s_bar[11];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int i = 0; i < 4; ++i) mbar_init(&s_bar[i], 1);
+    for (int g2 = 0; g2 < 2; ++g2) {
+      mbar_init(&s_bar[5 * g2], 1);
+      mbar_init(&s_bar[5 * g2 + 1], 1);
+      mbar_init(&s_bar[5 * g2 + 2], 8);
+      mbar_init(&s_bar[5 * g2 + 3], 4);
+      mbar_init(&s_bar[5 * g2 + 4], 4);
+    }
+    mbar_init(&s_bar[10], 8);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -788,7 +812,8 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   const int k = tid >> 8, lt = tid & 255;
   unsigned char* sm = sm0 + k * PREP_HALF;
   const uint32_t tmem = s_tmem + 256 * k;
-  const int nb = 1 + 3 * k;
+  WarpSet grp8{smem_u32(&s_bar[5 * k + 2]), 0u};
+  WarpSet head4{smem_u32(&s_bar[5 * k + 3 + ((lt >> 7) & 1)]), 0u};   // warps 0-3: head 0, 4-7: head 1
   const int32_t nch = a.chunk_off[a.num_seqs];
   const int n_items = nch * a.h_k;
   uint32_t ph = 0;
@@ -800,7 +825,7 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   // first chunks run on SMs with one busy group.
   const int n_groups = 2 * (int)gridDim.x;
   bool release_partner = k == 0;
-  if (k == 1) named_bar(7, 512);
+  if (k == 1 && !mbar_wait(&s_bar[10], 0, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   for (int item = k * (int)gridDim.x + (int)blockIdx.x; item < n_items; item += n_groups) {
     const int32_t gc = item / a.h_k;
     const int hk = item % a.h_k;
@@ -808,10 +833,11 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
     const int slot = a.slot_idx[b];
     if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
     const int next = item + n_groups < n_items ? item + n_groups : -1;
-    prep_item(a, gc, hk, b, slot, sm, lt, nb, &s_bar[2 * k], ph, tmem, next, release_partner);
+    prep_item(a, gc, hk, b, slot, sm, lt, grp8, head4, &s_bar[5 * k], ph, tmem, next, release_partner,
+              &s_bar[10]);
     ph ^= 1u;
   }
-  if (release_partner) named_arrive(7, 512);   // group 0 ran no item
+  if (release_partner && (lt & 31) == 0) mbar_arrive(&s_bar[10]);   // group 0 ran no item
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(s_tmem, 512);
