@@ -1107,13 +1107,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
                                 pack_bf16(H[8 * q + 4], H[8 * q + 5]),
                                 pack_bf16(H[8 * q + 6], H[8 * q + 7])));
       fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hready);
+      // o = e^{gamma} O1 + O2.  The next chunk's MMAs write the other [X | O1]
+      // buffer; O2 and this buffer are rewritten only after every thread's
+      // next W arrival, which follows these reads.
       if (!mbar_wait(bar_o, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
       float O1[16], O2[16];
       tmem_ld16x2(txo + 64 + 16 * grp, O1, tmem + lbase + TO2 + 16 * grp, O2);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(hready);
       // Stage this warp's 16 x 32 block of o in its own 1 KiB of the buffer's
       // U tile (read in the W phase, free now), then write it as 16-byte
       // pieces (8 values of one row each).
