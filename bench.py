@@ -376,6 +376,26 @@ def config_of(inp):
             "parallelism": "replicas (no cross-GPU exchange in the layer)"}
 
 
+# ---------------------------------------------------------------- replicas
+
+def max_over_ranks(dist, world, v, device):
+    """The largest of each rank's value (one all-reduce; the value itself
+    when there is one rank).  Timings take this so the slowest replica sets
+    the job time."""
+    if world == 1:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, units_per_rank, ms):
+    """Whole-job units per second when every rank processes its own replica
+    of `units_per_rank` units and the job takes `ms` milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(args):
@@ -450,18 +470,14 @@ def run_gdn(args):
         return 0
     e2e = None if args.no_e2e else bench_e2e(torch, gdn, pf["run"], args.steps, args.warmup)
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_ranks(v):
+        return max_over_ranks(dist, world, v, device)
 
     inp = pf["inp"]
     d = inp["dims"]
     T = inp["x"].shape[0]
-    ms = max_over_ranks(statistics.mean(pf["step_ms"]))
-    value = world * T / (ms / 1e3)
+    ms = max_ranks(statistics.mean(pf["step_ms"]))
+    value = replica_throughput(world, T, ms)
     flops_launch = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
     # The method's FLOPs by the stage that performs them: the chunk stage does
     # K K^T, Q K^T, T (beta V), T (beta e^gamma K) (8 C d per token and head),
@@ -479,7 +495,7 @@ def run_gdn(args):
     peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     roof = None
     if dom and stage_flops.get(dom):
-        dom_ms = max_over_ranks(stage[dom])
+        dom_ms = max_ranks(stage[dom])
         ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": ach / peak_tf,
@@ -492,6 +508,9 @@ def run_gdn(args):
                 "launch_ms": dom_ms, "flops_per_launch": stage_flops[dom]}
     stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()
                     if stage_flops.get(k)}
+    if dec:   # collectives: every rank takes part
+        dms = max_ranks(statistics.mean(dec["step_ms"]))
+        lms = max_ranks(statistics.mean(dec["layer_ms"]))
     out = None
     if rank == 0:
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -507,13 +526,12 @@ def run_gdn(args):
             "device_status": pf["status"],
         }
         if e2e:
-            line["e2e"] = {"value": world * T / (max_over_ranks(e2e["ms"]) / 1e3),
+            line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],
                            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
         if dec:
-            dms = statistics.mean(dec["step_ms"])
-            lms = statistics.mean(dec["layer_ms"])
-            gbs = dec["state_bytes"] / (dms / 1e3) / 1e9
+            # whole job: every rank moves its own replica's state bytes
+            gbs = replica_throughput(world, dec["state_bytes"], dms) / 1e9
             lgbs = dec["state_bytes"] / dec["layers"] / (lms / 1e3) / 1e9
             line["decode"] = {
                 "metric": "decode state GB/s", "value": gbs, "unit": "GB/s",
