@@ -258,7 +258,7 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
             if tr.stages_run & (1 << i):
                 vals.append(e["b"][i].elapsed_time(e["f"][i]))
         if vals:
-            stage_ms[name] = statistics.mean(vals)
+            stage_ms[name] = statistics.median(vals)
     status = int(run.status.item())
     return {"inp": inp, "run": run, "step_ms": step_ms, "stage_ms": stage_ms,
             "launches": launches, "status": status}
@@ -373,6 +373,7 @@ def config_of(inp):
             "d_k": d.d_k, "d_v": d.d_v, "conv_dim": d.conv_dim, "conv_w": d.conv_w,
             "chunk": d.chunk, "io": d.io, "state": "fp32, zero initial",
             "l2": "flushed by a 256 MiB write before every timed step",
+            "timing": "median of the K timed steps (CUDA events per step)",
             "parallelism": "replicas (no cross-GPU exchange in the layer)"}
 
 
@@ -462,8 +463,8 @@ def run_gdn(args):
     clocks = sampler.stop()
     if pf is None:
         if rank == 0 and dec is not None:
-            print(json.dumps({"decode_only": True, "ms_per_step": statistics.mean(dec["step_ms"]),
-                              "layer_ms": statistics.mean(dec["layer_ms"]),
+            print(json.dumps({"decode_only": True, "ms_per_step": statistics.median(dec["step_ms"]),
+                              "layer_ms": statistics.median(dec["layer_ms"]),
                               "state_bytes": dec["state_bytes"], "clocks": clocks}), flush=True)
         if world > 1:
             dist.destroy_process_group()
@@ -476,7 +477,7 @@ def run_gdn(args):
     inp = pf["inp"]
     d = inp["dims"]
     T = inp["x"].shape[0]
-    ms = max_ranks(statistics.mean(pf["step_ms"]))
+    ms = max_ranks(statistics.median(pf["step_ms"]))   # median of the K steps
     value = replica_throughput(world, T, ms)
     flops_launch = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
     # The method's FLOPs by the stage that performs them: the chunk stage does
@@ -509,8 +510,8 @@ def run_gdn(args):
     stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()
                     if stage_flops.get(k)}
     if dec:   # collectives: every rank takes part
-        dms = max_ranks(statistics.mean(dec["step_ms"]))
-        lms = max_ranks(statistics.mean(dec["layer_ms"]))
+        dms = max_ranks(statistics.median(dec["step_ms"]))
+        lms = max_ranks(statistics.median(dec["layer_ms"]))
     out = None
     if rank == 0:
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
