@@ -61,6 +61,8 @@ def _load():
     lib.oracle_gdn_layer.argtypes = [i64, i64, i64, i64, i64, p, p, p, p, p, p,
                                      p, i64, p, p, p, dbl, p, p, p, ctypes.c_int]
     lib.oracle_gdn_layer.restype = ctypes.c_int
+    lib.oracle_gated_rmsnorm.argtypes = [i64, i64, p, p, p, dbl, p]
+    lib.oracle_gated_rmsnorm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -173,3 +175,18 @@ def layer(x, a, b, conv_weight, A_log, dt_bias, cu_seqlens, h_k, h_v, d_k, d_v,
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
+
+
+def gated_rmsnorm(o, z, weight, eps=1e-6):
+    """Gated RMSNorm of the layer output: o, z [..., d_v] -> y float64 with
+    y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z) over the last axis."""
+    lib = _load()
+    o, z, weight = map(_f32, (o, z, weight))
+    shape = o.shape
+    d_v = shape[-1]
+    rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    y = np.zeros(shape)
+    rc = lib.oracle_gated_rmsnorm(rows, d_v, _ptr(o), _ptr(z), _ptr(weight), float(eps), _ptr(y))
+    if rc:
+        raise RuntimeError(f"oracle_gated_rmsnorm failed ({rc})")
+    return y

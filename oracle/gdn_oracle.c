@@ -333,3 +333,27 @@ int oracle_gdn_layer(int64_t h_k, int64_t h_v, int64_t d_k, int64_t d_v,
   free(tasks);
   return J.err;
 }
+
+/* ------------------------------------------------------------------ */
+/* Gated RMSNorm of the layer output (the DeltaNet "gated norm").     */
+/* Per row of d_v values (one token, one value head):                 */
+/*   y_j = o_j / sqrt(mean_j o_j^2 + eps) * w_j * SiLU(z_j)            */
+/* The weight is applied as stored: of the model's norms only this    */
+/* one carries no pre-added +1 (oxydllm 0.0.0-alpha.12.2 release      */
+/* notes, New Features, "GGUF qwen35 architecture"); the gated RMSNorm */
+/* runs over the whole token batch after the scan ("Gated DeltaNet    */
+/* fast paths").  The mean runs over the head's d_v values.           */
+int oracle_gated_rmsnorm(int64_t rows, int64_t d_v, const float* o, const float* z,
+                         const float* w, double eps, double* y) {
+  if (rows < 0 || d_v <= 0 || !o || !z || !w || !y) return -1;
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* orow = o + r * d_v;
+    const float* zrow = z + r * d_v;
+    double ss = 0.0;
+    for (int64_t j = 0; j < d_v; ++j) ss += (double)orow[j] * (double)orow[j];
+    const double inv = 1.0 / sqrt(ss / (double)d_v + eps);
+    for (int64_t j = 0; j < d_v; ++j)
+      y[r * d_v + j] = (double)orow[j] * inv * (double)w[j] * silu((double)zrow[j]);
+  }
+  return 0;
+}

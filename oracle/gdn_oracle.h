@@ -102,6 +102,12 @@ int oracle_gdn_layer(int64_t h_k, int64_t h_v, int64_t d_k, int64_t d_v,
                      double* o, double* state_out, double* window_out,
                      int n_threads);
 
+/* Gated RMSNorm over rows of d_v values: y [rows][d_v] float64 from o, z
+ * [rows][d_v] and the per-channel weight w [d_v] (applied as stored).
+ * Returns 0, or -1 on bad arguments. */
+int oracle_gated_rmsnorm(int64_t rows, int64_t d_v, const float* o, const float* z,
+                         const float* w, double eps, double* y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,6 +32,12 @@ MUTATIONS = {
                      "window0[(-tau - 1) * conv_dim + c]"),
     # softplus with the wrong sign inside
     "softplus_sign": ("log1p(exp(-fabs(z)))", "log1p(exp(fabs(z)))"),
+    # gated norm: sum of squares instead of their mean
+    "norm_sum_not_mean": ("sqrt(ss / (double)d_v + eps)", "sqrt(ss + eps)"),
+    # gated norm: a +1 pre-added to the weight
+    "norm_weight_plus_one": ("inv * (double)w[j] * silu", "inv * (1.0 + (double)w[j]) * silu"),
+    # gated norm: sigmoid gate instead of SiLU
+    "norm_sigmoid_gate": ("(double)w[j] * silu((double)zrow[j])", "(double)w[j] * sigmoid((double)zrow[j])"),
     # output read without the current token's write
     "output_before_write": (
         "for (int64_t i = 0; i < d_k; ++i) acc += S[j * d_k + i] * q[i];",

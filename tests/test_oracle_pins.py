@@ -306,3 +306,47 @@ def test_layer_matches_per_head_pipeline_and_threads_are_deterministic():
     assert np.array_equal(rm["o"][lo:hi, h], r1["o"][lo:hi, h])
     assert np.array_equal(rm["state"][s, h], r1["state"][s, h])
     assert not rm["o"][lo:hi, h - 1].any()
+
+
+# ---- gated RMSNorm of the output (the DeltaNet "gated norm") ------------------
+
+def _norm_case(rows=5, d_v=32, seed=21):
+    rng = np.random.default_rng(seed)
+    o = rng.standard_normal((rows, d_v)).astype(np.float32)
+    z = rng.standard_normal((rows, d_v)).astype(np.float32)
+    w = rng.uniform(0.25, 2.0, d_v).astype(np.float32)
+    return o, z, w
+
+
+def test_gated_norm_closed_gate_is_zero():
+    """SiLU(0) = 0: a zero gate gives a zero output whatever o and the weight."""
+    o, z, w = _norm_case()
+    assert not oracle.gated_rmsnorm(o, np.zeros_like(z), w).any()
+
+
+def test_gated_norm_constant_row_closed_form():
+    """A row of one value c has mean square c^2, so
+    y_j = c / sqrt(c^2 + eps) * w_j * z_j * sigmoid(z_j)  (library sigmoid)."""
+    _, z, w = _norm_case(rows=3)
+    for c, eps in ((0.7, 1e-6), (-3.0, 0.0), (2e-3, 1e-6)):
+        o = np.full_like(z, c)
+        c = np.float64(np.float32(c))   # the value o actually holds
+        ref = c / np.sqrt(c ** 2 + eps) * w.astype(np.float64) * \
+            z.astype(np.float64) * expit(z.astype(np.float64))
+        np.testing.assert_allclose(oracle.gated_rmsnorm(o, z, w, eps=eps), ref, rtol=1e-12,
+                                   atol=1e-15)
+
+
+def test_gated_norm_unit_rms_scale_invariance_and_weight_linearity():
+    """With eps = 0, unit weight and an open gate (z = 40, SiLU(z) = 40 to
+    1e-17), y / 40 has root mean square exactly 1; scaling o does not change y;
+    y is linear in the weight, channel by channel, with no offset."""
+    o, z, w = _norm_case()
+    zo = np.full_like(z, 40.0)
+    y = oracle.gated_rmsnorm(o, zo, np.ones_like(w), eps=0.0) / 40.0
+    np.testing.assert_allclose(np.sqrt(np.mean(y ** 2, axis=-1)), 1.0, rtol=1e-12)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(4.0 * o, z, w, eps=0.0),
+                               oracle.gated_rmsnorm(o, z, w, eps=0.0), rtol=1e-12)
+    y1 = oracle.gated_rmsnorm(o, z, w)
+    y2 = oracle.gated_rmsnorm(o, z, 2.0 * w)
+    np.testing.assert_allclose(y2, 2.0 * y1, rtol=1e-12)
