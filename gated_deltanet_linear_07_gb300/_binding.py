@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_prefill_noalloc.restype = ctypes.c_int
     lib.gdn_decode_step.argtypes = [D, PR, P, P, P, P, I32, P, P, I64, P, P, P]
     lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_gated_rmsnorm.argtypes = [D, P, ctypes.c_float, P, P, I64, P, P]
+    lib.gdn_gated_rmsnorm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -253,3 +255,22 @@ def gdn_decode_step(dims, conv_weight, A_log, dt_bias, x, a, b, slot_idx, state_
                                 _ptr(slot_idx), n, _ptr(state_pool), _ptr(conv_pool), num_slots,
                                 _ptr(o), _ptr(d_status), _stream(stream))
     _check("gdn_decode_step", rc)
+
+
+def gdn_gated_rmsnorm(dims, weight, o, z, y=None, eps=1e-6, stream=None):
+    """Gated RMSNorm of the layer output (see gdn_gated_rmsnorm in
+    include/gdn.h): o, z [n, h_v, d_v] in the I/O dtype, weight [d_v] fp32;
+    y defaults to o (in place).  Returns y."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    n = int(o.numel()) // (d.h_v * d.d_v) if d.h_v * d.d_v else 0
+    y = o if y is None else y
+    _expect(weight, "weight", torch.float32, d.d_v)
+    _expect(o, "o", io, n * d.h_v * d.d_v)
+    _expect(z, "z", io, n * d.h_v * d.d_v)
+    _expect(y, "y", io, n * d.h_v * d.d_v)
+    rc = load().gdn_gated_rmsnorm(ctypes.byref(d), _ptr(weight), float(eps), _ptr(o), _ptr(z), n,
+                                  _ptr(y), _stream(stream))
+    _check("gdn_gated_rmsnorm", rc)
+    return y

@@ -122,6 +122,21 @@ GDN_EXPORT int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
   return cuda_rc(gdn_launch_conv_update(a, dims->io, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+GDN_EXPORT int gdn_gated_rmsnorm(const gdn_dims* dims, const float* weight, float eps,
+                                 const void* o, const void* z, int64_t n, void* y,
+                                 gdn_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (n < 0 || !(eps >= 0.f)) return GDN_EINVAL;
+  if (dims->d_v != 16 && dims->d_v != 32 && dims->d_v != 64 && dims->d_v != 128)
+    return GDN_EUNSUPPORTED;
+  if (n == 0) return GDN_OK;
+  if (!weight || !o || !z || !y) return GDN_EINVAL;
+  if (!aligned16(weight) || !aligned16(o) || !aligned16(z) || !aligned16(y)) return GDN_EALIGN;
+  return cuda_rc(gdn_launch_gated_rmsnorm(weight, eps, o, z, n * dims->h_v, dims->d_v, dims->io, y,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                              int32_t num_seqs) {
   if (check_prefill_dims(dims) != GDN_OK || total_tokens < 0 || num_seqs < 0) return 0;

@@ -133,6 +133,8 @@ struct GdnPrefillArgs {
 cudaError_t gdn_launch_decode(const GdnDecodeArgs& a, int d_k, int d_v, int io,
                               cudaStream_t s);
 cudaError_t gdn_launch_conv_update(const GdnConvArgs& a, int io, cudaStream_t s);
+cudaError_t gdn_launch_gated_rmsnorm(const float* weight, float eps, const void* o, const void* z,
+                                     int64_t rows, int d_v, int io, void* y, cudaStream_t s);
 cudaError_t gdn_launch_prefill_simt(const GdnPrefillArgs& a, int io, cudaStream_t s,
                                     gdn_trace* trace);
 

@@ -114,6 +114,25 @@ int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
                       const int32_t* slot_idx, int32_t n, void* y,
                       int32_t* d_status, gdn_stream_t stream);
 
+/*
+ * gdn_gated_rmsnorm -- the DeltaNet "gated norm" on the layer output, for
+ * every row of d_v values (one token, one value head):
+ *   y[r][j] = o[r][j] / sqrt(mean_j o[r][j]^2 + eps) * weight[j] * SiLU(z[r][j])
+ * The weight is applied as stored: of the model's norms only this one has no
+ * pre-added +1 (oxydllm notes, New Features, "GGUF qwen35 architecture"); it
+ * runs once over the whole token batch after the layer ("Gated DeltaNet fast
+ * paths").  Used after gdn_prefill and after gdn_decode_step alike.
+ *   weight     [d_v] fp32 (device)
+ *   o, z       [n][h_v][d_v] IO (device)
+ *   y          [n][h_v][d_v] IO (device); may be o itself (in place)
+ * Uses dims->h_v, d_v (16, 32, 64 or 128) and io.  Returns GDN_EINVAL (null
+ * pointer, n < 0, eps < 0), GDN_EUNSUPPORTED (d_v) or GDN_EALIGN (a pointer
+ * not 16-byte aligned) without launching anything.  The caller owns every
+ * buffer.
+ */
+int gdn_gated_rmsnorm(const gdn_dims* dims, const float* weight, float eps, const void* o,
+                      const void* z, int64_t n, void* y, gdn_stream_t stream);
+
 /* Bytes of device workspace gdn_prefill needs for this shape (0 on bad dims). */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                   int32_t num_seqs);

@@ -119,6 +119,22 @@ def test_decode_and_conv_reject_bad_calls_before_launch(lib):
                                  None) == 0
 
 
+def test_gated_rmsnorm_rejects_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    call = lambda **kw: lib.gdn_gated_rmsnorm(  # noqa: E731
+        ctypes.byref(kw.get("dims", d)), kw.get("w", FAKE), ctypes.c_float(kw.get("eps", 1e-6)),
+        kw.get("o", FAKE), kw.get("z", FAKE), kw.get("n", 4), kw.get("y", FAKE), None)
+    assert call(dims=gdn.make_dims(**dict(D4B, d_v=48))) == -2
+    assert call(o=None) == -1
+    assert call(z=None) == -1
+    assert call(n=-1) == -1
+    assert call(eps=-1.0) == -1
+    assert call(eps=float("nan")) == -1
+    assert call(n=0) == 0
+    assert call(w=FAKE + 4) == -5
+    assert call(y=FAKE + 8) == -5
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
