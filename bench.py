@@ -4,7 +4,8 @@
 One step = one gdn_prefill call over the Qwen3.5-4B-shaped layer workload
 (B=1, T=4096, H_k=16 -> H_v=32, d_k=d_v=128, conv over 8192 channels, bf16
 I/O, fp32 state, chunk 64, zero initial state), inputs resident in HBM, L2
-flushed (a 256 MiB write) before every timed step.  The same JSON line also
+flushed before every timed step (a 256 MiB write, then a 256 MiB read so the
+write-backs land outside the timed region).  The same JSON line also
 carries the decode step (24 layers x 64 slots, one bf16 token per slot,
 shuffled slots, random fp32 states) as a second measured quantity, the
 end-to-end figure through the C ABI with host buffers, the roofline of the
@@ -145,6 +146,21 @@ def gpu_id_of(torch, dev_index):
 
 # ---------------------------------------------------------------- workloads
 
+class L2Flush:
+    """Before a timed call: write a buffer larger than L2 (evicting the
+    inputs), then read another one, so the write's dirty lines are written
+    back before the timed region instead of inside it."""
+
+    def __init__(self, torch, device):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty(1, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        self.sink.copy_(self.r.sum().reshape(1))
+
+
 def alg_flops_per_token_head(C, d):
     """Method FLOPs per (token, value head): five C x C x d contractions
     (K K^T, Q K^T, T (beta V), T (beta e^gamma K), P W) and three C x d x d
@@ -219,7 +235,7 @@ class Prefill:
 def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     inp = workloads.prefill_4b()
     run = Prefill(torch, gdn, inp, device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(torch, device)
     ns = gdn.STAGES
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     for _ in range(max(warmup, 1)):
@@ -234,7 +250,7 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     torch.cuda.synchronize()
     # Timed pass: the plain call, events only around each step.
     for e in ev:
-        flush.fill_(1.0)
+        flush()
         e["s"].record(stream)
         run()
         e["e"].record(stream)
@@ -245,7 +261,7 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     launches = 0
     traces = []
     for e in ev:
-        flush.fill_(1.0)
+        flush()
         tr = gdn.make_trace(e["b"], e["f"])
         run(trace=tr)
         launches += tr.launches
@@ -299,6 +315,31 @@ def bench_e2e(torch, gdn, run, steps, warmup):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
+
+
+def bench_gated_norm(torch, gdn, dims, T, device, steps, warmup):
+    """Gated RMSNorm of a T-token layer output (o, z [T, h_v, d_v] in the I/O
+    dtype, out of place), L2 flushed before every timed call."""
+    io = torch.bfloat16 if dims.io == "bf16" else torch.float32
+    g = torch.Generator(device=device).manual_seed(1234)
+    o = torch.randn((T, dims.h_v, dims.d_v), generator=g, device=device).to(io)
+    z = torch.randn((T, dims.h_v, dims.d_v), generator=g, device=device).to(io)
+    w = torch.rand(dims.d_v, generator=g, device=device) + 0.5
+    y = torch.empty_like(o)
+    flush = L2Flush(torch, device)
+    for _ in range(max(warmup, 1)):
+        gdn.gdn_gated_rmsnorm(dims, w, o, z, y=y)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for a_, b_ in ev:
+        flush()
+        a_.record()
+        gdn.gdn_gated_rmsnorm(dims, w, o, z, y=y)
+        b_.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in ev)
+    nbytes = 3 * o.numel() * o.element_size()
+    return {"ms": ms, "bytes": nbytes, "rows": T * dims.h_v}
 
 
 def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64):
@@ -372,7 +413,7 @@ def config_of(inp):
             "B": len(inp["lengths"]), "T": int(inp["x"].shape[0]), "h_k": d.h_k, "h_v": d.h_v,
             "d_k": d.d_k, "d_v": d.d_v, "conv_dim": d.conv_dim, "conv_w": d.conv_w,
             "chunk": d.chunk, "io": d.io, "state": "fp32, zero initial",
-            "l2": "flushed by a 256 MiB write before every timed step",
+            "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
             "timing": "median of the K timed steps (CUDA events per step)",
             "parallelism": "replicas (no cross-GPU exchange in the layer)"}
 
@@ -455,6 +496,11 @@ def run_gdn(args):
     if not args.no_prefill:
         pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
         barrier()
+    gn = None
+    if pf is not None:
+        gn = bench_gated_norm(torch, gdn, pf["inp"]["dims"], pf["inp"]["x"].shape[0], device,
+                              args.steps, args.warmup)
+        barrier()
     dec = None
     if not args.no_decode:
         dec = bench_decode(torch, gdn, workloads, device, args.decode_steps or args.steps,
@@ -530,6 +576,18 @@ def run_gdn(args):
             line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],
                            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+        if gn:
+            ggbs = gn["bytes"] / (gn["ms"] / 1e3) / 1e9
+            line["gated_norm"] = {
+                "metric": "gated RMSNorm of the layer output, GB/s", "value": ggbs, "unit": "GB/s",
+                "ms_per_call": gn["ms"],
+                "config": {"workload": f"o, z [{T}, {d.h_v}, {d.d_v}] {d.io}, out of place",
+                           "bytes_per_call": gn["bytes"],
+                           "l2": "flushed before every timed call (256 MiB written, then 256 MiB read)"},
+                "roofline": {"bound": "hbm", "achieved": ggbs, "peak": hbm, "unit": "GB/s",
+                             "frac": ggbs / hbm, "traffic": None,
+                             "kernel": "gated_rmsnorm_kernel", "peak_source": f"hbm_gbs ({peak_src})",
+                             "launch_ms": gn["ms"]}}
         if dec:
             # whole job: every rank moves its own replica's state bytes
             gbs = replica_throughput(world, dec["state_bytes"], dms) / 1e9
