@@ -173,6 +173,7 @@ KERNEL_SOURCES = {
     "prefill_scan": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "prefill_chunk": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "prefill_overlap": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
+    "gated_norm": ("gdn_norm.cu", "gdn_common.cuh"),
 }
 
 
@@ -585,7 +586,7 @@ def run_gdn(args):
                            "bytes_per_call": gn["bytes"],
                            "l2": "flushed before every timed call (256 MiB written, then 256 MiB read)"},
                 "roofline": {"bound": "hbm", "achieved": ggbs, "peak": hbm, "unit": "GB/s",
-                             "frac": ggbs / hbm, "traffic": None,
+                             "frac": ggbs / hbm, "traffic": recorded_traffic("gated_norm"),
                              "kernel": "gated_rmsnorm_kernel", "peak_source": f"hbm_gbs ({peak_src})",
                              "launch_ms": gn["ms"]}}
         if dec:

@@ -77,9 +77,11 @@ __global__ void __launch_bounds__(256) gated_rmsnorm_kernel(const float* __restr
     const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float zz = zv[i + k];
-      const float silu = zz / (1.0f + __expf(-zz));   // IEEE division: -0 when e^{-z} = inf
-      yv[i + k] = ov[i + k] * inv * wv[k] * silu;
+      // SiLU(z) = h + h tanh(h), h = z / 2 (saturates cleanly in both tails)
+      const float h = 0.5f * zv[i + k];
+      float t;
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+      yv[i + k] = ov[i + k] * inv * wv[k] * fmaf(h, t, h);
     }
   }
   if (live) V::store(reinterpret_cast<IO*>(y) + off, yv);
