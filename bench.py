@@ -389,6 +389,9 @@ def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=
             "layers": layers, "slots": slots, "status": int(status.item())}
 
 
+CPU_BASELINE_SECONDS = 10.0
+
+
 def oracle_prefill_time(inp, n_threads):
     import oracle
     d = inp["dims"]
@@ -608,11 +611,15 @@ def run_gdn(args):
                 "device_status": dec["status"]}
         if not args.no_cpu_baseline and world == 1:
             cores = os.cpu_count() or 1
-            secs = oracle_prefill_time(inp, cores)
-            line["cpu_baseline"] = {"value": T / secs, "unit": "tokens/s", "cores": cores,
-                                    "kind": "oracle",
-                                    "sample": f"the whole workload once ({T} tokens x {d.h_v} heads), "
-                                              f"{secs:.2f} s"}
+            # whole-workload passes until about 10 s of oracle time have run
+            passes, secs = 0, 0.0
+            while passes == 0 or secs < CPU_BASELINE_SECONDS:
+                secs += oracle_prefill_time(inp, cores)
+                passes += 1
+            line["cpu_baseline"] = {"value": passes * T / secs, "unit": "tokens/s",
+                                    "cores": cores, "kind": "oracle",
+                                    "sample": f"{passes} passes over the whole workload "
+                                              f"({T} tokens x {d.h_v} heads each), {secs:.1f} s"}
         out = line
     if world > 1:
         dist.barrier()
