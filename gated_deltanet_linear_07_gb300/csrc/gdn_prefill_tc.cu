@@ -844,30 +844,38 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
 }
 
 // ---------------------------------------------------------------------------
-// scan: one CTA (576 threads) per (sequence, value head).
+// scan: one CTA (704 threads) per (sequence, value head).
 //   warp 0: bulk loads of chunk inputs (two buffers)
-//   warp 1: MMA issue, three groups per chunk:
-//             [X | O1] = H^T [Wk; Q]^T       (N = 128, TMEM double-buffered)
-//             dH       = Wt^T K              (N = 128; Wt = diag(e^{gamma_C-gamma}) W)
-//             O2       = W^T P^T             (N = 64)
-//   warps 2..17: epilogue; warp w owns TMEM lanes 32*(w%4).., and group
-//               (w-2)/4 takes one quarter of the columns.
+//   warp 1: MMA issue, four groups per chunk, every A operand in tensor memory
+//           (bf16, written by the chain warps), every B operand in shared memory:
+//             X  = H^T Wk^T                  (N = 64)
+//             O1 = H^T Q^T                   (N = 64, double-buffered)
+//             dH = Wt^T K                    (N = 128; Wt = diag(e^{gamma_C-gamma}) W)
+//             O2 = W^T P^T                   (N = 64)
+//   warps 2..17: the state chain (W and the H update); warp w owns TMEM lanes
+//               32*(w%4).., and group (w-2)/4 takes one quarter of the columns.
+//   warps 18..21: the output o = e^gamma O1 + O2 of the previous chunk, written
+//               while the chain warps work on the next one.
 
 struct ScanSmem {
   // per buffer: P (K-major 64 x 64) | UT | EXP | K (K-major 64 x 128, used MN-major) |
   //             B1 = [Wk; Q] (K-major 128 x 128)
+  // B1 is released once X and O1 have read it, the rest once O2 and the chain
+  // warps have; the output warps read e^gamma from a copy of their own.
   static constexpr uint32_t BUF = 74752;
   static constexpr uint32_t B_P = 0, B_UT = 8192, B_EXP = 24576, B_K = 25600, B_B1 = 41984;
-  static constexpr uint32_t HT = 2 * BUF;     // 32768, K-major 128 x 128
-  static constexpr uint32_t WT = HT + 32768;  // 16384, K-major 128 x 64: W^T
-  static constexpr uint32_t WTT = WT + 16384; // 16384: W^T diag(e^{gamma_C - gamma})
-  static constexpr uint32_t BAR = WTT + 16384;
-  static constexpr uint32_t SIZE = BAR + 256;
+  static constexpr uint32_t REST = B_B1;      // bytes of P | UT | EXP | K
+  static constexpr uint32_t BAR = 2 * BUF;
+  static constexpr uint32_t OST = BAR + 256;  // output staging, 2 KiB per output warp
+  static constexpr uint32_t EG = OST + 8192;  // e^{gamma} [64] x 2 buffers
+  static constexpr uint32_t SIZE = EG + 512;
 };
-// TMEM columns: [X | O1] x 2 buffers, dH, O2
-constexpr uint32_t TXO = 0, TDH = 256, TO2 = 384;
-constexpr int SCAN_THREADS = 576;
-constexpr uint32_t EPI_THREADS = 512;
+// TMEM columns (fp32 accumulators, then the bf16 A operands, two per column):
+//   X [64] | O1 x 2 [64] | dH [128] | O2 [64] | H^T [64] | Wt^T [32] | W^T [32]
+constexpr uint32_t TX = 0, TO1 = 64, TDH = 192, TO2 = 320, THT = 384, TWT = 448, TW = 480;
+constexpr int SCAN_THREADS = 704;
+constexpr uint32_t EPI_THREADS = 512;   // the chain warps
+constexpr uint32_t OUT_WARPS = 4;
 
 __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -888,14 +896,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   const bool init = a.has_init ? a.has_init[b] != 0 : false;
   const uint32_t s_base = smem_u32(sm);
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + ScanSmem::BAR);      // [2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + ScanSmem::BAR);      // [2] P|UT|EXP|K
   uint64_t* empty = full + 2;                                             // [2]
   uint64_t* bar_x = full + 4;
   uint64_t* bar_dh = full + 5;
   uint64_t* wready = full + 6;
   uint64_t* hready = full + 7;
-  uint64_t* bar_o = full + 8;
-  uint64_t* wtready = full + 11;
+  uint64_t* bar_o = full + 12;                                            // [2]
+  uint64_t* ofree = full + 14;                                            // [2]
+  uint64_t* full_b1 = full + 16;                                          // [2] [Wk; Q]
+  uint64_t* empty_b1 = full + 18;                                         // [2]
+  uint64_t* full_eg = full + 20;                                          // [2] e^gamma copy
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 9);
   volatile int* s_abort = reinterpret_cast<volatile int*>(full + 10);
 
@@ -906,15 +917,24 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   if (tid == 32) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    // a buffer is free once its MMAs are done and every epilogue warp has
-    // finished staging its output in the buffer's (consumed) U tile
+    // P|UT|EXP|K of a buffer is free once its MMAs are done and every chain
+    // warp has read U and the decays; [Wk; Q] once X and O1 are done
     mbar_init(&empty[0], 1 + EPI_THREADS / 32);
     mbar_init(&empty[1], 1 + EPI_THREADS / 32);
+    mbar_init(&full_b1[0], 1);
+    mbar_init(&full_b1[1], 1);
+    mbar_init(&empty_b1[0], 1);
+    mbar_init(&empty_b1[1], 1);
+    mbar_init(&full_eg[0], 1);
+    mbar_init(&full_eg[1], 1);
     mbar_init(bar_x, 1);
     mbar_init(bar_dh, 1);
-    mbar_init(bar_o, 1);
-    mbar_init(wtready, EPI_THREADS / 32);
-    // one arrival per epilogue warp, after the warp's writes are fenced
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    // the output warps have read O1 and O2 of a TMEM buffer and their e^gamma copy
+    mbar_init(&ofree[0], OUT_WARPS);
+    mbar_init(&ofree[1], OUT_WARPS);
+    // one arrival per chain warp, after its tensor-memory stores are complete
     mbar_init(wready, EPI_THREADS / 32);
     mbar_init(hready, EPI_THREADS / 32);
     *s_abort = 0;
@@ -936,7 +956,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     if (lane == 0) {
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
-        if (c >= 2 && !mbar_wait(&empty[s], ((c >> 1) - 1) & 1, WAIT_LIMIT)) { fail(); break; }
+        const uint32_t rel = ((c >> 1) - 1) & 1;   // phase of the release two chunks back
         if (*s_abort) break;
         const uint32_t dst = s_base + s * ScanSmem::BUF;
         {  // the chunk's records are published by the prep (possibly still running)
@@ -948,13 +968,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         }
         const unsigned char* vrec = a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC;
         const unsigned char* qrec = a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * Q_REC;
-        mbar_expect_tx(&full[s], ScanSmem::BUF);
+        if (c >= 2 && !mbar_wait(&empty_b1[s], rel, WAIT_LIMIT)) { fail(); break; }
+        mbar_expect_tx(&full_b1[s], ScanSmem::BUF - ScanSmem::REST);
+        bulk_g2s(dst + ScanSmem::B_B1, vrec + WK_OFF, 8192, &full_b1[s]);          // Wk K-block 0
+        bulk_g2s(dst + ScanSmem::B_B1 + 16384, vrec + WK_OFF + 8192, 8192, &full_b1[s]);  // 1
+        bulk_g2s(dst + ScanSmem::B_B1 + 8192, qrec, 8192, &full_b1[s]);            // Q K-block 0
+        bulk_g2s(dst + ScanSmem::B_B1 + 24576, qrec + 8192, 8192, &full_b1[s]);    // block 1
+        if (c >= 2 && !mbar_wait(&empty[s], rel, WAIT_LIMIT)) { fail(); break; }
+        mbar_expect_tx(&full[s], ScanSmem::REST);
         bulk_g2s(dst, vrec, VH_HEAD, &full[s]);                                   // P|UT|EXP
         bulk_g2s(dst + ScanSmem::B_K, qrec + K_IN_QREC, K_IN_QREC, &full[s]);      // K
-        bulk_g2s(dst + ScanSmem::B_B1, vrec + WK_OFF, 8192, &full[s]);             // Wk K-block 0
-        bulk_g2s(dst + ScanSmem::B_B1 + 16384, vrec + WK_OFF + 8192, 8192, &full[s]);  // block 1
-        bulk_g2s(dst + ScanSmem::B_B1 + 8192, qrec, 8192, &full[s]);               // Q K-block 0
-        bulk_g2s(dst + ScanSmem::B_B1 + 24576, qrec + 8192, 8192, &full[s]);       // block 1
+        if (c >= 2 && !mbar_wait(&ofree[s], rel, WAIT_LIMIT)) { fail(); break; }
+        mbar_expect_tx(&full_eg[s], 256);
+        bulk_g2s(s_base + ScanSmem::EG + 256 * s, vrec + EXP_OFF, 256, &full_eg[s]);
       }
     }
   } else if (warp == 1) {
@@ -963,44 +989,49 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       constexpr uint32_t ID_XO = idesc_bf16(128, 64, false, false);
       constexpr uint32_t ID_DH = idesc_bf16(128, 128, false, true);
       constexpr uint32_t ID_O2 = idesc_bf16(128, 64, false, false);
-      const uint64_t d_ht = sdesc_kmaj(s_base + ScanSmem::HT, 128, 0);
-      const uint64_t d_wt = sdesc_kmaj(s_base + ScanSmem::WT, 128, 0);
-      const uint64_t d_wtt = sdesc_kmaj(s_base + ScanSmem::WTT, 128, 0);
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t buf = s_base + s * ScanSmem::BUF;
         const uint64_t d_b1 = sdesc_kmaj(buf + ScanSmem::B_B1, 128, 0);
         const uint64_t d_k = sdesc_mnmaj(buf + ScanSmem::B_K, 64, 0);
         const uint64_t d_p = sdesc_kmaj(buf + ScanSmem::B_P, 64, 0);
-        if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT) ||
-            !mbar_wait(hready, c & 1, WAIT_LIMIT)) { fail(); break; }
+        // Only the two hand-offs of the chain are waited on here, polled without
+        // suspending: every barrier operation of this thread is slow while the
+        // other warps are busy, so the chain warps certify the rest.  hready (from
+        // chain warp 2) also means that [Wk; Q] of this chunk has landed and that
+        // O1's buffer has been read; wready that P | U | EXP | K has landed.
+        if (!mbar_spin(hready, c & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
+        // A operands advance 16 K elements = 8 columns per step; B operands are
+        // 128B-swizzled K-major tiles of 64-element K blocks.
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // X = H^T Wk^T first: it is on the chain
-          mma_bf16(tmem + TXO + 128 * s, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
+          mma_bf16_ts(tmem + TX, tmem + THT + 8 * ks,
+                      sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(bar_x);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T (completes with bar_o)
-          mma_bf16(tmem + TXO + 128 * s + 64, sdesc_add(d_ht, (ks >> 2) * 16384 + (ks & 3) * 32),
-                   sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
-        if (!mbar_wait(wready, c & 1, WAIT_LIMIT)) { fail(); break; }
+        for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T
+          mma_bf16_ts(tmem + TO1 + 64 * s, tmem + THT + 8 * ks,
+                      sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
+        mma_commit(&empty_b1[s]);
+        if (!mbar_spin(wready, c & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
-          mma_bf16(tmem + TDH, sdesc_add(d_wtt, ks * 32), sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
+          mma_bf16_ts(tmem + TDH, tmem + TWT + 8 * ks, sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
         mma_commit(bar_dh);
-        if (!mbar_wait(wtready, c & 1, WAIT_LIMIT)) { fail(); break; }
+        // O2 rewrites what the output warps read for the previous chunk
+        if (c >= 1 && !mbar_wait(&ofree[s ^ 1], ((c - 1) >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
-          mma_bf16(tmem + TO2, sdesc_add(d_wt, ks * 32), sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
-        mma_commit(bar_o);
+          mma_bf16_ts(tmem + TO2, tmem + TW + 8 * ks, sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
+        mma_commit(&bar_o[s]);
         mma_commit(&empty[s]);
       }
     }
-  } else {
-    // ---------------- epilogue ----------------
+  } else if (warp < 2 + (int)(EPI_THREADS / 32)) {
+    // ---------------- state chain ----------------
     const int grp = (warp - 2) >> 2;            // 0..3
     const uint32_t lbase = (uint32_t)(32 * (warp & 3)) << 16;
     const int j = 32 * (warp & 3) + lane;       // TMEM lane = value index
@@ -1008,27 +1039,24 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       H[i] = init ? gstate[(size_t)(32 * grp + i) * D + j] : 0.f;
-    // Shared-memory addresses of this thread's rows, fixed for the whole scan.  In a
-    // 128B-swizzled row the consecutive 16-byte pieces q of one 64-column block sit at
-    // (first piece) ^ 16 q, so only the first address is kept.
+    // Shared-memory address of this thread's U^T row piece, fixed for the whole scan.
+    // In a 128B-swizzled row the consecutive 16-byte pieces q of one 64-column block
+    // sit at (first piece) ^ 16 q, so only the first address is kept.
     const uint32_t a_ut0 = ScanSmem::B_UT + kmaj_off(128, j, 16 * grp);   // + buffer base
-    const uint32_t a_wt0 = s_base + ScanSmem::WT + kmaj_off(128, j, 16 * grp);
-    const uint32_t a_ht0 = s_base + ScanSmem::HT + kmaj_off(128, j, 32 * grp);
-    constexpr uint32_t WTT_OFF = ScanSmem::WTT - ScanSmem::WT;
-    // output: this warp's 16 x 32 block, lane writes rows e = lane/4 (+8), 8 values at 8*(lane%4)
-    const uint32_t o_row = (uint32_t)a.h_v * D;   // elements between consecutive tokens
-    // this lane's first output element of chunk 0; advanced by C rows per chunk
-    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o) +
-                        ((size_t)(start + 16 * grp + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) +
-                        8 * (lane & 3);
-    const int Tbi = (int)Tb;
+    // this thread's bf16 A-operand columns: H^T[j][32 grp ..], W^T[j][16 grp ..]
+    const uint32_t t_ht = tmem + lbase + THT + 16 * grp;
+    const uint32_t t_wt = tmem + lbase + TWT + 8 * grp;
+    const uint32_t t_w = tmem + lbase + TW + 8 * grp;
+    {
+      uint32_t hp[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4((a_ht0 ^ (16u * q)),
-                   make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
-                              pack_bf16(H[8 * q + 4], H[8 * q + 5]),
-                              pack_bf16(H[8 * q + 6], H[8 * q + 7])));
-    fence_async_smem();
+      for (int e = 0; e < 16; ++e) hp[e] = pack_bf16(H[2 * e], H[2 * e + 1]);
+      tmem_st16(t_ht, hp);
+    }
+    // warp 2 certifies, through its hready arrivals, what the MMA issuer would
+    // otherwise wait for: the next chunk's [Wk; Q] landed, its O1 buffer read
+    if (warp == 2 && nch > 0 && !mbar_wait(&full_b1[0], 0, WAIT_LIMIT)) fail();
+    tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(hready);
@@ -1037,8 +1065,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
       const uint32_t ex = buf + ScanSmem::B_EXP;   // e^{gamma} [64] | e^{gamma_C - gamma} [64] | e^{gamma_C}
-      const uint32_t txo = tmem + lbase + TXO + 128 * s;
-      const int L = min(C, Tbi - c * C);
       if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
       // U and the decay are loaded while X is computed (the decay factors per row
       // after X: holding them across the wait costs registers).
@@ -1046,43 +1072,45 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       const float dec = ld_shared_f32(ex + 4 * 128);
       if (!mbar_wait(bar_x, c & 1, WAIT_LIMIT)) { fail(); break; }
       tc_fence_after();
-      // W^T = U^T - X for r in this group's quarter
+      // W^T = U^T - X for r in this group's quarter, and Wt^T = W^T diag(e^{gamma_C - gamma})
       {
         float X[16];
-        tmem_ld16(txo + 16 * grp, X);
+        tmem_ld16(tmem + lbase + TX + 16 * grp, X);
         float edv[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 f = ld_shared_f4(ex + 4 * (64 + 16 * grp + 4 * q));
           edv[4 * q] = f.x; edv[4 * q + 1] = f.y; edv[4 * q + 2] = f.z; edv[4 * q + 3] = f.w;
         }
-        uint4 wpk[2];   // W^T in bf16, stored after the chain's tile
+        uint32_t wp[8], wtp[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           float u[8];
           bf16x8_to_float(q == 0 ? ut0 : ut1, u);
-          float wv[8], wt[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            wv[e] = u[e] - X[8 * q + e];
-            wt[e] = wv[e] * edv[8 * q + e];
+          for (int e = 0; e < 8; e += 2) {
+            const float w0 = u[e] - X[8 * q + e], w1 = u[e + 1] - X[8 * q + e + 1];
+            wp[4 * q + e / 2] = pack_bf16(w0, w1);
+            wtp[4 * q + e / 2] = pack_bf16(w0 * edv[8 * q + e], w1 * edv[8 * q + e + 1]);
           }
-          wpk[q] = make_uint4(pack_bf16(wv[0], wv[1]), pack_bf16(wv[2], wv[3]),
-                              pack_bf16(wv[4], wv[5]), pack_bf16(wv[6], wv[7]));
-          st_shared_v4((a_wt0 ^ (16u * q)) + WTT_OFF,
-                       make_uint4(pack_bf16(wt[0], wt[1]), pack_bf16(wt[2], wt[3]),
-                                  pack_bf16(wt[4], wt[5]), pack_bf16(wt[6], wt[7])));
         }
-        // (the X read is ordered before later MMAs into this buffer by the
-        // tcgen05 fence ahead of the next hready arrival)
-        fence_async_smem();
+        tmem_st8(t_wt, wtp);
+        tmem_st8(t_w, wp);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(wready);
-        st_shared_v4(a_wt0, wpk[0]);
-        st_shared_v4(a_wt0 ^ 16u, wpk[1]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wtready);
+        if (lane == 0) {
+          mbar_arrive(wready);
+          mbar_arrive(&empty[s]);   // U and the decays of buffer s are read
+        }
+      }
+      if (warp == 2 && c + 1 < nch) {   // idle until dH: certify the next chunk's inputs
+        const int s1 = (c + 1) & 1;
+        if (!mbar_wait(&full_b1[s1], ((c + 1) >> 1) & 1, WAIT_LIMIT) ||
+            (c + 1 >= 2 && !mbar_wait(&ofree[s1], (((c + 1) >> 1) - 1) & 1, WAIT_LIMIT))) {
+          fail();
+          break;
+        }
       }
 
       if (!mbar_wait(bar_dh, c & 1, WAIT_LIMIT)) { fail(); break; }
@@ -1100,58 +1128,70 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
           H[2 * e + 1] = r2.y;
         }
       }
+      {
+        uint32_t hp[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_shared_v4((a_ht0 ^ (16u * q)),
-                     make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
-                                pack_bf16(H[8 * q + 4], H[8 * q + 5]),
-                                pack_bf16(H[8 * q + 6], H[8 * q + 7])));
-      fence_async_smem();
+        for (int e = 0; e < 16; ++e) hp[e] = pack_bf16(H[2 * e], H[2 * e + 1]);
+        tmem_st16(t_ht, hp);
+      }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(hready);
-      // o = e^{gamma} O1 + O2.  The next chunk's MMAs write the other [X | O1]
-      // buffer; O2 and this buffer are rewritten only after every thread's
-      // next W arrival, which follows these reads.
-      if (!mbar_wait(bar_o, c & 1, WAIT_LIMIT)) { fail(); break; }
-      tc_fence_after();
-      float O1[16], O2[16];
-      tmem_ld16x2(txo + 64 + 16 * grp, O1, tmem + lbase + TO2 + 16 * grp, O2);
-      // Stage this warp's 16 x 32 block of o in its own 1 KiB of the buffer's
-      // U tile (read in the W phase, free now), then write it as 16-byte
-      // pieces (8 values of one row each).
-      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + s * ScanSmem::BUF + ScanSmem::B_UT +
-                                                            (warp - 2) * 1024);
-      float eg[16];   // e^{gamma_r} of this group's rows
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 f = ld_shared_f4(ex + 4 * (16 * grp + 4 * q));
-        eg[4 * q] = f.x; eg[4 * q + 1] = f.y; eg[4 * q + 2] = f.z; eg[4 * q + 3] = f.w;
-      }
-#pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        const float2 o2 = __ffma2_rn(make_float2(eg[e], eg[e + 1]), make_float2(O1[e], O1[e + 1]),
-                                     make_float2(O2[e], O2[e + 1]));
-        ost[e * 32 + lane] = __float2bfloat16_rn(o2.x);
-        ost[(e + 1) * 32 + lane] = __float2bfloat16_rn(o2.y);
-      }
-      __syncwarp();
-      {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {            // rows e = lane/4 and lane/4 + 8
-          const int e = (lane >> 2) + 8 * q;
-          if (16 * grp + e < L)
-            *reinterpret_cast<uint4*>(ob + 8 * q * o_row) =
-                *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * (lane & 3));
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with buffer s
-      ob += (size_t)C * o_row;
     }
     if (!*s_abort) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) gstate[(size_t)(32 * grp + i) * D + j] = H[i];
+    }
+  } else {
+    // ---------------- output ----------------
+    // o[t][h][j] = e^{gamma_r} O1[j][r] + O2[j][r] for the chunk's tokens r.  This
+    // warp holds the values j = 32 (w % 4) + lane; it stages 16 tokens at a time in
+    // its own 2 KiB (two 1 KiB halves, alternating) and writes them as 16-byte
+    // pieces, 8 values of one token each.
+    const uint32_t lbase = (uint32_t)(32 * (warp & 3)) << 16;
+    const int ow = warp - 2 - (int)(EPI_THREADS / 32);   // 0..3
+    const size_t o_row = (size_t)a.h_v * D;
+    // this lane's piece: token e = lane/4 (+8), values 8 (lane % 4) .. of the warp's 32
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                        ((size_t)(start + (lane >> 2)) * a.h_v + h) * D + 32 * (warp & 3) +
+                        8 * (lane & 3);
+    for (int c = 0; c < nch; ++c) {
+      if (*s_abort) break;
+      const int s = c & 1;
+      const uint32_t ex = s_base + ScanSmem::EG + 256 * s;   // e^{gamma} [64]
+      const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
+      if (!mbar_wait(&full_eg[s], (c >> 1) & 1, WAIT_LIMIT) ||
+          !mbar_wait(&bar_o[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int g = 0; g < C / 16; ++g) {
+        float O1[16], O2[16];
+        tmem_ld16x2(tmem + lbase + TO1 + 64 * s + 16 * g, O1, tmem + lbase + TO2 + 16 * g, O2);
+        float eg[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = ld_shared_f4(ex + 4 * (16 * g + 4 * q));
+          eg[4 * q] = f.x; eg[4 * q + 1] = f.y; eg[4 * q + 2] = f.z; eg[4 * q + 3] = f.w;
+        }
+        __nv_bfloat16* ost =
+            reinterpret_cast<__nv_bfloat16*>(sm + ScanSmem::OST + ow * 2048 + (g & 1) * 1024);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ost[e * 32 + lane] = __float2bfloat16_rn(fmaf(eg[e], O1[e], O2[e]));
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int e = (lane >> 2) + 8 * q;
+          if (16 * g + e < L)
+            *reinterpret_cast<uint4*>(ob + (size_t)(16 * g + 8 * q) * o_row) =
+                *reinterpret_cast<const uint4*>(ost + e * 32 + 8 * (lane & 3));
+        }
+        __syncwarp();   // this half is rewritten two groups later
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofree[s]);
+      ob += (size_t)C * o_row;
     }
   }
   tc_fence_before();
