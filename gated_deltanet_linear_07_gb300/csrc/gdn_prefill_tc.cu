@@ -108,7 +108,7 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
-// Barrier among the warps of an item group (or of one head's four warps) on a
+// Barrier among the warps working on an item (or one head's four warps) on a
 // shared-memory mbarrier that expects one arrival per warp: the warp
 // reconverges, lane 0 arrives, everyone waits (bounded) for the phase.  Each
 // thread keeps the phase parity it waits for.
@@ -306,18 +306,12 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, 
   return lo;
 }
 
-// L2 prefetch of one work item's inputs: the x rows of its q, k and two v
-// segments including the 3-token halo, and its a / b rows, one 128-byte line
-// per request, spread over n threads (thread index i).  Every address lies
-// inside the item's own rows.
-__device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item, int i, int n) {
-  const int32_t gc = item / a.h_k;
-  const int hk = item % a.h_k;
-  const int b = find_seq(a.chunk_off, a.num_seqs, gc);
-  const int64_t start = a.cu_seqlens[b];
-  const int64_t t0 = start + (int64_t)(gc - a.chunk_off[b]) * C;
-  const int64_t t1 = min(t0 + C, (int64_t)a.cu_seqlens[b + 1]);
-  const int64_t r0 = t0 - 3 > start ? t0 - 3 : start;
+// L2 prefetch of one work item's inputs: the x rows [r0, t1) of key head hk's
+// q, k and two v segments (r0 includes the 3-token halo) and the a / b rows
+// [t0, t1), one 128-byte line per request, spread over n threads (thread
+// index i).  The caller keeps the rows inside the input.
+__device__ __forceinline__ void prefetch_rows(const GdnPrefillArgs& a, int hk, int64_t r0,
+                                              int64_t t0, int64_t t1, int i, int n) {
   const size_t cd2 = (size_t)a.conv_dim * 2;
   const unsigned char* x = reinterpret_cast<const unsigned char*>(a.x);
   const size_t seg_q = (size_t)hk * D * 2, seg_k = (size_t)(a.h_k + hk) * D * 2,
@@ -335,19 +329,33 @@ __device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item,
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const unsigned char*>(a.b) + q) : "memory");
   }
 }
+// The same for work item `item` (chunk-major (chunk, key head) index), found
+// through the chunk table.
+__device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item, int i, int n) {
+  const int32_t gc = item / a.h_k;
+  const int hk = item % a.h_k;
+  const int b = find_seq(a.chunk_off, a.num_seqs, gc);
+  const int64_t start = a.cu_seqlens[b];
+  const int64_t t0 = start + (int64_t)(gc - a.chunk_off[b]) * C;
+  const int64_t t1 = min(t0 + C, (int64_t)a.cu_seqlens[b + 1]);
+  prefetch_rows(a, hk, t0 - 3 > start ? t0 - 3 : start, t0, t1, i, n);
+}
 
-// Two item groups per SM: 256 threads, <= 128 registers, ~107 KB shared memory
-// and 256 TMEM columns each, so one group's latency-bound phases overlap the
-// other's.
-// One (chunk, key head) work item, run by a group of 256 threads (thread
-// index tid) on its own shared memory `sm`, its own two MMA mbarriers
-// (completing once per item; parity ph) and 256 TMEM columns from `tmem`.
-// grp8 synchronises the group's 8 warps, head4 the 4 warps of one value head.
+// One (chunk, key head) work item, run by the 16 warps of the CTA (thread index
+// tid, <= 128 registers each) on ~107 KB of shared memory `sm`, two MMA
+// mbarriers (completing once per item; parity ph) and 256 TMEM columns from
+// `tmem`.  One item at a time per SM: the scan starts once the first chunk is
+// published, and a 16-warp item takes about 60 % of the time of two 8-warp
+// items sharing an SM (which would give more items per second, but the scan
+// consumes them no faster than this).  grp synchronises the 16 warps, head4
+// the 4 warps of one value head in the phases that run on warps 0..7 only.
+constexpr int NW = 16;
+constexpr int WPS = NW / 4;             // warps per front-end segment
+constexpr int TPW = C / WPS;            // tokens per front-end warp
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
-                                          int slot, unsigned char* sm, int tid, WarpSet& grp8,
-                                          WarpSet& head4,
-                                          uint64_t* bar, uint32_t ph, uint32_t tmem, int next,
-                                          bool& release_partner, uint64_t* release_bar) {
+                                          int slot, unsigned char* sm, int tid, WarpSet& grp,
+                                          WarpSet& head4, uint64_t* bar, uint32_t ph, uint32_t tmem,
+                                          int next) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -363,13 +371,13 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
-  // ---- front end: conv + SiLU + L2 norm; warp = (segment, 32 tokens), lane = 4 channels ----
+  // ---- front end: conv + SiLU + L2 norm; warp = (segment, TPW tokens), lane = 4 channels ----
   {
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* win =
         reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * cd;
-    const int seg = warp >> 1;          // 0: q, 1: k, 2 / 3: v of value head 2 hk / 2 hk + 1
-    const int r0 = (warp & 1) * 32;
+    const int seg = warp / WPS;         // 0: q, 1: k, 2 / 3: v of value head 2 hk / 2 hk + 1
+    const int r0 = (warp % WPS) * TPW;
     int ch;
     if (seg == 0) ch = hk * D;
     else if (seg == 1) ch = (a.h_k + hk) * D;
@@ -416,11 +424,11 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = load_row(r0 + i);
 #pragma unroll 1
-    for (int hh = 0; hh < 8; ++hh) {
+    for (int hh = 0; hh < TPW / 4; ++hh) {
       const int rb = r0 + 4 * hh;
       uint2 nxt[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) nxt[i] = hh < 7 ? load_row(rb + 4 + i) : make_uint2(0, 0);
+      for (int i = 0; i < 4; ++i) nxt[i] = hh < TPW / 4 - 1 ? load_row(rb + 4 + i) : make_uint2(0, 0);
       float2 y[4][2];   // SiLU(conv) of the step's 4 tokens, channel pairs
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -493,11 +501,12 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
   }
-  // Warps 4 and 5 (v, no norm) finish first: they prefetch the group's next item.
-  if (next >= 0 && (warp == 4 || warp == 5)) prefetch_item(a, next, tid - 128, 64);
-  // ---- gates of the two value heads (warps 6, 7) ----
-  if (warp >= 6) {
-    const int g = warp - 6;
+  // The v warps (no norm) finish first: those of value head 2 hk prefetch the
+  // next item, two of those of value head 2 hk + 1 compute the gates.
+  if (next >= 0 && warp >= 2 * WPS && warp < 3 * WPS) prefetch_item(a, next, tid - 64 * WPS, 32 * WPS);
+  // ---- gates of the two value heads ----
+  if (warp == 3 * WPS || warp == 3 * WPS + 1) {
+    const int g = warp - 3 * WPS;
     const int h = 2 * hk + g;
     const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(a.a);
     const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(a.b);
@@ -540,11 +549,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   }
   fence_async_smem();
   tc_fence_before();
-  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  if (release_partner) {   // first item of group 0: the other group may start now
-    if (lane == 0) mbar_arrive(release_bar);
-    release_partner = false;
-  }
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
@@ -553,9 +558,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
                ks > 0);
     mma_commit(&bar[0]);
   }
-  // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); warp = (head, lanes) ----
+  // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); warp = (32-column
+  //      half, head, lanes) ----
   {
-    const int q = warp & 3, g = warp >> 2;
+    const int q = warp & 3, g = (warp >> 2) & 1;
     const int m = 32 * q + lane;
     const bool ok = mbar_wait(&bar[0], ph, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
@@ -566,8 +572,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     const float br = beta[g * 64 + r];
     float* Arow = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH) + r * S;
     unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {   // 32 columns s at a time
+    {
+      const int hf = warp >> 3;
       float d[32];
       if (ok) {
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, d);
@@ -603,15 +609,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     }
   }
   tc_fence_before();
-  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  // ---- T = (I + A)^-1 in place, per value head: 4 warps per head ----
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  // ---- T = (I + A)^-1 in place, per value head: warps 0..3 and 4..7 ----
   // With 16 x 16 blocks b: T_bb = (I + A_bb)^-1 by forward substitution (fp32),
   // then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then the lower-left
   // 32 x 32 block -T_[23][23] A_[23][01] T_[01][01] (products on the tensor
   // cores in TF32).  Only products of exact blocks, no matrix powers: finite
   // for fully correlated keys.
   float tv[4][8];   // this thread's T entries for the B operands (read before they are overwritten)
-  {
+  if (warp < 8) {
     const int g = warp >> 2, gt = tid & 127, wb = warp & 3;
     float* AT = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
     constexpr int RS = PrepSmem::RST;
@@ -674,8 +680,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? AT[r * S + s0 + k] : 0.f;
     }
   }
-  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);  // both heads' T read: the B-operand tiles overwrite the whole region
-  {
+  // both heads' T read: the B-operand tiles overwrite the whole region
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (warp < 8) {
     const int g = warp >> 2, gt = tid & 127;
     const uint32_t bu = s_base + PrepSmem::AT + 8192 * g;
     const uint32_t bw = s_base + PrepSmem::AT + 16384 + 8192 * g;  // rows 64g.. of [BW_0; BW_1]
@@ -699,7 +706,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   }
   fence_async_smem();
   tc_fence_before();
-  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   if (tid == 0) {
 #pragma unroll
@@ -722,21 +729,25 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     bulk_s2g(qrec + K_IN_QREC + 8192, s_base + PrepSmem::KQ + 16384, 8192);
   }
   // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
+  // Staged as the records' tile images in shared memory that the second MMAs
+  // have finished reading (V and A/T), then written as four 16 KB bulk copies.
+  constexpr uint32_t STG = PrepSmem::V;   // U^T_0 | U^T_1 | Wk_0 | Wk_1, 16 KB each
   {
     const bool ok = mbar_wait(&bar[1], ph, WAIT_LIMIT);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
-    // 16 tasks of (lane quarter, 64 columns); warp w takes tasks w and w+8.
-    for (int task = warp; task < 16 && ok; task += 8) {
+    // 16 tasks of (lane quarter, 64 columns), one per warp
+    if (ok) {
+      const int task = warp;
       const int kind = task >> 2;                // 0,1: U^T_g   2,3: Wk column halves
       const uint32_t col = 64 * kind;
-      unsigned char* dst;
+      uint32_t tile;
       int row, R, c0;
       if (kind < 2) {            // U^T_g row j = m
-        dst = vrec0 + kind * VH_REC + UT_OFF; row = m; R = 128; c0 = 0;
+        tile = STG + 16384 * kind; row = m; R = 128; c0 = 0;
       } else {                   // Wk of head m/64, row r = m%64, columns i in this half
-        dst = vrec0 + (m >> 6) * VH_REC + WK_OFF; row = m & 63; R = 64; c0 = 64 * (kind - 2);
+        tile = STG + 32768 + 16384 * (m >> 6); row = m & 63; R = 64; c0 = 64 * (kind - 2);
       }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -745,57 +756,58 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
           const float* f = &v[8 * ck];
-          *reinterpret_cast<uint4*>(dst + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck)) =
-              make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                         pack_bf16(f[6], f[7]));
+          st_shared_v4(s_base + tile + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck),
+                       make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                  pack_bf16(f[6], f[7])));
         }
       }
     }
   }
-  // Publish the item: every record byte written (generic stores made visible
-  // device-wide, bulk stores completed), then the ready flag with release.
-  // One gpu-scope fence after the group barrier covers every thread's stores
-  // (cumulativity), so only thread 0 waits for them.
+  fence_async_smem();
   tc_fence_before();
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  // Publish the item: every record byte written (bulk stores completed and
+  // made visible device-wide, generic stores fenced), then the ready flag with
+  // release.  One gpu-scope fence after the group barrier covers every thread's
+  // stores (cumulativity), so only thread 0 waits for them.
   if (tid == 32) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      bulk_s2g(vrec0 + g * VH_REC + UT_OFF, s_base + STG + 16384 * g, 16384);
+      bulk_s2g(vrec0 + g * VH_REC + WK_OFF, s_base + STG + 32768 + 16384 * g, 16384);
+    }
     bulk_wait_all();
     fence_proxy_async_global();
   }
-  if (!warpset_sync(grp8, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   if (tid == 0) {
     __threadfence();
     st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
   }
 }
 
-// Persistent prep: one CTA per SM runs two independent 256-thread item
-// pipelines (two halves of shared memory and TMEM), each pulling (chunk, key
-// head) items in chunk-major order from an atomic counter.  It lets dependent
-// grids (the scan) launch at once.
-constexpr uint32_t PREP_HALF = (PrepSmem::SIZE + 1023) / 1024 * 1024;
+// Persistent prep: one CTA per SM, its 16 warps on one (chunk, key head) item
+// at a time.  It lets dependent grids (the scan) launch at once.
+constexpr uint32_t PREP_SMEM = (PrepSmem::SIZE + 1023) / 1024 * 1024;
 
 __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* sm0 = reinterpret_cast<unsigned char*>(
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_tmem;
-  // per group: 2 MMA barriers, the 8-warp group barrier, 2 head barriers;
-  // then the barrier group 1 waits on before its first item
-  __shared__ __align__(8) uint64_t s_bar[11];
+  // 2 MMA barriers, the 16-warp barrier, 2 head barriers
+  __shared__ __align__(8) uint64_t s_bar[5];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
-    tmem_alloc(&s_tmem, 512);
+    tmem_alloc(&s_tmem, 256);
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int g2 = 0; g2 < 2; ++g2) {
-      mbar_init(&s_bar[5 * g2], 1);
-      mbar_init(&s_bar[5 * g2 + 1], 1);
-      mbar_init(&s_bar[5 * g2 + 2], 8);
-      mbar_init(&s_bar[5 * g2 + 3], 4);
-      mbar_init(&s_bar[5 * g2 + 4], 4);
-    }
-    mbar_init(&s_bar[10], 8);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    mbar_init(&s_bar[2], 16);
+    mbar_init(&s_bar[3], 4);
+    mbar_init(&s_bar[4], 4);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -806,41 +818,31 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!a.ws_flag[0]) {
-    if (warp == 0) tmem_dealloc(s_tmem, 512);
+    if (warp == 0) tmem_dealloc(s_tmem, 256);
     return;
   }
-  const int k = tid >> 8, lt = tid & 255;
-  unsigned char* sm = sm0 + k * PREP_HALF;
-  const uint32_t tmem = s_tmem + 256 * k;
-  WarpSet grp8{smem_u32(&s_bar[5 * k + 2]), 0u};
-  WarpSet head4{smem_u32(&s_bar[5 * k + 3 + ((lt >> 7) & 1)]), 0u};   // warps 0-3: head 0, 4-7: head 1
+  WarpSet grp16{smem_u32(&s_bar[2]), 0u};
+  WarpSet head4{smem_u32(&s_bar[3 + ((tid >> 7) & 1)]), 0u};   // warps 0-3: head 0, 4-7: head 1
   const int32_t nch = a.chunk_off[a.num_seqs];
   const int n_items = nch * a.h_k;
+  const int n = (int)gridDim.x;
   uint32_t ph = 0;
   // Static round-robin over the (chunk, key head) items in chunk-major order:
-  // in round r, group k of CTA i takes item r G + k n + i (n CTAs, G = 2n
-  // groups), so each round finishes the earliest chunks first.  Group 1 starts
-  // once group 0 has finished its first front end: the two groups then stay
-  // about half an item apart, which spreads their memory traffic, and the
-  // first chunks run on SMs with one busy group.
-  const int n_groups = 2 * (int)gridDim.x;
-  bool release_partner = k == 0;
-  if (k == 1 && !mbar_wait(&s_bar[10], 0, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  for (int item = k * (int)gridDim.x + (int)blockIdx.x; item < n_items; item += n_groups) {
+  // in round r, CTA i takes item r n + i, so each round finishes the earliest
+  // chunks first.
+  for (int item = (int)blockIdx.x; item < n_items; item += n) {
     const int32_t gc = item / a.h_k;
     const int hk = item % a.h_k;
     const int b = find_seq(a.chunk_off, a.num_seqs, gc);
     const int slot = a.slot_idx[b];
     if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
-    const int next = item + n_groups < n_items ? item + n_groups : -1;
-    prep_item(a, gc, hk, b, slot, sm, lt, grp8, head4, &s_bar[5 * k], ph, tmem, next, release_partner,
-              &s_bar[10]);
+    const int next = item + n < n_items ? item + n : -1;
+    prep_item(a, gc, hk, b, slot, sm, tid, grp16, head4, s_bar, ph, s_tmem, next);
     ph ^= 1u;
   }
-  if (release_partner && (lt & 31) == 0) mbar_arrive(&s_bar[10]);   // group 0 ran no item
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(s_tmem, 512);
+  if (warp == 0) tmem_dealloc(s_tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -1226,7 +1228,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   const int64_t n_scan = (int64_t)a.num_seqs * a.h_v;
   const bool overlap = n_scan <= n_sm / 2;
   const int workers = overlap ? n_sm - (int)n_scan : n_sm;
-  const int psmem = (int)(2 * PREP_HALF) + 1024;
+  const int psmem = (int)PREP_SMEM + 1024;
   const int ssmem = (int)ScanSmem::SIZE + 1024;
   if ((e = cudaFuncSetAttribute(prep_persistent_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess)
