@@ -173,6 +173,54 @@ def layer(x, a, b, conv_weight, A_log, dt_bias, cu_seqlens, h_k, h_v, d_k, d_v,
     return {"o": o, "state": st, "window": win}
 
 
+def slot_copy(state_pool, conv_pool, src, dst):
+    """Snapshot / restore of recurrent state between slots (Vallmo.jl README,
+    src/: the recurrent state is snapshotted and restored for prefix caching;
+    PicoLM changelog, SSM State Checkpointing: capture and restore the full SSM
+    state): for each pair i with src[i] >= 0 and dst[i] >= 0, slot dst[i]
+    receives slot src[i]'s state and conv window.  Pairs apply in order;
+    returns new float64 arrays."""
+    st = np.array(state_pool, dtype=np.float64, copy=True)
+    cw = np.array(conv_pool, dtype=np.float64, copy=True)
+    for s_, d_ in zip(np.asarray(src).ravel(), np.asarray(dst).ravel()):
+        if s_ >= 0 and d_ >= 0:
+            st[d_] = st[s_]
+            cw[d_] = cw[s_]
+    return st, cw
+
+
+def prefill_checkpoints(x, a, b, conv_weight, A_log, dt_bias, cu_seqlens, h_k, h_v, d_k, d_v,
+                        every, window0=None, state0=None, l2_eps=L2_EPS):
+    """Interval checkpoints of a prefill (PicoLM changelog, SSM State
+    Checkpointing: checkpoints every N tokens during prefill; on reuse the
+    closest one is restored and the remaining tokens are processed again).
+    For sequence b and every k >= 1 with k * every < len_b: the state (S^T) and
+    conv window after the first k * every tokens of the sequence, the
+    sequence's initial state and window included -- by definition, the layer
+    run on that prefix.  Returns a list over sequences of (states [n_b, h_v,
+    d_k, d_v], windows [n_b, W-1, conv_dim]), n_b = ceil(len_b / every) - 1."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    B = cu.shape[0] - 1
+    conv_dim = np.asarray(x).shape[1]
+    conv_w = np.asarray(conv_weight).shape[1]
+    out = []
+    for bi in range(B):
+        s0, ln = int(cu[bi]), int(cu[bi + 1] - cu[bi])
+        n_b = max(0, -(-ln // every) - 1)
+        states = np.zeros((n_b, h_v, d_k, d_v))
+        windows = np.zeros((n_b, conv_w - 1, conv_dim))
+        for k in range(1, n_b + 1):
+            t = k * every
+            r = layer(x[s0:s0 + t], a[s0:s0 + t], b[s0:s0 + t], conv_weight, A_log, dt_bias,
+                      [0, t], h_k, h_v, d_k, d_v,
+                      window0=None if window0 is None else window0[bi:bi + 1],
+                      state0=None if state0 is None else state0[bi:bi + 1], l2_eps=l2_eps)
+            states[k - 1] = r["state"][0]
+            windows[k - 1] = r["window"][0]
+        out.append((states, windows))
+    return out
+
+
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
 

@@ -1,8 +1,9 @@
 """The oracle's pins must catch plausible slips.
 
 Each case copies the oracle to a temporary directory, plants one mistake in the
-copy's C source (never in the committed oracle), rebuilds it and runs the pin
-suite against the copy, which must fail.  This runs on the CPU only.
+copy's C source or Python wrapper (never in the committed oracle), rebuilds it
+and runs the pin suite against the copy, which must fail.  This runs on the CPU
+only.
 """
 import os
 import shutil
@@ -42,17 +43,24 @@ MUTATIONS = {
     "output_before_write": (
         "for (int64_t i = 0; i < d_k; ++i) acc += S[j * d_k + i] * q[i];",
         "for (int64_t i = 0; i < d_k; ++i) acc += (S[j * d_k + i] - bt * vt[j] * k[i]) * q[i];"),
+    # checkpoint taken one token late
+    "checkpoint_one_late": ("__init__.py", "t = k * every\n", "t = k * every + 1\n"),
+    # a checkpoint also at the end of a sequence whose length is a multiple of the interval
+    "checkpoint_count": ("__init__.py", "n_b = max(0, -(-ln // every) - 1)", "n_b = max(0, ln // every)"),
+    # snapshot copied the wrong way round
+    "slot_copy_reversed": ("__init__.py", "st[d_] = st[s_]", "st[s_] = st[d_]"),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name, tmp_path):
-    before, after = MUTATIONS[name]
-    src = open(os.path.join(ROOT, "oracle", "gdn_oracle.c")).read()
+    m = MUTATIONS[name]
+    fname, before, after = m if len(m) == 3 else ("gdn_oracle.c", *m)
+    src = open(os.path.join(ROOT, "oracle", fname)).read()
     assert before in src, "mutation site moved; update the mutation table"
     shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
                     ignore=shutil.ignore_patterns("*.so", "__pycache__"))
-    (tmp_path / "oracle" / "gdn_oracle.c").write_text(src.replace(before, after, 1))
+    (tmp_path / "oracle" / fname).write_text(src.replace(before, after, 1))
     shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
                     ignore=shutil.ignore_patterns("__pycache__", "golden"))
     shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path)

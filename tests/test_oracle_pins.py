@@ -350,3 +350,55 @@ def test_gated_norm_unit_rms_scale_invariance_and_weight_linearity():
     y1 = oracle.gated_rmsnorm(o, z, w)
     y2 = oracle.gated_rmsnorm(o, z, 2.0 * w)
     np.testing.assert_allclose(y2, 2.0 * y1, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- slots and checkpoints
+
+def test_slot_copy_moves_exactly_the_named_slots():
+    rng = RNG(41)
+    st = rng.standard_normal((6, 2, 3, 4))
+    cw = rng.standard_normal((6, 3, 5))
+    st2, cw2 = oracle.slot_copy(st, cw, [4, -1, 0], [1, 3, 5])
+    np.testing.assert_array_equal(st2[1], st[4])
+    np.testing.assert_array_equal(cw2[1], cw[4])
+    np.testing.assert_array_equal(st2[5], st[0])
+    for s_ in (0, 2, 3, 4):                      # sources and untouched slots (3: padding pair)
+        np.testing.assert_array_equal(st2[s_], st[s_])
+        np.testing.assert_array_equal(cw2[s_], cw[s_])
+    # snapshot then restore gives back the original slot after it was overwritten
+    snap_st, snap_cw = oracle.slot_copy(st, cw, [2], [5])
+    snap_st[2] += 1.0
+    back_st, back_cw = oracle.slot_copy(snap_st, snap_cw, [5], [2])
+    np.testing.assert_array_equal(back_st[2], st[2])
+    np.testing.assert_array_equal(back_cw[2], cw[2])
+
+
+@pytest.mark.parametrize("lengths,every", [((13,), 4), ((16, 5, 9), 4), ((7,), 8), ((24,), 8)])
+def test_checkpoints_count_and_resume(lengths, every):
+    """There are ceil(len / every) - 1 checkpoints per sequence, and resuming
+    from checkpoint k over the remaining tokens reproduces the full run's
+    outputs for them and its final state and window -- a checkpoint one token
+    off would apply that token twice or not at all."""
+    c = _layer_case(50 + every, lengths=lengths)
+    kw = dict(h_k=c["h_k"], h_v=c["h_v"], d_k=c["d_k"], d_v=c["d_v"])
+    p = (c["conv_weight"], c["A_log"], c["dt_bias"])
+    full = oracle.layer(c["x"], c["a"], c["b"], *p, c["cu_seqlens"], window0=c["window0"],
+                        state0=c["state0"], **kw)
+    ck = oracle.prefill_checkpoints(c["x"], c["a"], c["b"], *p, c["cu_seqlens"], every=every,
+                                    window0=c["window0"], state0=c["state0"], **kw)
+    cu = c["cu_seqlens"]
+    for bi, (states, windows) in enumerate(ck):
+        s0, ln = int(cu[bi]), int(cu[bi + 1] - cu[bi])
+        assert states.shape[0] == windows.shape[0] == -(-ln // every) - 1
+        for k in range(1, states.shape[0] + 1):
+            t = k * every
+            rest = oracle.layer(c["x"][s0 + t:s0 + ln], c["a"][s0 + t:s0 + ln],
+                                c["b"][s0 + t:s0 + ln], *p, [0, ln - t],
+                                window0=windows[k - 1:k].astype(np.float32),
+                                state0=states[k - 1:k].astype(np.float32), **kw)
+            # the resume rounds the state to float32 on the way; allow for that
+            np.testing.assert_allclose(rest["o"], full["o"][s0 + t:s0 + ln], rtol=0, atol=1e-6)
+            np.testing.assert_allclose(rest["state"][0], full["state"][bi], rtol=0, atol=1e-6)
+            np.testing.assert_array_equal(rest["window"][0], full["window"][bi])
+            # the window of checkpoint k is the raw inputs just before position t
+            np.testing.assert_array_equal(windows[k - 1], c["x"][s0 + t - 3:s0 + t])
