@@ -86,6 +86,11 @@ def load() -> ctypes.CDLL:
     lib.gdn_decode_step.restype = ctypes.c_int
     lib.gdn_gated_rmsnorm.argtypes = [D, P, ctypes.c_float, P, P, I64, P, P]
     lib.gdn_gated_rmsnorm.restype = ctypes.c_int
+    lib.gdn_prefill_checkpointed.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P,
+                                             SZ, I64, P, P, P]
+    lib.gdn_prefill_checkpointed.restype = ctypes.c_int
+    lib.gdn_slot_copy.argtypes = [D, P, P, I64, P, P, I32, P, P]
+    lib.gdn_slot_copy.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -184,6 +189,57 @@ def gdn_prefill(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx
     else:
         _check("gdn_prefill_traced",
                load().gdn_prefill_traced(*args, ctypes.byref(trace), _stream(stream)))
+
+
+def gdn_prefill_checkpointed(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx,
+                             has_initial_state, state_pool, conv_pool, o, workspace, ckpt_every,
+                             ckpt_slot, d_status=None, stream=None):
+    """gdn_prefill plus interval checkpoints: every ckpt_every tokens (a multiple
+    of the chunk) strictly inside sequence b, its state and conv window go to
+    slot ckpt_slot[b] + k - 1 (see gdn_prefill_checkpointed in include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    B = int(cu_seqlens.numel()) - 1
+    T = int(x.shape[0]) if x is not None else 0
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, T * cd)
+    _expect(a, "a", io, T * d.h_v)
+    _expect(b, "b", io, T * d.h_v)
+    _expect(o, "o", io, T * d.h_v * d.d_v)
+    _expect(cu_seqlens, "cu_seqlens", torch.int32)
+    _expect(slot_idx, "slot_idx", torch.int32, B)
+    _expect(has_initial_state, "has_initial_state", torch.uint8, B)
+    _expect(ckpt_slot, "ckpt_slot", torch.int32, B)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("gdn_prefill_checkpointed", load().gdn_prefill_checkpointed(
+        ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b), _ptr(cu_seqlens), B, T,
+        _ptr(slot_idx), _ptr(has_initial_state), _ptr(state_pool), _ptr(conv_pool), num_slots,
+        _ptr(o), _ptr(workspace), ws_bytes, int(ckpt_every), _ptr(ckpt_slot), _ptr(d_status),
+        _stream(stream)))
+
+
+def gdn_slot_copy(dims, state_pool, conv_pool, src_slot, dst_slot, d_status=None, stream=None):
+    """Copy whole slots (state and conv window): slot dst_slot[i] <- slot
+    src_slot[i]; padding pairs (< 0) skipped (see gdn_slot_copy in include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", _io_dtype(d))
+    n = int(src_slot.numel())
+    _expect(src_slot, "src_slot", torch.int32, n)
+    _expect(dst_slot, "dst_slot", torch.int32, n)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    _check("gdn_slot_copy", load().gdn_slot_copy(
+        ctypes.byref(d), _ptr(state_pool), _ptr(conv_pool), num_slots, _ptr(src_slot),
+        _ptr(dst_slot), n, _ptr(d_status), _stream(stream)))
 
 
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20

@@ -143,14 +143,15 @@ GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total
   return prefill_layout(dims, total_tokens, num_seqs).total;
 }
 
-GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
-                                  const void* x, const void* a, const void* b,
-                                  const int32_t* cu_seqlens, int32_t num_seqs,
-                                  int64_t total_tokens, const int32_t* slot_idx,
-                                  const uint8_t* has_initial_state, float* state_pool,
-                                  void* conv_pool, int64_t num_slots, void* o, void* workspace,
-                                  size_t workspace_bytes, int32_t* d_status, gdn_trace* trace,
-                                  gdn_stream_t stream) {
+// The prefill behind every public variant; ckpt_every_chunks = 0 and
+// ckpt_slot = null: no interval checkpoints.
+static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const void* x,
+                        const void* a, const void* b, const int32_t* cu_seqlens, int32_t num_seqs,
+                        int64_t total_tokens, const int32_t* slot_idx,
+                        const uint8_t* has_initial_state, float* state_pool, void* conv_pool,
+                        int64_t num_slots, void* o, void* workspace, size_t workspace_bytes,
+                        int32_t ckpt_every_chunks, const int32_t* ckpt_slot, int32_t* d_status,
+                        gdn_trace* trace, gdn_stream_t stream) {
   if (trace) {
     trace->launches = 0;
     trace->stages_run = 0;
@@ -182,6 +183,7 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   p.cu_seqlens = cu_seqlens; p.slot_idx = slot_idx; p.has_init = has_initial_state;
   p.conv_weight = params->conv_weight; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
   p.state_pool = state_pool; p.conv_pool = conv_pool; p.o = o; p.d_status = d_status;
+  p.ckpt_every_chunks = ckpt_every_chunks; p.ckpt_slot = ckpt_slot;
   char* ws = reinterpret_cast<char*>(workspace);
   p.ws_flag = reinterpret_cast<int32_t*>(ws + L.flag);
   p.ws_q = reinterpret_cast<float*>(ws + L.q);
@@ -199,6 +201,56 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
   }
   return cuda_rc(
       gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace));
+}
+
+GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
+                                  const void* x, const void* a, const void* b,
+                                  const int32_t* cu_seqlens, int32_t num_seqs,
+                                  int64_t total_tokens, const int32_t* slot_idx,
+                                  const uint8_t* has_initial_state, float* state_pool,
+                                  void* conv_pool, int64_t num_slots, void* o, void* workspace,
+                                  size_t workspace_bytes, int32_t* d_status, gdn_trace* trace,
+                                  gdn_stream_t stream) {
+  return prefill_impl(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
+                      has_initial_state, state_pool, conv_pool, num_slots, o, workspace,
+                      workspace_bytes, 0, nullptr, d_status, trace, stream);
+}
+
+GDN_EXPORT int gdn_prefill_checkpointed(const gdn_dims* dims, const gdn_params* params,
+                                        const void* x, const void* a, const void* b,
+                                        const int32_t* cu_seqlens, int32_t num_seqs,
+                                        int64_t total_tokens, const int32_t* slot_idx,
+                                        const uint8_t* has_initial_state, float* state_pool,
+                                        void* conv_pool, int64_t num_slots, void* o,
+                                        void* workspace, size_t workspace_bytes,
+                                        int64_t ckpt_every, const int32_t* ckpt_slot,
+                                        int32_t* d_status, gdn_stream_t stream) {
+  const int rc = check_prefill_dims(dims);   // validates chunk before the division below
+  if (rc != GDN_OK) return rc;
+  if (ckpt_every <= 0 || ckpt_every % dims->chunk != 0 || !ckpt_slot) return GDN_EINVAL;
+  if (ckpt_every / dims->chunk > INT32_MAX) return GDN_EUNSUPPORTED;
+  return prefill_impl(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
+                      has_initial_state, state_pool, conv_pool, num_slots, o, workspace,
+                      workspace_bytes, (int32_t)(ckpt_every / dims->chunk), ckpt_slot, d_status,
+                      nullptr, stream);
+}
+
+GDN_EXPORT int gdn_slot_copy(const gdn_dims* dims, float* state_pool, void* conv_pool,
+                             int64_t num_slots, const int32_t* src_slot, const int32_t* dst_slot,
+                             int32_t n, int32_t* d_status, gdn_stream_t stream) {
+  const int rc = check_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (n < 0 || num_slots < 0) return GDN_EINVAL;
+  if (n == 0) return GDN_OK;
+  if (!state_pool || !conv_pool || !src_slot || !dst_slot) return GDN_EINVAL;
+  if (!aligned16(state_pool) || !aligned16(conv_pool)) return GDN_EALIGN;
+  const int64_t state_bytes = (int64_t)dims->h_v * dims->d_k * dims->d_v * 4;
+  const int64_t window_bytes =
+      (int64_t)(dims->conv_w - 1) * conv_dim_of(dims) * (dims->io == GDN_BF16 ? 2 : 4);
+  if (state_bytes % 16 != 0 || window_bytes % 16 != 0) return GDN_EUNSUPPORTED;
+  return cuda_rc(gdn_launch_slot_copy(state_pool, conv_pool, num_slots, state_bytes, window_bytes,
+                                      src_slot, dst_slot, n, d_status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 GDN_EXPORT int gdn_prefill(const gdn_dims* dims, const gdn_params* params, const void* x,

@@ -127,12 +127,36 @@ struct GdnPrefillArgs {
   uint8_t* kq_ws;       // [max_chunks][h_k] [K;Q] tile images
   uint8_t* vh_ws;       // [max_chunks][h_v] P | U^T | decay factors | Wk records
   int32_t* chunk_ready; // [max_chunks][h_k] set to 1 when the prep published the chunk
+  // interval checkpoints (0 / null: none): every ckpt_every_chunks chunks strictly
+  // inside sequence b, the state and window go to slot ckpt_slot[b] + k - 1
+  int32_t ckpt_every_chunks;
+  const int32_t* ckpt_slot;   // [num_seqs], < 0: no checkpoints for that sequence
 };
+
+// Slot of checkpoint k >= 1 (after k * every chunks) of sequence b, or -1 when
+// there is none there; out-of-range slots set the status bit and give -1.
+__device__ __forceinline__ int64_t ckpt_slot_of(const GdnPrefillArgs& a, int b, int64_t chunks_done,
+                                                int64_t seq_len) {
+  if (a.ckpt_every_chunks <= 0 || chunks_done % a.ckpt_every_chunks != 0) return -1;
+  if (chunks_done * a.chunk >= seq_len) return -1;
+  const int32_t base = a.ckpt_slot[b];
+  if (base < 0) return -1;
+  const int64_t cs = (int64_t)base + chunks_done / a.ckpt_every_chunks - 1;
+  if (cs >= a.num_slots) {
+    gdn::set_status(a.d_status, GDN_DEV_BAD_SLOT);
+    return -1;
+  }
+  return cs;
+}
 
 // Launchers (defined in the kernel translation units); return cudaError_t.
 cudaError_t gdn_launch_decode(const GdnDecodeArgs& a, int d_k, int d_v, int io,
                               cudaStream_t s);
 cudaError_t gdn_launch_conv_update(const GdnConvArgs& a, int io, cudaStream_t s);
+cudaError_t gdn_launch_slot_copy(float* state_pool, void* conv_pool, int64_t num_slots,
+                                 int64_t state_bytes, int64_t window_bytes, const int32_t* src,
+                                 const int32_t* dst, int32_t n, int32_t* d_status,
+                                 cudaStream_t s);
 cudaError_t gdn_launch_gated_rmsnorm(const float* weight, float eps, const void* o, const void* z,
                                      int64_t rows, int d_v, int io, void* y, cudaStream_t s);
 cudaError_t gdn_launch_prefill_simt(const GdnPrefillArgs& a, int io, cudaStream_t s,

@@ -135,6 +135,18 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
   }
 #pragma unroll
   for (int r = 0; r < 3; ++r) win[(size_t)r * cd + c] = vals[r];
+  // windows of the interval checkpoints: the three raw inputs before position
+  // k * every (every >= 16 chunks' worth of tokens > 3, so all inside the sequence)
+  if (args.ckpt_every_chunks > 0) {
+    const int64_t every = (int64_t)args.ckpt_every_chunks * args.chunk;
+    for (int64_t k = 1; k * every < T; ++k) {
+      const int64_t cs = ckpt_slot_of(args, b, k * args.ckpt_every_chunks, T);
+      if (cs < 0) continue;
+      IO* cw = reinterpret_cast<IO*>(args.conv_pool) + (size_t)cs * 3 * cd;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) cw[(size_t)r * cd + c] = x[(size_t)(start + k * every - 3 + r) * cd + c];
+    }
+  }
 }
 
 struct ScanSmem {
@@ -290,12 +302,17 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     // S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
     const float glast = sG[C - 1];
     const float dlast = expf(glast);
+    // interval checkpoint: the state after these c0 / C + 1 chunks, each thread
+    // storing the elements it just updated
+    const int64_t cs = args.ckpt_every_chunks > 0 ? ckpt_slot_of(args, b, c0 / C + 1, Tlen) : -1;
+    float* cst = cs >= 0 ? args.state_pool + ((size_t)cs * args.h_v + h) * (size_t)DK * DV : nullptr;
     for (int e = tid; e < DK * DVT; e += NT) {
       const int i = e / DVT, j = e % DVT;
       float acc = 0.f;
       for (int r = 0; r < Lc; ++r)
         acc = fmaf(sK[r * DK + i] * expf(glast - sG[r]), sU[r * DVT + j], acc);
       sH[e] = fmaf(dlast, sH[e], acc);
+      if (cst) cst[(size_t)i * DV + j0 + j] = sH[e];
     }
   }
   __syncthreads();

@@ -1140,6 +1140,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(hready);
+      // interval checkpoint: the state after c + 1 chunks (off the chain: the next
+      // chunk's X MMA is already under way)
+      if (a.ckpt_every_chunks > 0) {
+        const int64_t cs = ckpt_slot_of(a, b, c + 1, Tb);
+        if (cs >= 0) {
+          float* cst = a.state_pool + ((size_t)cs * a.h_v + h) * (size_t)(D * D);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cst[(size_t)(32 * grp + i) * D + j] = H[i];
+        }
+      }
     }
     if (!*s_abort) {
 #pragma unroll

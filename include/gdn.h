@@ -251,6 +251,61 @@ int gdn_prefill_noalloc(const gdn_dims* dims, const gdn_params* params,
                         void* conv_pool, int64_t num_slots, void* o,
                         int32_t* d_status, gdn_stream_t stream);
 
+/*
+ * gdn_prefill_checkpointed -- gdn_prefill that also leaves interval
+ * checkpoints of each sequence's recurrent state in other slots of the same
+ * pools (PicoLM changelog, "SSM State Checkpointing": checkpoints every N
+ * tokens during prefill; on a partial prefix match the closest checkpoint is
+ * restored and only the remaining tokens are processed).  Same arguments as
+ * gdn_prefill plus:
+ *   ckpt_every  interval in tokens: a positive multiple of dims->chunk, else
+ *               GDN_EINVAL with nothing enqueued
+ *   ckpt_slot   device int32 [num_seqs]: first checkpoint slot of each
+ *               sequence; < 0 = no checkpoints for it.  NULL: GDN_EINVAL.
+ * For sequence b and every k >= 1 with k * ckpt_every < len_b, slot
+ * ckpt_slot[b] + k - 1 receives the state (fp32 [h_v][d_k][d_v], S^T) and the
+ * conv window (the last conv_w - 1 raw inputs) after the first k * ckpt_every
+ * tokens of the sequence, its initial state and window included -- exactly
+ * what a gdn_prefill of that prefix would leave in its slot, so a prefill of
+ * the remaining tokens from that slot (has_initial_state = 1) continues the
+ * sequence.  The final state goes to slot_idx[b] as in gdn_prefill.  A
+ * checkpoint slot >= num_slots sets GDN_DEV_BAD_SLOT in *d_status and that
+ * checkpoint is skipped.  Checkpoint slots must differ from every slot the
+ * call reads or writes otherwise (the caller's contract; overlaps are
+ * undefined).  Costs one extra state write per checkpoint.
+ */
+int gdn_prefill_checkpointed(const gdn_dims* dims, const gdn_params* params,
+                             const void* x, const void* a, const void* b,
+                             const int32_t* cu_seqlens, int32_t num_seqs,
+                             int64_t total_tokens, const int32_t* slot_idx,
+                             const uint8_t* has_initial_state, float* state_pool,
+                             void* conv_pool, int64_t num_slots, void* o,
+                             void* workspace, size_t workspace_bytes,
+                             int64_t ckpt_every, const int32_t* ckpt_slot,
+                             int32_t* d_status, gdn_stream_t stream);
+
+/*
+ * gdn_slot_copy -- copy whole recurrent slots: for each i < n, slot
+ * dst_slot[i] receives the state and conv window of slot src_slot[i].
+ * Snapshot (a live slot to a spare one), restore (back) and fork (one prefix
+ * into several sequences) are this copy (Vallmo.jl README, src/: recurrent
+ * state snapshotted and restored for prefix caching; PicoLM changelog, "SSM
+ * State Checkpointing": capture and restore the full SSM state).
+ *   state_pool  device fp32 [num_slots][h_v][d_k][d_v], 16-byte aligned
+ *   conv_pool   device I/O dtype [num_slots][conv_w-1][conv_dim], 16-byte aligned
+ *   src_slot, dst_slot  device int32 [n]; a pair with either < 0 is padding and
+ *               skipped; src == dst is a no-op; either >= num_slots sets
+ *               GDN_DEV_BAD_SLOT in *d_status and that pair is skipped
+ * Host-checkable problems (bad dims, NULL pointers with n > 0, misalignment,
+ * n < 0) return an error with nothing enqueued.  The pairs are copied
+ * concurrently: a slot that is one pair's destination must not be another
+ * pair's source or destination (undefined otherwise).  HBM-bound: each pair
+ * reads and writes the state and window bytes once.
+ */
+int gdn_slot_copy(const gdn_dims* dims, float* state_pool, void* conv_pool,
+                  int64_t num_slots, const int32_t* src_slot, const int32_t* dst_slot,
+                  int32_t n, int32_t* d_status, gdn_stream_t stream);
+
 /* Static description of a gdn_status code. */
 const char* gdn_status_str(int status);
 

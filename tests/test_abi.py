@@ -140,3 +140,31 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _binding.load()
+
+
+def test_slot_copy_and_checkpointed_prefill_reject_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    copy = lambda **kw: lib.gdn_slot_copy(  # noqa: E731
+        ctypes.byref(kw.get("dims", d)), kw.get("state", FAKE), kw.get("conv", FAKE), 8,
+        kw.get("src", FAKE), kw.get("dst", FAKE), kw.get("n", 4), None, None)
+    assert copy(dims=gdn.make_dims(**dict(D4B, d_v=48))) == -2
+    assert copy(src=None) == -1
+    assert copy(dst=None) == -1
+    assert copy(state=None) == -1
+    assert copy(n=-1) == -1
+    assert copy(n=0) == 0                          # nothing to copy
+    assert copy(state=FAKE + 4) == -5
+    assert copy(conv=FAKE + 8) == -5
+    p = _binding.gdn_params(FAKE, FAKE, FAKE)
+
+    def ck(dims=d, every=128, ckpt=FAKE, cu=FAKE, x=FAKE):
+        return lib.gdn_prefill_checkpointed(
+            ctypes.byref(dims), ctypes.byref(p), x, FAKE, FAKE, cu, 1, 64, FAKE, None, FAKE,
+            FAKE, 1, FAKE, FAKE, 1 << 40, every, ckpt, None, None)
+    assert ck(dims=gdn.make_dims(**dict(D4B, d_k=48))) == -2
+    assert ck(every=0) == -1
+    assert ck(every=-64) == -1
+    assert ck(every=96) == -1                      # not a multiple of the chunk (64)
+    assert ck(ckpt=None) == -1
+    assert ck(cu=None) == -1                       # and every gdn_prefill check still applies
+    assert ck(x=FAKE + 2) == -5
