@@ -174,6 +174,7 @@ KERNEL_SOURCES = {
     "prefill_chunk": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "prefill_overlap": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "gated_norm": ("gdn_norm.cu", "gdn_common.cuh"),
+    "slot_copy": ("gdn_slots.cu", "gdn_common.cuh"),
 }
 
 
@@ -343,6 +344,65 @@ def bench_gated_norm(torch, gdn, dims, T, device, steps, warmup):
     return {"ms": ms, "bytes": nbytes, "rows": T * dims.h_v}
 
 
+def bench_slot_copy(torch, gdn, dims, device, steps, warmup, pairs=64):
+    """Copy `pairs` whole slots (state and conv window) to `pairs` others in one
+    call; the pool (2 x pairs slots, ~270 MB at the Qwen3.5-4B shape) is larger
+    than L2."""
+    io = torch.bfloat16 if dims.io == "bf16" else torch.float32
+    n = 2 * pairs
+    st = torch.randn((n, dims.h_v, dims.d_k, dims.d_v), device=device)
+    cv = torch.randn((n, dims.conv_w - 1, gdn.conv_dim(dims)), device=device).to(io)
+    src = torch.arange(pairs, dtype=torch.int32, device=device)
+    dst = src + pairs
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    for _ in range(max(warmup, 1)):
+        gdn.gdn_slot_copy(dims, st, cv, src, dst, d_status=status)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for a_, b_ in ev:
+        a_.record()
+        gdn.gdn_slot_copy(dims, st, cv, src, dst, d_status=status)
+        b_.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in ev)
+    per_slot = st[0].numel() * 4 + cv[0].numel() * cv.element_size()
+    return {"ms": ms, "bytes": 2 * pairs * per_slot, "pairs": pairs, "status": int(status.item())}
+
+
+def bench_checkpointed(torch, gdn, run, steps, warmup, every=256):
+    """The timed prefill again through gdn_prefill_checkpointed, leaving a
+    checkpoint every `every` tokens (the interval PicoLM's server uses by
+    default) in extra pool slots; L2 flushed before every timed step."""
+    inp, d = run.inp, run.dims
+    T = run.T
+    n_ck = max(0, -(-T // every) - 1)
+    base = run.state.shape[0]
+    st = torch.cat([run.state, torch.zeros((n_ck,) + tuple(run.state.shape[1:]),
+                                           device=run.state.device)])
+    cv = torch.cat([run.conv, torch.zeros((n_ck,) + tuple(run.conv.shape[1:]), dtype=run.conv.dtype,
+                                          device=run.conv.device)])
+    ck = torch.tensor([base], dtype=torch.int32, device=run.state.device)
+    flush = L2Flush(torch, run.state.device)
+
+    def call():
+        gdn.gdn_prefill_checkpointed(d, run.cw, run.A_log, run.dt_bias, run.x, run.a, run.b, run.cu,
+                                     run.slot, run.init, st, cv, run.o, run.ws, every, ck,
+                                     d_status=run.status)
+
+    for _ in range(max(warmup, 1)):
+        call()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for a_, b_ in ev:
+        flush()
+        a_.record()
+        call()
+        b_.record()
+    torch.cuda.synchronize()
+    return {"ms": statistics.median(a_.elapsed_time(b_) for a_, b_ in ev), "every": every,
+            "checkpoints": n_ck, "T": T, "status": int(run.status.item())}
+
+
 def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64):
     runs = []
     for layer in range(layers):
@@ -500,10 +560,14 @@ def run_gdn(args):
     if not args.no_prefill:
         pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
         barrier()
-    gn = None
+    gn = sc = ck = None
     if pf is not None:
         gn = bench_gated_norm(torch, gdn, pf["inp"]["dims"], pf["inp"]["x"].shape[0], device,
                               args.steps, args.warmup)
+        barrier()
+        sc = bench_slot_copy(torch, gdn, pf["inp"]["dims"], device, args.steps, args.warmup)
+        barrier()
+        ck = bench_checkpointed(torch, gdn, pf["run"], args.steps, args.warmup)
         barrier()
     dec = None
     if not args.no_decode:
@@ -592,6 +656,29 @@ def run_gdn(args):
                              "frac": ggbs / hbm, "traffic": recorded_traffic("gated_norm"),
                              "kernel": "gated_rmsnorm_kernel", "peak_source": f"hbm_gbs ({peak_src})",
                              "launch_ms": gn["ms"]}}
+        if sc:
+            sgbs = sc["bytes"] / (sc["ms"] / 1e3) / 1e9
+            line["slot_copy"] = {
+                "metric": "slot copy (snapshot / restore) GB/s", "value": sgbs, "unit": "GB/s",
+                "ms_per_call": sc["ms"],
+                "config": {"workload": f"{sc['pairs']} slot pairs of the {T}-token layer's shape "
+                                       f"(fp32 [{d.h_v}, {d.d_k}, {d.d_v}] state + conv window)",
+                           "bytes_per_call": sc["bytes"],
+                           "l2": "inputs larger than L2 (the pool is twice the copied bytes)"},
+                "roofline": {"bound": "hbm", "achieved": sgbs, "peak": hbm, "unit": "GB/s",
+                             "frac": sgbs / hbm, "traffic": recorded_traffic("slot_copy"),
+                             "kernel": "slot_copy_kernel", "peak_source": f"hbm_gbs ({peak_src})",
+                             "launch_ms": sc["ms"]},
+                "device_status": sc["status"]}
+        if ck:
+            line["checkpointed_prefill"] = {
+                "metric": "prefill tokens/s with interval checkpoints", "unit": "tokens/s",
+                "value": ck["T"] / (ck["ms"] / 1e3), "ms_per_step": ck["ms"],
+                "overhead_vs_plain": ck["ms"] / ms - 1.0,
+                "config": {"workload": f"the timed prefill, a checkpoint every {ck['every']} tokens",
+                           "checkpoints_per_step": ck["checkpoints"],
+                           "l2": "flushed before every timed step"},
+                "device_status": ck["status"]}
         if dec:
             # whole job: every rank moves its own replica's state bytes
             gbs = replica_throughput(world, dec["state_bytes"], dms) / 1e9

@@ -26,6 +26,8 @@
 //       O = diag(e^gamma) Q S^T + tril(Q K^T * e^{gamma_r - gamma_s}) W
 //       S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
 //     Only e^{x} with x <= 0 is ever formed.
+#include <type_traits>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -123,7 +125,24 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
   const int64_t T = args.cu_seqlens[b + 1] - start;
   const bool init = args.has_init ? args.has_init[b] != 0 : false;
   const int cd = args.conv_dim;
-  const IO* x = reinterpret_cast<const IO*>(args.x);
+  const IO* __restrict__ x = reinterpret_cast<const IO*>(args.x);
+  if (blockIdx.z > 0) {
+    // windows of the interval checkpoints k = z, z + (gridDim.z - 1), ...: the
+    // three raw inputs before position k * every (every >= 16 tokens > 3, so all
+    // inside the sequence)
+    const int64_t every = (int64_t)args.ckpt_every_chunks * args.chunk;
+    for (int64_t k = blockIdx.z; k * every < T; k += gridDim.z - 1) {
+      const int64_t cs = ckpt_slot_of(args, b, k * args.ckpt_every_chunks, T);
+      if (cs < 0) continue;
+      IO* cw = reinterpret_cast<IO*>(args.conv_pool) + (size_t)cs * 3 * cd;
+      IO v[3];
+#pragma unroll
+      for (int r = 0; r < 3; ++r) v[r] = x[(size_t)(start + k * every - 3 + r) * cd + c];
+#pragma unroll
+      for (int r = 0; r < 3; ++r) cw[(size_t)r * cd + c] = v[r];
+    }
+    return;
+  }
   IO* win = reinterpret_cast<IO*>(args.conv_pool) + (size_t)slot * 3 * cd;
   IO vals[3];
 #pragma unroll
@@ -135,18 +154,6 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
   }
 #pragma unroll
   for (int r = 0; r < 3; ++r) win[(size_t)r * cd + c] = vals[r];
-  // windows of the interval checkpoints: the three raw inputs before position
-  // k * every (every >= 16 chunks' worth of tokens > 3, so all inside the sequence)
-  if (args.ckpt_every_chunks > 0) {
-    const int64_t every = (int64_t)args.ckpt_every_chunks * args.chunk;
-    for (int64_t k = 1; k * every < T; ++k) {
-      const int64_t cs = ckpt_slot_of(args, b, k * args.ckpt_every_chunks, T);
-      if (cs < 0) continue;
-      IO* cw = reinterpret_cast<IO*>(args.conv_pool) + (size_t)cs * 3 * cd;
-#pragma unroll
-      for (int r = 0; r < 3; ++r) cw[(size_t)r * cd + c] = x[(size_t)(start + k * every - 3 + r) * cd + c];
-    }
-  }
 }
 
 struct ScanSmem {
@@ -345,10 +352,7 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 wgrid(a.num_seqs, (a.conv_dim + 255) / 256);
-  window_writeback_kernel<IO><<<wgrid, 256, 0, s>>>(a);
-  gdn_trace_count(tr, 1);
-  e = cudaGetLastError();
+  e = gdn_launch_window(a, std::is_same<IO, float>::value ? GDN_FP32 : GDN_BF16, s, tr);
   if (e != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 0, false, s)) != cudaSuccess) return e;
   const int DVT = scan_dv_tile(a.d_v);
@@ -376,7 +380,16 @@ cudaError_t gdn_launch_check(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace*
 }
 
 cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, gdn_trace* tr) {
-  dim3 wgrid(a.num_seqs, (a.conv_dim + 255) / 256);
+  // z = 0: each sequence's own window; z >= 1: its interval checkpoints (each
+  // z-block loops over every (gridDim.z - 1)-th one), as many z-blocks as a
+  // sequence of average length has checkpoints, 1 to 64
+  int64_t nz = 1;
+  if (a.ckpt_every_chunks > 0) {
+    const int64_t every = (int64_t)a.ckpt_every_chunks * a.chunk;
+    const int64_t avg = (a.total_tokens / (a.num_seqs > 0 ? a.num_seqs : 1) + every - 1) / every;
+    nz = 1 + (avg < 1 ? 1 : (avg > 64 ? 64 : avg));
+  }
+  dim3 wgrid(a.num_seqs, (a.conv_dim + 255) / 256, (unsigned)nz);
   if (io == GDN_BF16)
     gdn::window_writeback_kernel<__nv_bfloat16><<<wgrid, 256, 0, s>>>(a);
   else

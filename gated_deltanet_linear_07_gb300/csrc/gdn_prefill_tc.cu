@@ -871,6 +871,10 @@ struct ScanSmem {
   static constexpr uint32_t OST = BAR + 256;  // output staging, 2 KiB per output warp
   static constexpr uint32_t EG = OST + 8192;  // e^{gamma} [64] x 2 buffers
   static constexpr uint32_t SIZE = EG + 512;
+  // only when checkpointing: a checkpoint's fp32 state [d_k][d_v] (64 KB); the
+  // plain call does not reserve it (more of the SM's memory stays L1)
+  static constexpr uint32_t CK = SIZE;
+  static constexpr uint32_t SIZE_CK = CK + 65536;
 };
 // TMEM columns (fp32 accumulators, then the bf16 A operands, two per column):
 //   X [64] | O1 x 2 [64] | dH [128] | O2 [64] | H^T [64] | Wt^T [32] | W^T [32]
@@ -897,6 +901,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   const int32_t gc0 = a.chunk_off[b];
   const bool init = a.has_init ? a.has_init[b] != 0 : false;
   const uint32_t s_base = smem_u32(sm);
+  // Interval checkpoints: the state after chunks ck_every - 1, 2 ck_every - 1,
+  // ... (those before the last chunk) goes to slots ck_base, ck_base + 1, ...
+  // The chain warps stage it in shared memory before their hready arrival; the
+  // MMA issuer, which waits for that arrival anyway, sends it with one bulk
+  // copy, walking the checkpoints with a counter (the next checkpoint's chunk):
+  // that thread is on the chain and each of its instructions is slow.
+  const int32_t ck_every = a.ckpt_every_chunks;
+  const int32_t ck_base = ck_every > 0 ? a.ckpt_slot[b] : -1;
+  const bool ckpt_on = ck_base >= 0;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + ScanSmem::BAR);      // [2] P|UT|EXP|K
   uint64_t* empty = full + 2;                                             // [2]
@@ -991,6 +1004,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       constexpr uint32_t ID_XO = idesc_bf16(128, 64, false, false);
       constexpr uint32_t ID_DH = idesc_bf16(128, 128, false, true);
       constexpr uint32_t ID_O2 = idesc_bf16(128, 64, false, false);
+      bool ck_reading = false;   // a checkpoint copy may still be reading the staging area
+      int ck_next = ck_every - 1;           // chunk after which the next checkpoint falls
+      int64_t ck_slot = ck_base;            // and its slot
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1;
         const uint32_t buf = s_base + s * ScanSmem::BUF;
@@ -1004,6 +1020,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         // O1's buffer has been read; wready that P | U | EXP | K has landed.
         if (!mbar_spin(hready, c & 1, SPIN_LIMIT)) { fail(); break; }
         tc_fence_after();
+        if (ckpt_on && c - 1 == ck_next) {   // the checkpoint after chunk c - 1 (c < nch)
+          if (ck_slot >= a.num_slots) {
+            set_status(a.d_status, GDN_DEV_BAD_SLOT);
+          } else {
+            bulk_s2g(a.state_pool + ((size_t)ck_slot * a.h_v + h) * (size_t)(D * D),
+                     s_base + ScanSmem::CK, 65536);
+            ck_reading = true;
+          }
+          ck_next += ck_every;
+          ++ck_slot;
+        }
         // A operands advance 16 K elements = 8 columns per step; B operands are
         // 128B-swizzled K-major tiles of 64-element K blocks.
 #pragma unroll
@@ -1021,6 +1048,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
           mma_bf16_ts(tmem + TDH, tmem + TWT + 8 * ks, sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
+        // the chain warps stage the next checkpoint (after this chunk, if there is
+        // one) only after bar_dh: the copy has read the staging area by then
+        if (ck_reading && c == ck_next && c + 1 < nch) {
+          bulk_wait_read();
+          ck_reading = false;
+        }
         mma_commit(bar_dh);
         // O2 rewrites what the output warps read for the previous chunk
         if (c >= 1 && !mbar_wait(&ofree[s ^ 1], ((c - 1) >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
@@ -1031,6 +1064,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         mma_commit(&bar_o[s]);
         mma_commit(&empty[s]);
       }
+      if (ckpt_on) bulk_wait_all();   // checkpoint copies complete before the CTA exits
     }
   } else if (warp < 2 + (int)(EPI_THREADS / 32)) {
     // ---------------- state chain ----------------
@@ -1136,20 +1170,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         for (int e = 0; e < 16; ++e) hp[e] = pack_bf16(H[2 * e], H[2 * e + 1]);
         tmem_st16(t_ht, hp);
       }
+      if (ckpt_on && (c + 1) % ck_every == 0 && c + 1 < nch) {   // stage it, [i][j] as in the pool
+        float* ck = reinterpret_cast<float*>(sm + ScanSmem::CK);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ck[(32 * grp + i) * D + j] = H[i];
+        fence_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(hready);
-      // interval checkpoint: the state after c + 1 chunks (off the chain: the next
-      // chunk's X MMA is already under way)
-      if (a.ckpt_every_chunks > 0) {
-        const int64_t cs = ckpt_slot_of(a, b, c + 1, Tb);
-        if (cs >= 0) {
-          float* cst = a.state_pool + ((size_t)cs * a.h_v + h) * (size_t)(D * D);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) cst[(size_t)(32 * grp + i) * D + j] = H[i];
-        }
-      }
     }
     if (!*s_abort) {
 #pragma unroll
@@ -1239,7 +1269,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   const bool overlap = n_scan <= n_sm / 2;
   const int workers = overlap ? n_sm - (int)n_scan : n_sm;
   const int psmem = (int)PREP_SMEM + 1024;
-  const int ssmem = (int)ScanSmem::SIZE + 1024;
+  const int ssmem = (int)(a.ckpt_every_chunks > 0 ? ScanSmem::SIZE_CK : ScanSmem::SIZE) + 1024;
   if ((e = cudaFuncSetAttribute(prep_persistent_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess)
     return e;
