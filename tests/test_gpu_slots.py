@@ -154,3 +154,37 @@ def test_checkpoint_slot_out_of_range_sets_status(gpu_lib):
     # checkpoints 1..3 would go to slots 2, 3, 4: slots 3 and 4 do not exist
     assert got["status"] & gdn.GDN_DEV_BAD_SLOT
     assert np.isfinite(got["o"]).all()
+
+
+def test_checkpointed_prefill_full_size_sampled(gpu_lib):
+    """The T=4096 Qwen3.5-4B prefill with a checkpoint every 256 tokens (15 of
+    them, the bench's configuration): checkpoints 1, 8 and 15 against the
+    oracle on the prefix, on 6 sampled value heads; their windows exact."""
+    inp = workloads.prefill_4b()
+    d = inp["dims"]
+    every, n_ck = 256, 15
+    base = inp["num_slots"]
+    inp["state_pool"] = np.concatenate(
+        [inp["state_pool"], np.zeros((n_ck,) + inp["state_pool"].shape[1:], np.float32)])
+    inp["conv_pool"] = np.concatenate(
+        [inp["conv_pool"], np.zeros((n_ck,) + inp["conv_pool"].shape[1:], np.float32)])
+    inp["num_slots"] = base + n_ck
+    run = PrefillRun(inp)
+    gdn.gdn_prefill_checkpointed(d, run.cw, run.A_log, run.dt_bias, run.x, run.a, run.b, run.cu,
+                                 run.slot, run.init, run.state, run.conv, run.o, run.ws, every,
+                                 dev(np.array([base], np.int32)), d_status=run.status)
+    got = run.results()
+    assert got["status"] == 0
+    heads = np.random.default_rng(7).choice(d.h_v, 6, replace=False)
+    mask = np.zeros((1, d.h_v), bool)
+    mask[0, heads] = True
+    for k in (1, 8, 15):
+        t = k * every
+        ref = oracle.layer(inp["x"][:t], inp["a"][:t], inp["b"][:t], inp["conv_weight"],
+                           inp["A_log"], inp["dt_bias"], [0, t], d.h_k, d.h_v, d.d_k, d.d_v,
+                           head_mask=mask, l2_eps=d.l2_eps)
+        sl = base + k - 1
+        for h in heads:
+            assert_close(got["state_pool"][sl, h], ref["state"][0, h], d,
+                         f"checkpoint {k} head {h}")
+        np.testing.assert_array_equal(got["conv_pool"][sl], inp["x"][t - 3:t].astype(np.float32))
