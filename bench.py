@@ -445,8 +445,49 @@ def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=
     layer_ms = [s.elapsed_time(e) for s, e in one]
     d = runs[0]["dims"]
     state_bytes = 2 * layers * slots * d.h_v * d.d_k * d.d_v * 4
+    norm = bench_decode_gated_norm(torch, gdn, runs, status, steps, warmup)
     return {"step_ms": step_ms, "layer_ms": layer_ms, "state_bytes": state_bytes,
-            "layers": layers, "slots": slots, "status": int(status.item())}
+            "layers": layers, "slots": slots, "status": int(status.item()), "gated_norm": norm}
+
+
+def bench_decode_gated_norm(torch, gdn, runs, status, steps, warmup):
+    """The same decode step with the gated RMSNorm of every layer's output:
+    fused into the step (gdn_decode_step_gated_norm) and as the plain step plus
+    the standalone norm per layer; median ms per 24-layer step of each."""
+    d = runs[0]["dims"]
+    dev = runs[0]["o"].device
+    g = torch.Generator(device=dev).manual_seed(99)
+    for r in runs:
+        r["z"] = torch.randn(tuple(r["o"].shape), generator=g, device=dev).to(r["o"].dtype)
+        r["w"] = torch.rand(d.d_v, generator=g, device=dev) + 0.5
+        r["y"] = torch.empty_like(r["o"])
+
+    def fused():
+        for r in runs:
+            gdn.gdn_decode_step_gated_norm(r["dims"], r["cw"], r["A"], r["dt"], r["x"], r["a"],
+                                           r["b"], r["slot"], r["state"], r["conv"], r["z"],
+                                           r["w"], r["y"], d_status=status)
+
+    def unfused():
+        for r in runs:
+            gdn.gdn_decode_step(r["dims"], r["cw"], r["A"], r["dt"], r["x"], r["a"], r["b"],
+                                r["slot"], r["state"], r["conv"], r["o"], d_status=status)
+            gdn.gdn_gated_rmsnorm(r["dims"], r["w"], r["o"], r["z"], y=r["y"])
+
+    out = {}
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        for _ in range(max(warmup, 1)):
+            fn()
+        evs = [(mk(), mk()) for _ in range(steps)]
+        for a_, b_ in evs:
+            a_.record()
+            fn()
+            b_.record()
+        torch.cuda.synchronize()
+        out[name + "_ms_per_step"] = statistics.median(a_.elapsed_time(b_) for a_, b_ in evs)
+    out["saving_vs_unfused"] = 1.0 - out["fused_ms_per_step"] / out["unfused_ms_per_step"]
+    return out
 
 
 CPU_BASELINE_SECONDS = 10.0
@@ -695,6 +736,8 @@ def run_gdn(args):
                              "kernel": "decode_step_kernel (one per-layer call)",
                              "peak_source": f"hbm_gbs ({peak_src})", "launch_ms": lms},
                 "frac_whole_step": gbs / hbm, "gpu_launches": dec["layers"] * len(dec["step_ms"]),
+                "gated_norm": dict(dec["gated_norm"], workload="the same step writing "
+                                   "y = rmsnorm(o) * w * SiLU(z) for every layer"),
                 "device_status": dec["status"]}
         if not args.no_cpu_baseline and world == 1:
             cores = os.cpu_count() or 1

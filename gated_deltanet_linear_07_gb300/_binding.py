@@ -91,6 +91,12 @@ def load() -> ctypes.CDLL:
     lib.gdn_prefill_checkpointed.restype = ctypes.c_int
     lib.gdn_slot_copy.argtypes = [D, P, P, I64, P, P, I32, P, P]
     lib.gdn_slot_copy.restype = ctypes.c_int
+    F = ctypes.c_float
+    lib.gdn_prefill_gated_norm.argtypes = [D, PR, P, P, P, P, I32, I64, P, P, P, P, I64, P, P, F,
+                                           P, P, SZ, P, P]
+    lib.gdn_prefill_gated_norm.restype = ctypes.c_int
+    lib.gdn_decode_step_gated_norm.argtypes = [D, PR, P, P, P, P, I32, P, P, I64, P, P, F, P, P, P]
+    lib.gdn_decode_step_gated_norm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -224,6 +230,71 @@ def gdn_prefill_checkpointed(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seql
         _ptr(slot_idx), _ptr(has_initial_state), _ptr(state_pool), _ptr(conv_pool), num_slots,
         _ptr(o), _ptr(workspace), ws_bytes, int(ckpt_every), _ptr(ckpt_slot), _ptr(d_status),
         _stream(stream)))
+
+
+def gdn_prefill_gated_norm(dims, conv_weight, A_log, dt_bias, x, a, b, cu_seqlens, slot_idx,
+                           has_initial_state, state_pool, conv_pool, z, norm_weight, y, workspace,
+                           eps=1e-6, d_status=None, stream=None):
+    """gdn_prefill with the gated RMSNorm of the output fused in: writes
+    y = rmsnorm(o) * norm_weight * SiLU(z) (see gdn_prefill_gated_norm in
+    include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    B = int(cu_seqlens.numel()) - 1
+    T = int(x.shape[0]) if x is not None else 0
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, T * cd)
+    _expect(a, "a", io, T * d.h_v)
+    _expect(b, "b", io, T * d.h_v)
+    _expect(z, "z", io, T * d.h_v * d.d_v)
+    _expect(y, "y", io, T * d.h_v * d.d_v)
+    _expect(norm_weight, "norm_weight", torch.float32, d.d_v)
+    _expect(cu_seqlens, "cu_seqlens", torch.int32)
+    _expect(slot_idx, "slot_idx", torch.int32, B)
+    _expect(has_initial_state, "has_initial_state", torch.uint8, B)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("gdn_prefill_gated_norm", load().gdn_prefill_gated_norm(
+        ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b), _ptr(cu_seqlens), B, T,
+        _ptr(slot_idx), _ptr(has_initial_state), _ptr(state_pool), _ptr(conv_pool), num_slots,
+        _ptr(z), _ptr(norm_weight), float(eps), _ptr(y), _ptr(workspace), ws_bytes,
+        _ptr(d_status), _stream(stream)))
+
+
+def gdn_decode_step_gated_norm(dims, conv_weight, A_log, dt_bias, x, a, b, slot_idx, state_pool,
+                               conv_pool, z, norm_weight, y, eps=1e-6, d_status=None, stream=None):
+    """gdn_decode_step with the gated RMSNorm of the output fused in (see
+    gdn_decode_step_gated_norm in include/gdn.h)."""
+    import torch
+    d = dims_from(dims)
+    io = _io_dtype(d)
+    n = int(slot_idx.numel())
+    cd = conv_dim(d)
+    _expect(conv_weight, "conv_weight", torch.float32, cd * d.conv_w)
+    _expect(A_log, "A_log", torch.float32, d.h_v)
+    _expect(dt_bias, "dt_bias", torch.float32, d.h_v)
+    _expect(x, "x", io, n * cd)
+    _expect(a, "a", io, n * d.h_v)
+    _expect(b, "b", io, n * d.h_v)
+    _expect(z, "z", io, n * d.h_v * d.d_v)
+    _expect(y, "y", io, n * d.h_v * d.d_v)
+    _expect(norm_weight, "norm_weight", torch.float32, d.d_v)
+    _expect(slot_idx, "slot_idx", torch.int32, n)
+    _expect(state_pool, "state_pool", torch.float32)
+    _expect(conv_pool, "conv_pool", io)
+    num_slots = state_pool.numel() // (d.h_v * d.d_k * d.d_v)
+    p = gdn_params(conv_weight.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr())
+    _check("gdn_decode_step_gated_norm", load().gdn_decode_step_gated_norm(
+        ctypes.byref(d), ctypes.byref(p), _ptr(x), _ptr(a), _ptr(b), _ptr(slot_idx), n,
+        _ptr(state_pool), _ptr(conv_pool), num_slots, _ptr(z), _ptr(norm_weight), float(eps),
+        _ptr(y), _ptr(d_status), _stream(stream)))
 
 
 def gdn_slot_copy(dims, state_pool, conv_pool, src_slot, dst_slot, d_status=None, stream=None):

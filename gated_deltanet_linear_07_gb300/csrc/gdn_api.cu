@@ -150,7 +150,8 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
                         int64_t total_tokens, const int32_t* slot_idx,
                         const uint8_t* has_initial_state, float* state_pool, void* conv_pool,
                         int64_t num_slots, void* o, void* workspace, size_t workspace_bytes,
-                        int32_t ckpt_every_chunks, const int32_t* ckpt_slot, int32_t* d_status,
+                        int32_t ckpt_every_chunks, const int32_t* ckpt_slot, const void* z,
+                        const float* norm_weight, float norm_eps, int32_t* d_status,
                         gdn_trace* trace, gdn_stream_t stream) {
   if (trace) {
     trace->launches = 0;
@@ -191,16 +192,25 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   p.ws_v = reinterpret_cast<float*>(ws + L.v);
   p.ws_g = reinterpret_cast<float*>(ws + L.g);
   p.ws_beta = reinterpret_cast<float*>(ws + L.beta);
+  cudaError_t e;
   if (use_tc(dims)) {
     p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
     p.chunk_ready = reinterpret_cast<int32_t*>(ws + L.ready);
     p.max_chunks = L.max_chunks;
     p.kq_ws = reinterpret_cast<uint8_t*>(ws + L.kq);
     p.vh_ws = reinterpret_cast<uint8_t*>(ws + L.vh);
-    return cuda_rc(gdn_launch_prefill_tc(p, reinterpret_cast<cudaStream_t>(stream), trace));
+    e = gdn_launch_prefill_tc(p, reinterpret_cast<cudaStream_t>(stream), trace);
+  } else {
+    e = gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace);
   }
-  return cuda_rc(
-      gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace));
+  // The gated norm of the output, in place on o, right after the layer: both
+  // prefill scans write o from several warps or CTAs per token, and a norm in
+  // the tensor-core scan's output warps lengthened its chunk period (they are
+  // short of issue slots there), so the standalone kernel is the faster way.
+  if (e == cudaSuccess && z && total_tokens > 0)
+    e = gdn_launch_gated_rmsnorm(norm_weight, norm_eps, o, z, total_tokens * dims->h_v, dims->d_v,
+                                 dims->io, o, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_rc(e);
 }
 
 GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
@@ -213,7 +223,7 @@ GDN_EXPORT int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params
                                   gdn_stream_t stream) {
   return prefill_impl(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
                       has_initial_state, state_pool, conv_pool, num_slots, o, workspace,
-                      workspace_bytes, 0, nullptr, d_status, trace, stream);
+                      workspace_bytes, 0, nullptr, nullptr, nullptr, 0.f, d_status, trace, stream);
 }
 
 GDN_EXPORT int gdn_prefill_checkpointed(const gdn_dims* dims, const gdn_params* params,
@@ -231,8 +241,29 @@ GDN_EXPORT int gdn_prefill_checkpointed(const gdn_dims* dims, const gdn_params* 
   if (ckpt_every / dims->chunk > INT32_MAX) return GDN_EUNSUPPORTED;
   return prefill_impl(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
                       has_initial_state, state_pool, conv_pool, num_slots, o, workspace,
-                      workspace_bytes, (int32_t)(ckpt_every / dims->chunk), ckpt_slot, d_status,
-                      nullptr, stream);
+                      workspace_bytes, (int32_t)(ckpt_every / dims->chunk), ckpt_slot, nullptr,
+                      nullptr, 0.f, d_status, nullptr, stream);
+}
+
+GDN_EXPORT int gdn_prefill_gated_norm(const gdn_dims* dims, const gdn_params* params,
+                                      const void* x, const void* a, const void* b,
+                                      const int32_t* cu_seqlens, int32_t num_seqs,
+                                      int64_t total_tokens, const int32_t* slot_idx,
+                                      const uint8_t* has_initial_state, float* state_pool,
+                                      void* conv_pool, int64_t num_slots, const void* z,
+                                      const float* norm_weight, float eps, void* y,
+                                      void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                      gdn_stream_t stream) {
+  const int rc = check_prefill_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (!(eps >= 0.f) || eps > 1e30f) return GDN_EINVAL;   // also rejects NaN
+  if (total_tokens > 0 && (!z || !norm_weight)) return GDN_EINVAL;
+  if (z && z == y) return GDN_EINVAL;   // the SIMT path writes o into y before the norm reads z
+  if ((z && !aligned16(z)) || (norm_weight && !aligned16(norm_weight))) return GDN_EALIGN;
+  return prefill_impl(dims, params, x, a, b, cu_seqlens, num_seqs, total_tokens, slot_idx,
+                      has_initial_state, state_pool, conv_pool, num_slots, y, workspace,
+                      workspace_bytes, 0, nullptr, total_tokens > 0 ? z : nullptr, norm_weight,
+                      eps, d_status, nullptr, stream);
 }
 
 GDN_EXPORT int gdn_slot_copy(const gdn_dims* dims, float* state_pool, void* conv_pool,
@@ -264,10 +295,12 @@ GDN_EXPORT int gdn_prefill(const gdn_dims* dims, const gdn_params* params, const
                             workspace_bytes, d_status, nullptr, stream);
 }
 
-GDN_EXPORT int gdn_decode_step(const gdn_dims* dims, const gdn_params* params, const void* x,
-                               const void* a, const void* b, const int32_t* slot_idx, int32_t n,
-                               float* state_pool, void* conv_pool, int64_t num_slots, void* o,
-                               int32_t* d_status, gdn_stream_t stream) {
+// The decode step behind both public variants; z = null: plain o.
+static int decode_impl(const gdn_dims* dims, const gdn_params* params, const void* x,
+                       const void* a, const void* b, const int32_t* slot_idx, int32_t n,
+                       float* state_pool, void* conv_pool, int64_t num_slots, void* o,
+                       const void* z, const float* norm_weight, float norm_eps,
+                       int32_t* d_status, gdn_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != GDN_OK) return rc;
   if (!params || n < 0 || num_slots < 0) return GDN_EINVAL;
@@ -285,6 +318,31 @@ GDN_EXPORT int gdn_decode_step(const gdn_dims* dims, const gdn_params* params, c
   p.x = x; p.a = a; p.b = b; p.slot_idx = slot_idx;
   p.conv_weight = params->conv_weight; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
   p.state_pool = state_pool; p.conv_pool = conv_pool; p.o = o; p.d_status = d_status;
+  p.z = z; p.norm_weight = norm_weight; p.norm_eps = norm_eps;
   return cuda_rc(gdn_launch_decode(p, dims->d_k, dims->d_v, dims->io,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+GDN_EXPORT int gdn_decode_step(const gdn_dims* dims, const gdn_params* params, const void* x,
+                               const void* a, const void* b, const int32_t* slot_idx, int32_t n,
+                               float* state_pool, void* conv_pool, int64_t num_slots, void* o,
+                               int32_t* d_status, gdn_stream_t stream) {
+  return decode_impl(dims, params, x, a, b, slot_idx, n, state_pool, conv_pool, num_slots, o,
+                     nullptr, nullptr, 0.f, d_status, stream);
+}
+
+GDN_EXPORT int gdn_decode_step_gated_norm(const gdn_dims* dims, const gdn_params* params,
+                                          const void* x, const void* a, const void* b,
+                                          const int32_t* slot_idx, int32_t n, float* state_pool,
+                                          void* conv_pool, int64_t num_slots, const void* z,
+                                          const float* norm_weight, float eps, void* y,
+                                          int32_t* d_status, gdn_stream_t stream) {
+  const int rc = check_dims(dims);
+  if (rc != GDN_OK) return rc;
+  if (!(eps >= 0.f) || eps > 1e30f) return GDN_EINVAL;   // also rejects NaN
+  if (n > 0 && (!z || !norm_weight)) return GDN_EINVAL;
+  if (z && z == y) return GDN_EINVAL;
+  if ((z && !aligned16(z)) || (norm_weight && !aligned16(norm_weight))) return GDN_EALIGN;
+  return decode_impl(dims, params, x, a, b, slot_idx, n, state_pool, conv_pool, num_slots, y,
+                     n > 0 ? z : nullptr, norm_weight, eps, d_status, stream);
 }

@@ -84,6 +84,10 @@ struct GdnDecodeArgs {
   void* conv_pool;
   void* o;
   int32_t* d_status;
+  // fused gated RMSNorm of the output (null z: plain o): o <- rmsnorm(o) w SiLU(z)
+  const void* z;            // [n][h_v][d_v], I/O dtype
+  const float* norm_weight; // [d_v]
+  float norm_eps;
 };
 
 struct GdnConvArgs {

@@ -64,6 +64,9 @@ decode_step_kernel(const GdnDecodeArgs args) {
   __shared__ __align__(16) float s_delta[DV];
   __shared__ float s_red[2][C::NW][DV];
   __shared__ float s_scal[4];
+  __shared__ float s_nrm[(DV + 31) / 32];   // fused gated norm: per-warp sums of o^2
+  static_assert(C::NT >= DV, "one output value per thread");
+  const bool fuse = args.z != nullptr;
 
   const int slot = args.slot_idx[n];
   if (slot < 0 || slot >= args.num_slots) {
@@ -135,6 +138,14 @@ decode_step_kernel(const GdnDecodeArgs args) {
                            args.A_log[h], args.dt_bias[h]);
     const float alpha = expf(g);
     const float beta = sigmoidf_(ld_io(reinterpret_cast<const IO*>(args.b) + (size_t)n * args.h_v + h));
+    // fused gated norm: the gate and weight are fetched now, used after the
+    // state write-back
+    const size_t oi = ((size_t)n * args.h_v + h) * DV + t;
+    float zv = 0.f, wt = 0.f;
+    if (fuse && t < DV) {
+      zv = ld_io(reinterpret_cast<const IO*>(args.z) + oi);
+      wt = args.norm_weight[t];
+    }
     __syncthreads();  // s_v written, s_q / s_k normalised
 
     float u[4] = {0.f, 0.f, 0.f, 0.f}, r[4] = {0.f, 0.f, 0.f, 0.f};
@@ -166,7 +177,9 @@ decode_step_kernel(const GdnDecodeArgs args) {
       }
     }
     __syncthreads();
-    for (int j = t; j < DV; j += C::NT) {
+    float oj = 0.f;   // this thread's output value (j = t < DV)
+    if (t < DV) {
+      const int j = t;
       float uj = 0.f, rj = 0.f;
 #pragma unroll
       for (int ww = 0; ww < C::NW; ++ww) {
@@ -175,7 +188,15 @@ decode_step_kernel(const GdnDecodeArgs args) {
       }
       const float d = beta * (s_v[j] - alpha * uj);
       s_delta[j] = d;
-      st_io(o + ((size_t)n * args.h_v + h) * DV + j, fmaf(alpha, rj, d * s_scal[2]));
+      oj = fmaf(alpha, rj, d * s_scal[2]);
+      if (!fuse) st_io(o + oi, oj);
+    }
+    if (fuse) {
+      // gated RMSNorm over the head's d_v values (the gdn_gated_rmsnorm
+      // definition): y = o / sqrt(mean(o^2) + eps) * w * SiLU(z); the per-warp
+      // sums of o^2 cross the barrier the state update needs anyway
+      const float sq = warp_sum(oj * oj);
+      if ((t & 31) == 0 && t < DV) s_nrm[t >> 5] = sq;
     }
     __syncthreads();
     const float4 dl = *reinterpret_cast<const float4*>(&s_delta[4 * cg]);
@@ -190,7 +211,14 @@ decode_step_kernel(const GdnDecodeArgs args) {
       s.w = fmaf(alpha, S[m].w, ki * dl.w);
       st_stream(base + (size_t)i * C::CG + cg, s);
     }
-    __syncthreads();  // s_v / s_red / s_delta reused by the next head
+    if (fuse && t < DV) {
+      float tot = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < (DV + 31) / 32; ++ww) tot += s_nrm[ww];
+      const float inv = rsqrtf(tot * (1.0f / DV) + args.norm_eps);
+      st_io(o + oi, oj * inv * wt * silu(zv));
+    }
+    __syncthreads();  // s_v / s_red / s_delta / s_nrm reused by the next head
   }
 }
 

@@ -306,6 +306,43 @@ int gdn_slot_copy(const gdn_dims* dims, float* state_pool, void* conv_pool,
                   int64_t num_slots, const int32_t* src_slot, const int32_t* dst_slot,
                   int32_t n, int32_t* d_status, gdn_stream_t stream);
 
+/*
+ * gdn_prefill_gated_norm / gdn_decode_step_gated_norm -- gdn_prefill and
+ * gdn_decode_step followed by the gated RMSNorm of the layer output (the norm
+ * that follows the Gated DeltaNet core in the Qwen3.5 layer: oxydllm release
+ * notes, New Features, GGUF qwen35 architecture and "Gated DeltaNet fast
+ * paths"; PicoLM changelog, SSM/GDN kernel notes): instead of o they write
+ *     y[t][h][:] = o[t][h][:] / sqrt(mean_j o[t][h][j]^2 + eps) * w * SiLU(z[t][h][:])
+ * exactly as gdn_gated_rmsnorm defines it.  Same arguments as gdn_prefill /
+ * gdn_decode_step, with the output o replaced by:
+ *   z            device, I/O dtype, [total_tokens or n][h_v][d_v], 16-byte aligned
+ *   norm_weight  device fp32 [d_v], 16-byte aligned
+ *   eps          >= 0 (NaN or negative: GDN_EINVAL)
+ *   y            device, I/O dtype, [total_tokens or n][h_v][d_v]; must not
+ *                overlap z (y == z: GDN_EINVAL) nor any other input
+ * In decode the norm runs in the step's own epilogue (one CTA holds a head's
+ * whole output row), so o never reaches memory.  In prefill the layer writes o
+ * into y and the standalone norm kernel rewrites it in place on the same
+ * stream: the scans spread a token's values over several warps (tensor-core
+ * path) or CTAs (SIMT path), and a norm inside the tensor-core scan's output
+ * warps lengthened its chunk period, so two launches are the faster order.
+ */
+int gdn_prefill_gated_norm(const gdn_dims* dims, const gdn_params* params,
+                           const void* x, const void* a, const void* b,
+                           const int32_t* cu_seqlens, int32_t num_seqs,
+                           int64_t total_tokens, const int32_t* slot_idx,
+                           const uint8_t* has_initial_state, float* state_pool,
+                           void* conv_pool, int64_t num_slots, const void* z,
+                           const float* norm_weight, float eps, void* y,
+                           void* workspace, size_t workspace_bytes,
+                           int32_t* d_status, gdn_stream_t stream);
+int gdn_decode_step_gated_norm(const gdn_dims* dims, const gdn_params* params,
+                               const void* x, const void* a, const void* b,
+                               const int32_t* slot_idx, int32_t n, float* state_pool,
+                               void* conv_pool, int64_t num_slots, const void* z,
+                               const float* norm_weight, float eps, void* y,
+                               int32_t* d_status, gdn_stream_t stream);
+
 /* Static description of a gdn_status code. */
 const char* gdn_status_str(int status);
 

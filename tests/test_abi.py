@@ -168,3 +168,36 @@ def test_slot_copy_and_checkpointed_prefill_reject_bad_calls_before_launch(lib):
     assert ck(ckpt=None) == -1
     assert ck(cu=None) == -1                       # and every gdn_prefill check still applies
     assert ck(x=FAKE + 2) == -5
+
+
+def test_fused_gated_norm_variants_reject_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    p = _binding.gdn_params(FAKE, FAKE, FAKE)
+    Z, Y = FAKE + 4096, FAKE + 8192
+
+    def pf(dims=d, z=Z, w=FAKE, eps=1e-6, y=Y, T=64, cu=FAKE):
+        return lib.gdn_prefill_gated_norm(
+            ctypes.byref(dims), ctypes.byref(p), FAKE, FAKE, FAKE, cu, 1, T, FAKE, None, FAKE,
+            FAKE, 1, z, w, ctypes.c_float(eps), y, FAKE, 1 << 40, None, None)
+    assert pf(dims=gdn.make_dims(**dict(D4B, d_v=48))) == -2
+    assert pf(z=None) == -1
+    assert pf(w=None) == -1
+    assert pf(eps=-1.0) == -1
+    assert pf(eps=float("nan")) == -1
+    assert pf(y=Z) == -1                           # y may not alias z
+    assert pf(z=Z + 8) == -5
+    assert pf(w=FAKE + 4) == -5
+    assert pf(y=Y + 2) == -5                       # y is the layer's output buffer
+    assert pf(cu=None) == -1                       # and every gdn_prefill check still applies
+
+    def dc(z=Z, w=FAKE, eps=1e-6, y=Y, n=4):
+        return lib.gdn_decode_step_gated_norm(
+            ctypes.byref(d), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, n, FAKE, FAKE, 8, z, w,
+            ctypes.c_float(eps), y, None, None)
+    assert dc(z=None) == -1
+    assert dc(w=None) == -1
+    assert dc(eps=float("nan")) == -1
+    assert dc(y=Z) == -1
+    assert dc(z=Z + 8) == -5
+    assert dc(y=Y + 4) == -5
+    assert dc(n=0) == 0                            # nothing to do
