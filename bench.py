@@ -403,6 +403,29 @@ def bench_checkpointed(torch, gdn, run, steps, warmup, every=256):
             "checkpoints": n_ck, "T": T, "status": int(run.status.item())}
 
 
+def bench_fp32_state(torch, gdn, inp, device, steps, warmup):
+    """The timed prefill with GDN_FP32_STATE (every product with the state in
+    fp32: the SIMT path) on the same inputs; L2 flushed before every step."""
+    import dataclasses
+    run = Prefill(torch, gdn, dict(inp, dims=dataclasses.replace(inp["dims"], flags=gdn.GDN_FP32_STATE)),
+                  device)
+    flush = L2Flush(torch, device)
+    for _ in range(max(warmup, 1)):
+        run()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for a_, b_ in ev:
+        flush()
+        a_.record()
+        run()
+        b_.record()
+    torch.cuda.synchronize()
+    out = {"ms": statistics.median(a_.elapsed_time(b_) for a_, b_ in ev), "T": run.T,
+           "status": int(run.status.item())}
+    del run
+    return out
+
+
 def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64):
     runs = []
     for layer in range(layers):
@@ -601,7 +624,7 @@ def run_gdn(args):
     if not args.no_prefill:
         pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
         barrier()
-    gn = sc = ck = None
+    gn = sc = ck = f32 = None
     if pf is not None:
         gn = bench_gated_norm(torch, gdn, pf["inp"]["dims"], pf["inp"]["x"].shape[0], device,
                               args.steps, args.warmup)
@@ -609,6 +632,8 @@ def run_gdn(args):
         sc = bench_slot_copy(torch, gdn, pf["inp"]["dims"], device, args.steps, args.warmup)
         barrier()
         ck = bench_checkpointed(torch, gdn, pf["run"], args.steps, args.warmup)
+        barrier()
+        f32 = bench_fp32_state(torch, gdn, pf["inp"], device, args.steps, args.warmup)
         barrier()
     dec = None
     if not args.no_decode:
@@ -720,6 +745,14 @@ def run_gdn(args):
                            "checkpoints_per_step": ck["checkpoints"],
                            "l2": "flushed before every timed step"},
                 "device_status": ck["status"]}
+        if f32:
+            line["fp32_state_prefill"] = {
+                "metric": "prefill tokens/s with fp32 state products (GDN_FP32_STATE)",
+                "unit": "tokens/s", "value": f32["T"] / (f32["ms"] / 1e3), "ms_per_step": f32["ms"],
+                "slowdown_vs_tensor_core": f32["ms"] / ms,
+                "config": {"workload": "the timed prefill through the SIMT path, fp32 state products",
+                           "l2": "flushed before every timed step"},
+                "device_status": f32["status"]}
         if dec:
             # whole job: every rank moves its own replica's state bytes
             gbs = replica_throughput(world, dec["state_bytes"], dms) / 1e9

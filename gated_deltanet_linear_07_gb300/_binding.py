@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(PKG, "libgdn_gb300.so")
 
 GDN_FP32, GDN_BF16 = 0, 1
 GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+GDN_FP32_STATE = 0x1   # gdn_dims.flags: fp32 state products in prefill
 STATUS = {0: "GDN_OK", -1: "GDN_EINVAL", -2: "GDN_EUNSUPPORTED", -3: "GDN_ECUDA",
           -4: "GDN_EWORKSPACE", -5: "GDN_EALIGN"}
 
@@ -29,7 +30,7 @@ class GdnError(RuntimeError):
 class gdn_dims(ctypes.Structure):
     _fields_ = [("h_k", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("conv_w", ctypes.c_int32), ("chunk", ctypes.c_int32),
-                ("io", ctypes.c_int32), ("l2_eps", ctypes.c_float)]
+                ("io", ctypes.c_int32), ("l2_eps", ctypes.c_float), ("flags", ctypes.c_int32)]
 
 
 class gdn_params(ctypes.Structure):
@@ -47,16 +48,19 @@ class gdn_trace(ctypes.Structure):
                 ("launches", ctypes.c_int32), ("stages_run", ctypes.c_int32)]
 
 
-def make_dims(h_k, h_v, d_k, d_v, chunk=64, io="bf16", conv_w=4, l2_eps=1e-6) -> gdn_dims:
+def make_dims(h_k, h_v, d_k, d_v, chunk=64, io="bf16", conv_w=4, l2_eps=1e-6,
+              flags=0) -> gdn_dims:
     io_code = {"fp32": GDN_FP32, "bf16": GDN_BF16}[io] if isinstance(io, str) else int(io)
-    return gdn_dims(h_k, h_v, d_k, d_v, conv_w, chunk, io_code, l2_eps)
+    return gdn_dims(h_k, h_v, d_k, d_v, conv_w, chunk, io_code, l2_eps, flags)
 
 
 def dims_from(d) -> gdn_dims:
-    """gdn_dims from any object with h_k, h_v, d_k, d_v, chunk, io, conv_w, l2_eps."""
+    """gdn_dims from any object with h_k, h_v, d_k, d_v, chunk, io, conv_w, l2_eps
+    (and optionally flags)."""
     if isinstance(d, gdn_dims):
         return d
-    return make_dims(d.h_k, d.h_v, d.d_k, d.d_v, d.chunk, d.io, d.conv_w, d.l2_eps)
+    return make_dims(d.h_k, d.h_v, d.d_k, d.d_v, d.chunk, d.io, d.conv_w, d.l2_eps,
+                     getattr(d, "flags", 0))
 
 
 def load() -> ctypes.CDLL:

@@ -29,6 +29,7 @@ int check_dims(const gdn_dims* d) {
   if (!d) return GDN_EINVAL;
   if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0) return GDN_EINVAL;
   if (!(d->l2_eps >= 0.0f)) return GDN_EINVAL;
+  if (d->flags & ~GDN_FP32_STATE) return GDN_EINVAL;
   if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
   if (d->conv_w != 4) return GDN_EUNSUPPORTED;
   if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
@@ -47,7 +48,8 @@ int check_prefill_dims(const gdn_dims* d) {
 }
 
 bool use_tc(const gdn_dims* d) {
-  return gdn_tc_prefill_supported(d->h_k, d->h_v, d->d_k, d->d_v, d->chunk, d->io);
+  return (d->flags & GDN_FP32_STATE) == 0 &&
+         gdn_tc_prefill_supported(d->h_k, d->h_v, d->d_k, d->d_v, d->chunk, d->io);
 }
 
 struct PrefillLayout {

@@ -157,13 +157,15 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
 }
 
 struct ScanSmem {
-  // offsets in floats
-  int H, K, Q, V, U, Wk, A, T, gam, beta, n;
+  // offsets in floats; K and Q rows are padded to d_k + 1 floats, so that the
+  // lanes of a warp reading one column of K for different tokens (K K^T, Q K^T)
+  // hit different banks
+  int H, K, Q, V, U, Wk, A, T, gam, beta, be, dl, eg, n;
   __host__ __device__ ScanSmem(int C, int DK, int DVT) {
     int o = 0;
     H = o; o += DK * DVT;
-    K = o; o += C * DK;
-    Q = o; o += C * DK;
+    K = o; o += C * (DK + 1);
+    Q = o; o += C * (DK + 1);
     V = o; o += C * DVT;
     U = o; o += C * DVT;
     Wk = o; o += C * DK;
@@ -171,6 +173,9 @@ struct ScanSmem {
     T = o; o += C * C;
     gam = o; o += C;
     beta = o; o += C;
+    be = o; o += C;   // beta_s e^{gamma_s}
+    dl = o; o += C;   // e^{gamma_last - gamma_r}
+    eg = o; o += C;   // e^{gamma_r}
     n = o;
   }
 };
@@ -190,8 +195,8 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
   }
   const ScanSmem L(C, DK, DVT);
   float* sH = sm + L.H;    // [DK][DVT]   S^T tile
-  float* sK = sm + L.K;    // [C][DK]
-  float* sQ = sm + L.Q;    // [C][DK]
+  float* sK = sm + L.K;    // [C][DK + 1]
+  float* sQ = sm + L.Q;    // [C][DK + 1]
   float* sV = sm + L.V;    // [C][DVT]
   float* sU = sm + L.U;    // [C][DVT]    U, then W
   float* sWk = sm + L.Wk;  // [C][DK]
@@ -199,6 +204,10 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
   float* sT = sm + L.T;    // [C][C]
   float* sG = sm + L.gam;  // [C]         cumulative log-decay
   float* sB = sm + L.beta; // [C]
+  float* sBe = sm + L.be;  // [C]
+  float* sDl = sm + L.dl;  // [C]
+  float* sEg = sm + L.eg;  // [C]
+  const int KS = DK + 1;   // row stride of sK, sQ
 
   const int hk = h / (args.h_v / args.h_k);
   const int64_t start = args.cu_seqlens[b];
@@ -217,8 +226,8 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     for (int e = tid; e < C * DK; e += NT) {
       const int r = e / DK, i = e % DK;
       const size_t tk = (size_t)(start + c0 + r);
-      sK[e] = r < Lc ? args.ws_k[(tk * args.h_k + hk) * DK + i] : 0.f;
-      sQ[e] = r < Lc ? args.ws_q[(tk * args.h_k + hk) * DK + i] : 0.f;
+      sK[r * KS + i] = r < Lc ? args.ws_k[(tk * args.h_k + hk) * DK + i] : 0.f;
+      sQ[r * KS + i] = r < Lc ? args.ws_q[(tk * args.h_k + hk) * DK + i] : 0.f;
     }
     for (int e = tid; e < C * DVT; e += NT) {
       const int r = e / DVT, j = e % DVT;
@@ -235,30 +244,36 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
       }
     }
     __syncthreads();
+    for (int r = tid; r < C; r += NT) {
+      sBe[r] = sB[r] * expf(sG[r]);
+      sDl[r] = expf(sG[C - 1] - sG[r]);
+      sEg[r] = expf(sG[r]);
+    }
     // A (strictly lower), P (lower incl. diagonal) need K K^T and Q K^T
     for (int e = tid; e < C * C; e += NT) {
       const int r = e / C, s = e % C;
       float a = 0.f;
       if (s < r) {
         float dot = 0.f;
-        for (int i = 0; i < DK; ++i) dot = fmaf(sK[r * DK + i], sK[s * DK + i], dot);
+        for (int i = 0; i < DK; ++i) dot = fmaf(sK[r * KS + i], sK[s * KS + i], dot);
         a = sB[r] * dot * expf(sG[r] - sG[s]);
       }
       sA[e] = a;
     }
     __syncthreads();
-    // T = (I + A)^-1: thread j owns column j; forward substitution down it.
-    for (int j = tid; j < C; j += NT) {
+    // T = (I + A)^-1 by forward substitution down each column j: T[r][j] =
+    // delta_rj - sum_{s<r} A[r][s] T[s][j].  TPC = NT / C threads share a column
+    // (adjacent lanes); thread q of the group owns the rows s = q mod TPC,
+    // sums its part of each row's series and the group adds the parts with
+    // shuffles.  Each T[s][j] is written and read only by its owner.
+    {
+      const int TPC = NT / C;              // 4, 8 or 16 (NT = 256, C = 64, 32, 16)
+      const int j = tid / TPC, q = tid % TPC;
       for (int r = 0; r < C; ++r) {
-        float v;
-        if (r < j) v = 0.f;
-        else if (r == j) v = 1.f;
-        else {
-          float acc = 0.f;
-          for (int s = j; s < r; ++s) acc = fmaf(sA[r * C + s], sT[s * C + j], acc);
-          v = -acc;
-        }
-        sT[r * C + j] = v;
+        float part = 0.f;
+        for (int s2 = q; s2 < r; s2 += TPC) part = fmaf(sA[r * C + s2], sT[s2 * C + j], part);
+        for (int m = TPC >> 1; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
+        if (r % TPC == q) sT[r * C + j] = r < j ? 0.f : (r == j ? 1.f : -part);
       }
     }
     __syncthreads();
@@ -272,8 +287,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     for (int e = tid; e < C * DK; e += NT) {
       const int r = e / DK, i = e % DK;
       float acc = 0.f;
-      for (int s = 0; s <= r; ++s)
-        acc = fmaf(sT[r * C + s] * sB[s] * expf(sG[s]), sK[s * DK + i], acc);
+      for (int s = 0; s <= r; ++s) acc = fmaf(sT[r * C + s] * sBe[s], sK[s * KS + i], acc);
       sWk[e] = acc;
     }
     __syncthreads();
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
       float p = 0.f;
       if (s <= r) {
         float dot = 0.f;
-        for (int i = 0; i < DK; ++i) dot = fmaf(sQ[r * DK + i], sK[s * DK + i], dot);
+        for (int i = 0; i < DK; ++i) dot = fmaf(sQ[r * KS + i], sK[s * KS + i], dot);
         p = dot * expf(sG[r] - sG[s]);
       }
       sA[e] = p;
@@ -299,10 +313,10 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     for (int e = tid; e < Lc * DVT; e += NT) {
       const int r = e / DVT, j = e % DVT;
       float qs = 0.f;
-      for (int i = 0; i < DK; ++i) qs = fmaf(sQ[r * DK + i], sH[i * DVT + j], qs);
+      for (int i = 0; i < DK; ++i) qs = fmaf(sQ[r * KS + i], sH[i * DVT + j], qs);
       float pw = 0.f;
       for (int s = 0; s <= r; ++s) pw = fmaf(sA[r * C + s], sU[s * DVT + j], pw);
-      const float ov = fmaf(expf(sG[r]), qs, pw);
+      const float ov = fmaf(sEg[r], qs, pw);
       st_io(out + ((size_t)(start + c0 + r) * args.h_v + h) * DV + j0 + j, ov);
     }
     __syncthreads();
@@ -316,8 +330,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     for (int e = tid; e < DK * DVT; e += NT) {
       const int i = e / DVT, j = e % DVT;
       float acc = 0.f;
-      for (int r = 0; r < Lc; ++r)
-        acc = fmaf(sK[r * DK + i] * expf(glast - sG[r]), sU[r * DVT + j], acc);
+      for (int r = 0; r < Lc; ++r) acc = fmaf(sK[r * KS + i] * sDl[r], sU[r * DVT + j], acc);
       sH[e] = fmaf(dlast, sH[e], acc);
       if (cst) cst[(size_t)i * DV + j0 + j] = sH[e];
     }

@@ -41,6 +41,7 @@ class Dims:
     chunk: int = 64
     io: str = "bf16"          # "fp32" | "bf16"
     l2_eps: float = 1e-6
+    flags: int = 0            # gdn_dims.flags (GDN_FP32_STATE)
 
     @property
     def conv_dim(self) -> int:

@@ -79,6 +79,16 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_DEV_BAD_CU_SEQLENS 0x2  /* cu_seqlens not 0..total_tokens non-decreasing: call skipped */
 #define GDN_DEV_WAIT_TIMEOUT 0x4    /* an inter-CTA wait gave up: results invalid */
 
+/* Bits of gdn_dims.flags.
+ * GDN_FP32_STATE: prefill keeps every product with the fp32 state in fp32
+ *   arithmetic (the SIMT path, any supported shape and chunk).  Without it the
+ *   tensor-core path, where it applies (d_k = d_v = 128, chunk 64, bf16 I/O,
+ *   h_v = 2 h_k), feeds the state to the MMAs rounded to bf16 (its products
+ *   accumulate in fp32); the error that rounding leaves in the state and in o
+ *   is measured against the fp32 option on long, correlated-key sequences by
+ *   the precision tests.  Decode always uses fp32 state products. */
+#define GDN_FP32_STATE 0x1
+
 typedef struct {
   int32_t h_k;     /* key/query heads */
   int32_t h_v;     /* value heads; multiple of h_k */
@@ -88,6 +98,7 @@ typedef struct {
   int32_t chunk;   /* prefill chunk length: 16, 32 or 64 */
   int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
   float l2_eps;    /* added to the sum of squares inside the L2-norm root */
+  int32_t flags;   /* GDN_FP32_STATE or 0; other bits: GDN_EINVAL */
 } gdn_dims;
 
 typedef struct {

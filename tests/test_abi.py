@@ -67,6 +67,13 @@ def test_workspace_size_rules(lib):
                 dict(D4B, conv_w=3), dict(D4B, io=7)):
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**bad), 4096, 1) == 0
     assert gdn.gdn_prefill_workspace_size(d, -1, 1) == 0
+    # GDN_FP32_STATE moves this shape to the SIMT path: its per-token fp32 layout
+    dfp = gdn.make_dims(**D4B, flags=gdn.GDN_FP32_STATE)
+    assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
+    assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) != w1
+    for bad_flags in (2, 4, -1):                   # unknown flag bits
+        assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**D4B, flags=bad_flags), 4096, 1) == 0
+        assert _prefill(lib, gdn.make_dims(**D4B, flags=bad_flags)) == -1
 
 
 FAKE = 1 << 20  # an aligned, never-dereferenced address: validation fails first

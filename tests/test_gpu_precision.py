@@ -1,0 +1,95 @@
+"""State-operand precision: the prefill with GDN_FP32_STATE (every product with
+the fp32 state in fp32, the SIMT path) against the float64 oracle, and the
+ablation of that option against the tensor-core path (the state fed to the
+MMAs as bf16) on the adversarial long-sequence workload.
+
+The fp32-state prefill is held to the fp32 tolerance of tests/_gpu.py on its
+final states (|err| <= 1e-3 max|ref| + 1e-5) even with bf16 I/O; its outputs,
+written in bf16, to the bf16 one.  In the ablation both variants meet their
+tolerances on every sampled (sequence, head), and the fp32-state final states
+are the closer ones.
+"""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+
+import gated_deltanet_linear_07_gb300 as gdn
+import oracle
+from gated_deltanet_linear_07_gb300 import workloads
+from gated_deltanet_linear_07_gb300.workloads import QWEN35_4B
+from tests._gpu import PrefillRun, assert_close, check_prefill, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+NCPU = os.cpu_count() or 1
+FP32_STATE = dataclasses.replace(QWEN35_4B, flags=gdn.GDN_FP32_STATE)
+FP32 = dataclasses.replace(QWEN35_4B, io="fp32")    # the fp32 tolerance, for states
+
+
+def _with_dims(inp, d):
+    out = dict(inp)
+    out["dims"] = d
+    return out
+
+
+@pytest.mark.parametrize("chunk", [64, 32])
+def test_fp32_state_prefill_matches_oracle(gpu_lib, chunk):
+    d = dataclasses.replace(FP32_STATE, chunk=chunk)
+    inp = workloads.layer_inputs(d, [130, 64, 300, 1, 77], seed=70 + chunk, init="mixed")
+    run = PrefillRun(inp)
+    run()
+    got = run.results()
+    ref = oracle_prefill(inp)
+    check_prefill(inp, got, ref)                       # bf16 tolerance on o
+    for s, slot in enumerate(inp["slot_idx"]):
+        assert_close(got["state_pool"][slot], ref["state"][s], FP32, f"state seq {s}")
+
+
+def _errors(got, ref, inp, mask):
+    cu = inp["cu_seqlens"]
+    eo, es = 0.0, 0.0
+    for s in range(mask.shape[0]):
+        slot = inp["slot_idx"][s]
+        for h in np.nonzero(mask[s])[0]:
+            r_o = ref["o"][cu[s]:cu[s + 1], h]
+            r_s = ref["state"][s, h]
+            eo = max(eo, float(np.abs(got["o"][cu[s]:cu[s + 1], h] - r_o).max() / np.abs(r_o).max()))
+            es = max(es, float(np.abs(got["state_pool"][slot, h] - r_s).max() / np.abs(r_s).max()))
+    return eo, es
+
+
+@pytest.mark.parametrize("sub", ["a", "b"])
+def test_state_precision_ablation_adversarial(gpu_lib, sub):
+    """4 x 32768 tokens of correlated keys (512 chunks per sequence): the
+    tensor-core path, the fp32-state path at chunk 64 and at chunk 32, each
+    against the oracle on 2 sampled heads per sequence."""
+    base = workloads.adversarial(sub=sub)
+    rng = np.random.default_rng(12)
+    mask = np.zeros((4, QWEN35_4B.h_v), bool)
+    for s in range(4):
+        mask[s, rng.choice(QWEN35_4B.h_v, 2, replace=False)] = True
+    ov = workloads.oracle_view(base)
+    ref = oracle.layer(base["x"], base["a"], base["b"], base["conv_weight"], base["A_log"],
+                       base["dt_bias"], base["cu_seqlens"], 16, 32, 128, 128,
+                       window0=ov["window0"], state0=ov["state0"], head_mask=mask,
+                       n_threads=NCPU)
+    errs = {}
+    for name, d in (("tensor-core, bf16 state operands", QWEN35_4B),
+                    ("fp32 state, chunk 64", FP32_STATE),
+                    ("fp32 state, chunk 32", dataclasses.replace(FP32_STATE, chunk=32))):
+        inp = _with_dims(base, d)
+        run = PrefillRun(inp)
+        run()
+        got = run.results()
+        assert got["status"] == 0
+        errs[name] = _errors(got, ref, inp, mask)
+        tol_state = 2e-2 if name.startswith("tensor") else 1e-3 + 1e-5
+        assert errs[name][0] <= 2e-2, (name, errs[name])
+        assert errs[name][1] <= tol_state, (name, errs[name])
+        del run
+    for name, (eo, es) in errs.items():
+        print(f"adversarial {sub}: {name:34s} worst normalised error o {eo:.2e} state {es:.2e}")
+    tc = errs["tensor-core, bf16 state operands"][1]
+    assert errs["fp32 state, chunk 64"][1] < tc
+    assert errs["fp32 state, chunk 32"][1] < tc
