@@ -234,6 +234,28 @@ class Prefill:
                              d_status=self.status, trace=trace)
 
 
+def trace_stages(torch, gdn, run, ev, flush):
+    """Attribution pass: the steps again with stage events and a launch count
+    (the events sit between kernels, so this pass is not the headline).
+    Returns the median ms of each stage that ran and the launches counted."""
+    launches = 0
+    traces = []
+    for e in ev:
+        flush()
+        tr = gdn.make_trace(e["b"], e["f"])
+        run(trace=tr)
+        launches += tr.launches
+        traces.append(tr)
+    torch.cuda.synchronize()
+    stage_ms = {}
+    for i, name in enumerate(gdn.STAGES):
+        vals = [e["b"][i].elapsed_time(e["f"][i]) for e, tr in zip(ev, traces)
+                if tr.stages_run & (1 << i)]
+        if vals:
+            stage_ms[name] = statistics.median(vals)
+    return stage_ms, launches
+
+
 def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     inp = workloads.prefill_4b()
     run = Prefill(torch, gdn, inp, device)
@@ -258,25 +280,7 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
         e["e"].record(stream)
     torch.cuda.synchronize()
     step_ms = [e["s"].elapsed_time(e["e"]) for e in ev]
-    # Attribution pass: the same steps with stage events and a launch count
-    # (the events sit between kernels, so this pass is not the headline).
-    launches = 0
-    traces = []
-    for e in ev:
-        flush()
-        tr = gdn.make_trace(e["b"], e["f"])
-        run(trace=tr)
-        launches += tr.launches
-        traces.append(tr)
-    torch.cuda.synchronize()
-    stage_ms = {}
-    for i, name in enumerate(ns):
-        vals = []
-        for e, tr in zip(ev, traces):
-            if tr.stages_run & (1 << i):
-                vals.append(e["b"][i].elapsed_time(e["f"][i]))
-        if vals:
-            stage_ms[name] = statistics.median(vals)
+    stage_ms, launches = trace_stages(torch, gdn, run, ev, flush)
     status = int(run.status.item())
     return {"inp": inp, "run": run, "step_ms": step_ms, "stage_ms": stage_ms,
             "launches": launches, "status": status}
@@ -413,15 +417,22 @@ def bench_fp32_state(torch, gdn, inp, device, steps, warmup):
     for _ in range(max(warmup, 1)):
         run()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    ev = [(mk(), mk()) for _ in range(steps)]
-    for a_, b_ in ev:
-        flush()
-        a_.record()
-        run()
-        b_.record()
+    ev = [{"s": mk(), "e": mk(), "b": [mk() for _ in gdn.STAGES], "f": [mk() for _ in gdn.STAGES]}
+          for _ in range(steps)]
+    stream = torch.cuda.current_stream()
+    for e in ev:   # create the event handles before handing them to the library
+        for x in [e["s"], e["e"], *e["b"], *e["f"]]:
+            x.record(stream)
     torch.cuda.synchronize()
-    out = {"ms": statistics.median(a_.elapsed_time(b_) for a_, b_ in ev), "T": run.T,
-           "status": int(run.status.item())}
+    for e in ev:
+        flush()
+        e["s"].record(stream)
+        run()
+        e["e"].record(stream)
+    torch.cuda.synchronize()
+    stage_ms, _ = trace_stages(torch, gdn, run, ev, flush)
+    out = {"ms": statistics.median(e["s"].elapsed_time(e["e"]) for e in ev), "T": run.T,
+           "stages_ms": stage_ms, "status": int(run.status.item())}
     del run
     return out
 
@@ -749,7 +760,7 @@ def run_gdn(args):
             line["fp32_state_prefill"] = {
                 "metric": "prefill tokens/s with fp32 state products (GDN_FP32_STATE)",
                 "unit": "tokens/s", "value": f32["T"] / (f32["ms"] / 1e3), "ms_per_step": f32["ms"],
-                "slowdown_vs_tensor_core": f32["ms"] / ms,
+                "slowdown_vs_tensor_core": f32["ms"] / ms, "stages_ms": f32["stages_ms"],
                 "config": {"workload": "the timed prefill through the SIMT path, fp32 state products",
                            "l2": "flushed before every timed step"},
                 "device_status": f32["status"]}

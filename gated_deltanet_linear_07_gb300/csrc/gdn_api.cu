@@ -54,7 +54,7 @@ bool use_tc(const gdn_dims* d) {
 
 struct PrefillLayout {
   // SIMT path
-  size_t flag, q, k, v, g, beta;
+  size_t flag, q, k, v, g, beta, u, wk, p, gam;
   // tensor-core path
   size_t chunk_off, ready, kq, vh;
   int64_t max_chunks;
@@ -74,11 +74,17 @@ PrefillLayout prefill_layout(const gdn_dims* d, int64_t T, int64_t B) {
     L.kq = o; o += (size_t)L.max_chunks * d->h_k * gdn_tc_kq_bytes();
     L.vh = o; o += (size_t)L.max_chunks * d->h_v * gdn_tc_vh_bytes();
   } else {
+    L.max_chunks = (T + d->chunk - 1) / d->chunk + B;
+    L.chunk_off = o; o += align_up((size_t)(B + 1) * sizeof(int32_t));
     L.q = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
     L.k = o; o += align_up((size_t)T * d->h_k * d->d_k * sizeof(float));
     L.v = o; o += align_up((size_t)T * d->h_v * d->d_v * sizeof(float));
     L.g = o; o += align_up((size_t)T * d->h_v * sizeof(float));
     L.beta = o; o += align_up((size_t)T * d->h_v * sizeof(float));
+    L.u = o; o += align_up((size_t)T * d->h_v * d->d_v * sizeof(float));
+    L.wk = o; o += align_up((size_t)T * d->h_v * d->d_k * sizeof(float));
+    L.p = o; o += align_up((size_t)T * d->h_v * d->chunk * sizeof(float));
+    L.gam = o; o += align_up((size_t)T * d->h_v * sizeof(float));
   }
   L.total = o;
   return L;
@@ -203,6 +209,12 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
     p.vh_ws = reinterpret_cast<uint8_t*>(ws + L.vh);
     e = gdn_launch_prefill_tc(p, reinterpret_cast<cudaStream_t>(stream), trace);
   } else {
+    p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
+    p.max_chunks = L.max_chunks;
+    p.ws_u = reinterpret_cast<float*>(ws + L.u);
+    p.ws_wk = reinterpret_cast<float*>(ws + L.wk);
+    p.ws_p = reinterpret_cast<float*>(ws + L.p);
+    p.ws_gam = reinterpret_cast<float*>(ws + L.gam);
     e = gdn_launch_prefill_simt(p, dims->io, reinterpret_cast<cudaStream_t>(stream), trace);
   }
   // The gated norm of the output, in place on o, right after the layer: both

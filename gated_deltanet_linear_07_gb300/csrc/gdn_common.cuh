@@ -125,6 +125,11 @@ struct GdnPrefillArgs {
   float* ws_v;       // [T][h_v][d_v]
   float* ws_g;       // [T][h_v] log-decay
   float* ws_beta;    // [T][h_v]
+  // SIMT path, written by its chunk kernel per token row of each chunk
+  float* ws_u;       // [T][h_v][d_v]  U = T diag(beta) V
+  float* ws_wk;      // [T][h_v][d_k]  Wk = T diag(beta e^gamma) K
+  float* ws_p;       // [T][h_v][chunk] P = tril(Q K^T * decay)
+  float* ws_gam;     // [T][h_v]       cumulative log-decay inside the chunk
   // tensor-core path workspace
   int32_t* chunk_off;   // [num_seqs+1] first global chunk of each sequence
   int64_t max_chunks;   // bound on the number of chunks: ceil(T/64) + num_seqs

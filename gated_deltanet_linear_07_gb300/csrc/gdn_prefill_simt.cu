@@ -11,35 +11,68 @@
 //                         history before the sequence start) + SiLU, L2 norm
 //                         of q and k with the 1/sqrt(d_k) query scale, gates.
 //   3. window_writeback   the last W-1 raw inputs of each sequence to its slot.
-//   4. scan               one CTA per (sequence, value head, d_v tile): the
-//                         chunked WY form, sequential over chunks, state in
-//                         shared memory.  Per chunk with cumulative log-decay
-//                         gamma (oxydllm 0.0.0-alpha.12.2 release notes, New
+//   4. chunk              one CTA per (chunk, value head), all chunks at once:
+//                         the state-independent factors of the chunked WY form
+//                         (oxydllm 0.0.0-alpha.12.2 release notes, New
 //                         Features, "Gated DeltaNet runtime": chunked parallel
-//                         scan, per-chunk unit-lower-triangular system):
+//                         scan, per-chunk unit-lower-triangular system), with
+//                         gamma the cumulative log-decay inside the chunk:
 //       A = strict_tril(diag(beta) K K^T * e^{gamma_r - gamma_s})
 //       T = (I + A)^-1           (column-wise forward substitution: exact
 //                                 entries, no matrix powers, finite on fully
 //                                 correlated keys)
-//       U = T diag(beta) V,  Wk = T diag(beta e^gamma) K
+//       U = T diag(beta) V,  Wk = T diag(beta e^gamma) K,
+//       P = tril(Q K^T * e^{gamma_r - gamma_s})
+//   5. scan               one CTA per (sequence, value head, d_v tile),
+//                         sequential over chunks, state in shared memory:
 //       W = U - Wk S^T
-//       O = diag(e^gamma) Q S^T + tril(Q K^T * e^{gamma_r - gamma_s}) W
+//       O = diag(e^gamma) Q S^T + P W
 //       S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
-//     Only e^{x} with x <= 0 is ever formed.
+//     Only e^{x} with x <= 0 is ever formed.  The products run as register
+//     blocks of 4 x 4 to 8 x 4 per thread on shared-memory operands.
 #include <type_traits>
 
 #include "gdn_common.cuh"
 
 namespace gdn {
 
-__global__ void check_cu_seqlens_kernel(const int32_t* __restrict__ cu, int num_seqs,
-                                        int64_t total, int32_t* flag, int32_t* d_status) {
+// Also, when chunk_off is given and cu_seqlens is valid, the first global
+// chunk of each sequence: chunk_off[b] = sum_{b' < b} ceil(len_b' / chunk),
+// chunk_off[num_seqs] = the number of chunks.
+__global__ void __launch_bounds__(256) check_cu_seqlens_kernel(const int32_t* __restrict__ cu,
+                                                               int num_seqs, int64_t total,
+                                                               int chunk, int32_t* chunk_off,
+                                                               int32_t* flag, int32_t* d_status) {
   __shared__ int bad;
+  __shared__ int part[256];
   if (threadIdx.x == 0) bad = (cu[0] != 0) || ((int64_t)cu[num_seqs] != total);
   __syncthreads();
   for (int i = threadIdx.x; i < num_seqs; i += blockDim.x)
     if (cu[i + 1] < cu[i]) bad = 1;
   __syncthreads();
+  if (chunk_off && !bad) {   // bad is the same for every thread here
+    const int per = (num_seqs + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int b0 = min(num_seqs, (int)threadIdx.x * per), b1 = min(num_seqs, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += (int)(((int64_t)cu[b + 1] - cu[b] + chunk - 1) / chunk);
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int i = 0; i < (int)blockDim.x; ++i) {
+        const int v = part[i];
+        part[i] = run;
+        run += v;
+      }
+      chunk_off[num_seqs] = run;
+    }
+    __syncthreads();
+    int run = part[threadIdx.x];
+    for (int b = b0; b < b1; ++b) {
+      chunk_off[b] = run;
+      run += (int)(((int64_t)cu[b + 1] - cu[b] + chunk - 1) / chunk);
+    }
+  }
   if (threadIdx.x == 0) {
     flag[0] = bad ? 0 : 1;
     if (bad) set_status(d_status, GDN_DEV_BAD_CU_SEQLENS);
@@ -57,6 +90,23 @@ __device__ __forceinline__ int seq_of_token(const int32_t* __restrict__ cu, int 
   return lo;
 }
 
+// Eight consecutive values of the I/O type as floats (16-byte aligned source).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(256) frontend_kernel(const GdnPrefillArgs args) {
   extern __shared__ float s_y[];  // [conv_dim]
@@ -71,19 +121,30 @@ __global__ void __launch_bounds__(256) frontend_kernel(const GdnPrefillArgs args
   const IO* __restrict__ x = reinterpret_cast<const IO*>(args.x);
   const IO* __restrict__ win = reinterpret_cast<const IO*>(args.conv_pool) + (size_t)slot * 3 * cd;
 
-  for (int c = threadIdx.x; c < cd; c += blockDim.x) {
-    const float4 w = *reinterpret_cast<const float4*>(args.conv_weight + 4 * (size_t)c);
-    const float wt[4] = {w.x, w.y, w.z, w.w};
-    float z = 0.f;
+  // eight channels per thread, 16-byte loads (conv_dim is a multiple of 16)
+  for (int c = 8 * threadIdx.x; c < cd; c += 8 * blockDim.x) {
+    float xv[4][8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int64_t tau = p - 3 + k;  // position of this tap's input
-      float xv;
-      if (tau >= 0) xv = ld_io(x + (size_t)(tok - 3 + k) * cd + c);
-      else xv = init ? ld_io(win + (size_t)(3 + tau) * cd + c) : 0.f;
-      z = fmaf(wt[k], xv, z);
+      if (tau >= 0) load8(x + (size_t)(tok - 3 + k) * cd + c, xv[k]);
+      else if (init) load8(win + (size_t)(3 + tau) * cd + c, xv[k]);
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[k][e] = 0.f;
     }
-    s_y[c] = silu(z);
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 w = *reinterpret_cast<const float4*>(args.conv_weight + 4 * (size_t)(c + e));
+      float z = w.x * xv[0][e];   // taps oldest first
+      z = fmaf(w.y, xv[1][e], z);
+      z = fmaf(w.z, xv[2][e], z);
+      z = fmaf(w.w, xv[3][e], z);
+      y[e] = silu(z);
+    }
+    *reinterpret_cast<float4*>(s_y + c) = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4*>(s_y + c + 4) = make_float4(y[4], y[5], y[6], y[7]);
   }
   __syncthreads();
 
@@ -156,33 +217,279 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
   for (int r = 0; r < 3; ++r) win[(size_t)r * cd + c] = vals[r];
 }
 
-struct ScanSmem {
-  // offsets in floats; K and Q rows are padded to d_k + 1 floats, so that the
-  // lanes of a warp reading one column of K for different tokens (K K^T, Q K^T)
-  // hit different banks
-  int H, K, Q, V, U, Wk, A, T, gam, beta, be, dl, eg, n;
-  __host__ __device__ ScanSmem(int C, int DK, int DVT) {
+// ---- register-tiled products on shared-memory operands -----------------------
+// Each thread accumulates an RM x RN block: acc[m][n] += sum_k a(m, k) b(k, n).
+// "rows" operands are read one float per row (row stride padded so that the
+// rows a warp reads sit in different banks); "cols" operands four floats at a
+// time from 16-byte aligned rows; sc, when given, scales b's row k.
+
+// a(m, k) = A[(r0 + m st) * lda + k], b(k, n) = B[(c0 + n st) * ldb + k] (both
+// by rows, rows st apart: the lanes of a warp then read consecutive rows)
+template <int RM, int RN>
+__device__ __forceinline__ void tile_rows_rows(float (&acc)[RM][RN], const float* A, int lda,
+                                               int r0, const float* B, int ldb, int c0, int st,
+                                               int K) {
+  for (int k = 0; k < K; ++k) {
+    float a[RM], b[RN];
+#pragma unroll
+    for (int m = 0; m < RM; ++m) a[m] = A[(r0 + m * st) * lda + k];
+#pragma unroll
+    for (int n = 0; n < RN; ++n) b[n] = B[(c0 + n * st) * ldb + k];
+#pragma unroll
+    for (int m = 0; m < RM; ++m)
+#pragma unroll
+      for (int n = 0; n < RN; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+  }
+}
+
+// a(m, k) = A[(r0 + m) * lda + k] (by rows), b(k, n) = sc[k] B[k * ldb + c0 + n] (by columns)
+template <int RM, int RN>
+__device__ __forceinline__ void tile_rows_cols(float (&acc)[RM][RN], const float* A, int lda,
+                                               int r0, const float* B, int ldb, int c0, int k0,
+                                               int k1, const float* sc) {
+  static_assert(RN % 4 == 0, "four columns per load");
+  for (int k = k0; k < k1; ++k) {
+    float a[RM], b[RN];
+#pragma unroll
+    for (int m = 0; m < RM; ++m) a[m] = A[(r0 + m) * lda + k];
+    const float s = sc ? sc[k] : 1.0f;
+#pragma unroll
+    for (int n = 0; n < RN; n += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(B + k * ldb + c0 + n);
+      b[n] = v.x * s; b[n + 1] = v.y * s; b[n + 2] = v.z * s; b[n + 3] = v.w * s;
+    }
+#pragma unroll
+    for (int m = 0; m < RM; ++m)
+#pragma unroll
+      for (int n = 0; n < RN; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+  }
+}
+
+// a(m, k) = A[k * lda + r0 + m], b(k, n) = sc[k] B[k * ldb + c0 + n] (both by columns)
+template <int RM, int RN>
+__device__ __forceinline__ void tile_cols_cols(float (&acc)[RM][RN], const float* A, int lda,
+                                               int r0, const float* B, int ldb, int c0, int K,
+                                               const float* sc) {
+  static_assert(RM % 4 == 0 && RN % 4 == 0, "four rows and columns per load");
+  for (int k = 0; k < K; ++k) {
+    float a[RM], b[RN];
+#pragma unroll
+    for (int m = 0; m < RM; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(A + k * lda + r0 + m);
+      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+    }
+    const float s = sc[k];
+#pragma unroll
+    for (int n = 0; n < RN; n += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(B + k * ldb + c0 + n);
+      b[n] = v.x * s; b[n + 1] = v.y * s; b[n + 2] = v.z * s; b[n + 3] = v.w * s;
+    }
+#pragma unroll
+    for (int m = 0; m < RM; ++m)
+#pragma unroll
+      for (int n = 0; n < RN; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+  }
+}
+
+// Rows r < L of a [C][cols] block from a token-major workspace array (row r is
+// token tok0 + r, `stride` floats apart) into shared rows `ld` floats apart;
+// rows L..C-1 zero.  cols is a multiple of 4.  Issued as 16-byte cp.async
+// copies (zero-filled past L), so all of a block is in flight at once; the
+// caller waits with cp_async_wait_all() and a barrier.
+__device__ __forceinline__ void load_rows(float* dst, int ld, const float* src, size_t stride,
+                                          int C, int L, int cols) {
+  const int c4 = cols / 4;
+  for (int e = threadIdx.x; e < C * c4; e += blockDim.x) {
+    const int r = e / c4, q = e % c4;
+    const float* g = r < L ? src + (size_t)r * stride + 4 * q : src;   // src: not read when r >= L
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst + r * ld + 4 * q);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(g),
+                 "r"(r < L ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// ---- the chunk-local WY factors: one CTA per (chunk, value head) ---------------
+// Shared-memory layout (floats): K [C][DK+4] | Q, then V [C][max(DK+4, DV)] |
+// A [C][C+4] | T [C][C+4] | gamma [C] | beta [C] | beta e^gamma [C].
+struct ChunkSmem {
+  int K, QV, A, T, gam, beta, be, n;
+  __host__ __device__ ChunkSmem(int C, int DK, int DV) {
+    const int qv = (DK + 4) > DV ? DK + 4 : DV;
     int o = 0;
-    H = o; o += DK * DVT;
-    K = o; o += C * (DK + 1);
-    Q = o; o += C * (DK + 1);
-    V = o; o += C * DVT;
-    U = o; o += C * DVT;
-    Wk = o; o += C * DK;
-    A = o; o += C * C;
-    T = o; o += C * C;
+    K = o; o += C * (DK + 4);
+    QV = o; o += C * qv;
+    A = o; o += C * (C + 4);
+    T = o; o += C * (C + 4);
     gam = o; o += C;
     beta = o; o += C;
-    be = o; o += C;   // beta_s e^{gamma_s}
-    dl = o; o += C;   // e^{gamma_last - gamma_r}
-    eg = o; o += C;   // e^{gamma_r}
+    be = o; o += C;
     n = o;
   }
 };
 
+// Chunk x of the whole batch (chunk_off[b] <= x < chunk_off[b+1]) and value head
+// h: with gamma the cumulative log-decay inside the chunk,
+//   A = strict_tril(diag(beta) K K^T * e^{gamma_r - gamma_s}),  T = (I + A)^-1,
+//   U = T diag(beta) V,  Wk = T diag(beta e^gamma) K,
+//   P = tril(Q K^T * e^{gamma_r - gamma_s})
+// written by token rows to ws_u, ws_wk, ws_p, with gamma to ws_gam.
+__global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs args) {
+  extern __shared__ __align__(16) float sm[];
+  if (!args.ws_flag[0]) return;
+  const int x = blockIdx.x, h = blockIdx.y;
+  const int B = args.num_seqs;
+  if (x >= args.chunk_off[B]) return;
+  int lo = 0, hi = B - 1;   // the largest b with chunk_off[b] <= x (skips empty sequences)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (args.chunk_off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int slot = args.slot_idx[b];
+  if (slot < 0 || slot >= args.num_slots) return;   // status set by the scan
+  const int C = args.chunk, DK = args.d_k, DV = args.d_v;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int64_t start = args.cu_seqlens[b];
+  const int64_t Tlen = args.cu_seqlens[b + 1] - start;
+  const int64_t c0 = (int64_t)(x - args.chunk_off[b]) * C;
+  const int L = (Tlen - c0) < (int64_t)C ? (int)(Tlen - c0) : C;
+  const int hk = h / (args.h_v / args.h_k);
+  const int64_t tok0 = start + c0;
+
+  const ChunkSmem S(C, DK, DV);
+  const int KS = DK + 4, CS = C + 4, QS = (DK + 4) > DV ? DK + 4 : DV;
+  float* sK = sm + S.K;
+  float* sQV = sm + S.QV;
+  float* sA = sm + S.A;
+  float* sT = sm + S.T;
+  float* sG = sm + S.gam;
+  float* sB = sm + S.beta;
+  float* sBe = sm + S.be;
+
+  load_rows(sK, KS, args.ws_k + ((size_t)tok0 * args.h_k + hk) * DK, (size_t)args.h_k * DK, C, L, DK);
+  load_rows(sQV, QS, args.ws_q + ((size_t)tok0 * args.h_k + hk) * DK, (size_t)args.h_k * DK, C, L, DK);
+  if (tid < 32) {
+    // cumulative log-decay over the chunk: a warp-wide scan per 32 rows
+    float carry = 0.f;
+    for (int r0 = 0; r0 < C; r0 += 32) {
+      const int r = r0 + tid;
+      float g = r < L ? args.ws_g[(size_t)(tok0 + r) * args.h_v + h] : 0.f;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, g, off);
+        if (tid >= off) g += o;
+      }
+      g += carry;
+      if (r < C) {
+        sG[r] = g;
+        sB[r] = r < L ? args.ws_beta[(size_t)(tok0 + r) * args.h_v + h] : 0.f;
+      }
+      carry = __shfl_sync(0xffffffffu, g, 31);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int r = tid; r < C; r += NT) sBe[r] = sB[r] * expf(sG[r]);
+  // A into shared memory, P straight to the workspace (rows r < L); a thread
+  // takes rows ti + m C/4 and columns tj + n C/4
+  const int nb = C / 4;
+  for (int tile = tid; tile < nb * nb; tile += NT) {
+    const int ti = tile / nb, tj = tile % nb;
+    float a[4][4] = {}, p[4][4] = {};
+    tile_rows_rows<4, 4>(a, sK, KS, ti, sK, KS, tj, nb, DK);
+    tile_rows_rows<4, 4>(p, sQV, QS, ti, sK, KS, tj, nb, DK);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int r = ti + m * nb;
+      float* prow = args.ws_p + ((size_t)(tok0 + r) * args.h_v + h) * C;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int s = tj + n * nb;
+        const float dec = s <= r ? expf(sG[r] - sG[s]) : 0.f;   // exponent <= 0
+        sA[r * CS + s] = s < r ? sB[r] * a[m][n] * dec : 0.f;
+        if (r < L) prow[s] = p[m][n] * dec;
+      }
+    }
+  }
+  __syncthreads();
+  // V over Q (Q is no longer read), in flight during the inverse
+  load_rows(sQV, QS, args.ws_v + ((size_t)tok0 * args.h_v + h) * DV, (size_t)args.h_v * DV, C, L, DV);
+  // T = (I + A)^-1 by forward substitution down each column j: T[r][j] =
+  // delta_rj - sum_{s<r} A[r][s] T[s][j].  TPC = NT / C threads share a column
+  // (adjacent lanes); thread q of the group owns the rows s = q mod TPC, sums
+  // its part of each row's series and the group adds the parts with shuffles.
+  // Each T[s][j] is written and read only by its owner.
+  {
+    const int TPC = NT / C;   // 4, 8 or 16 (NT = 256, C = 64, 32, 16)
+    const int j = tid / TPC, q = tid % TPC;
+    for (int r = 0; r < C; ++r) {
+      float part = 0.f;
+      for (int s2 = q; s2 < r; s2 += TPC) part = fmaf(sA[r * CS + s2], sT[s2 * CS + j], part);
+      for (int m = TPC >> 1; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
+      if (r % TPC == q) sT[r * CS + j] = r < j ? 0.f : (r == j ? 1.f : -part);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // U = T diag(beta) V and Wk = T diag(beta e^gamma) K, 4 x 8 blocks (the U
+  // blocks first, then the Wk ones; consecutive blocks share their rows, so a
+  // warp reads at most two rows of T at a time); T is lower triangular, so row
+  // block r0 needs k < r0 + 4 only
+  const int nv = DV / 8, nk = DK / 8;
+  for (int tile = tid; tile < nb * (nv + nk); tile += NT) {
+    const bool is_u = tile < nb * nv;
+    const int t2 = is_u ? tile : tile - nb * nv;
+    const int ncb = is_u ? nv : nk;
+    const int r0 = (t2 / ncb) * 4;
+    const int c0c = (t2 % ncb) * 8;
+    float acc[4][8] = {};
+    if (is_u) tile_rows_cols<4, 8>(acc, sT, CS, r0, sQV, QS, c0c, 0, r0 + 4, sB);
+    else tile_rows_cols<4, 8>(acc, sT, CS, r0, sK, KS, c0c, 0, r0 + 4, sBe);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int r = r0 + m;
+      if (r >= L) continue;
+      float* dst = is_u ? args.ws_u + ((size_t)(tok0 + r) * args.h_v + h) * DV + c0c
+                        : args.ws_wk + ((size_t)(tok0 + r) * args.h_v + h) * DK + c0c;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+    }
+  }
+  for (int r = tid; r < L; r += NT) args.ws_gam[(size_t)(tok0 + r) * args.h_v + h] = sG[r];
+}
+
+// ---- the scan: one CTA per (sequence, value head, d_v tile) --------------------
+// Shared-memory layout (floats): S^T [DK][DVT] | Wk [C][DK+4] | Q [C][DK+4] |
+// K [C][DK+4] | P [C][C+4] | U, then W [C][DVT] | e^gamma [C] | e^{gamma_last - gamma} [C].
+struct ScanSmem {
+  int H, Wk, Q, K, P, W, eg, dl, n;
+  __host__ __device__ ScanSmem(int C, int DK, int DVT) {
+    int o = 0;
+    H = o; o += DK * DVT;
+    Wk = o; o += C * (DK + 4);
+    Q = o; o += C * (DK + 4);
+    K = o; o += C * (DK + 4);
+    P = o; o += C * (C + 4);
+    W = o; o += C * DVT;
+    eg = o; o += C;
+    dl = o; o += C;
+    n = o;
+  }
+};
+
+// Per chunk, with the chunk's Wk, U, P and gamma from chunk_simt_kernel:
+//   W = U - Wk S^T
+//   O = diag(e^gamma) Q S^T + P W
+//   S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
+// The state tile S^T [DK][DVT] stays in shared memory for the whole sequence.
 template <typename IO>
 __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs args, int DVT) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   if (!args.ws_flag[0]) return;
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * DVT;
   const int tid = threadIdx.x, NT = blockDim.x;
@@ -193,21 +500,16 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
       set_status(args.d_status, GDN_DEV_BAD_SLOT);
     return;
   }
-  const ScanSmem L(C, DK, DVT);
-  float* sH = sm + L.H;    // [DK][DVT]   S^T tile
-  float* sK = sm + L.K;    // [C][DK + 1]
-  float* sQ = sm + L.Q;    // [C][DK + 1]
-  float* sV = sm + L.V;    // [C][DVT]
-  float* sU = sm + L.U;    // [C][DVT]    U, then W
-  float* sWk = sm + L.Wk;  // [C][DK]
-  float* sA = sm + L.A;    // [C][C]      A, then P
-  float* sT = sm + L.T;    // [C][C]
-  float* sG = sm + L.gam;  // [C]         cumulative log-decay
-  float* sB = sm + L.beta; // [C]
-  float* sBe = sm + L.be;  // [C]
-  float* sDl = sm + L.dl;  // [C]
-  float* sEg = sm + L.eg;  // [C]
-  const int KS = DK + 1;   // row stride of sK, sQ
+  const ScanSmem S(C, DK, DVT);
+  const int KS = DK + 4, CS = C + 4;
+  float* sH = sm + S.H;     // [DK][DVT]   S^T tile
+  float* sWk = sm + S.Wk;   // [C][KS]
+  float* sQ = sm + S.Q;     // [C][KS]
+  float* sK = sm + S.K;     // [C][KS]
+  float* sP = sm + S.P;     // [C][CS]
+  float* sW = sm + S.W;     // [C][DVT]    U, then W
+  float* sEg = sm + S.eg;   // [C]
+  float* sDl = sm + S.dl;   // [C]
 
   const int hk = h / (args.h_v / args.h_k);
   const int64_t start = args.cu_seqlens[b];
@@ -219,122 +521,100 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     sH[e] = init ? gstate[(size_t)i * DV + j0 + j] : 0.f;
   }
   IO* out = reinterpret_cast<IO*>(args.o);
+  const int nr = C / 4, nc = DVT / 4;   // 4 x 4 blocks of the [C][DVT] products
+  const int ni = DK / 8;                // 8 x 4 blocks of the [DK][DVT] state update
 
+  // Wk, Q and P of a chunk are fetched while the previous chunk still runs,
+  // as soon as it has finished reading them; K and U at the chunk's start.
+  auto len_at = [&](int64_t cc) { return (Tlen - cc) < (int64_t)C ? (int)(Tlen - cc) : C; };
+  auto fetch_wk = [&](int64_t cc) {
+    load_rows(sWk, KS, args.ws_wk + ((size_t)(start + cc) * args.h_v + h) * DK,
+              (size_t)args.h_v * DK, C, len_at(cc), DK);
+  };
+  auto fetch_qp = [&](int64_t cc) {
+    load_rows(sQ, KS, args.ws_q + ((size_t)(start + cc) * args.h_k + hk) * DK,
+              (size_t)args.h_k * DK, C, len_at(cc), DK);
+    load_rows(sP, CS, args.ws_p + ((size_t)(start + cc) * args.h_v + h) * C, (size_t)args.h_v * C,
+              C, len_at(cc), C);
+  };
+  if (Tlen > 0) {
+    fetch_wk(0);
+    fetch_qp(0);
+  }
   for (int64_t c0 = 0; c0 < Tlen; c0 += C) {
-    const int Lc = (Tlen - c0) < (int64_t)C ? (int)(Tlen - c0) : C;
-    __syncthreads();
-    for (int e = tid; e < C * DK; e += NT) {
-      const int r = e / DK, i = e % DK;
-      const size_t tk = (size_t)(start + c0 + r);
-      sK[r * KS + i] = r < Lc ? args.ws_k[(tk * args.h_k + hk) * DK + i] : 0.f;
-      sQ[r * KS + i] = r < Lc ? args.ws_q[(tk * args.h_k + hk) * DK + i] : 0.f;
-    }
-    for (int e = tid; e < C * DVT; e += NT) {
-      const int r = e / DVT, j = e % DVT;
-      const size_t tk = (size_t)(start + c0 + r);
-      sV[e] = r < Lc ? args.ws_v[(tk * args.h_v + h) * DV + j0 + j] : 0.f;
-    }
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int r = 0; r < C; ++r) {
-        const size_t tk = (size_t)(start + c0 + r);
-        acc += r < Lc ? args.ws_g[tk * args.h_v + h] : 0.f;
-        sG[r] = acc;
-        sB[r] = r < Lc ? args.ws_beta[tk * args.h_v + h] : 0.f;
-      }
-    }
-    __syncthreads();
+    const int L = len_at(c0);
+    const int64_t tok0 = start + c0;
+    const bool more = c0 + C < Tlen;
+    __syncthreads();   // the previous chunk's reads of K, W and S^T are done
+    load_rows(sK, KS, args.ws_k + ((size_t)tok0 * args.h_k + hk) * DK, (size_t)args.h_k * DK, C, L, DK);
+    load_rows(sW, DVT, args.ws_u + ((size_t)tok0 * args.h_v + h) * DV + j0, (size_t)args.h_v * DV, C, L, DVT);
+    const float glast = args.ws_gam[(size_t)(tok0 + L - 1) * args.h_v + h];
     for (int r = tid; r < C; r += NT) {
-      sBe[r] = sB[r] * expf(sG[r]);
-      sDl[r] = expf(sG[C - 1] - sG[r]);
-      sEg[r] = expf(sG[r]);
+      const float g = r < L ? args.ws_gam[(size_t)(tok0 + r) * args.h_v + h] : 0.f;
+      sEg[r] = r < L ? expf(g) : 0.f;
+      sDl[r] = r < L ? expf(glast - g) : 0.f;   // exponent <= 0
     }
-    // A (strictly lower), P (lower incl. diagonal) need K K^T and Q K^T
-    for (int e = tid; e < C * C; e += NT) {
-      const int r = e / C, s = e % C;
-      float a = 0.f;
-      if (s < r) {
-        float dot = 0.f;
-        for (int i = 0; i < DK; ++i) dot = fmaf(sK[r * KS + i], sK[s * KS + i], dot);
-        a = sB[r] * dot * expf(sG[r] - sG[s]);
-      }
-      sA[e] = a;
-    }
+    cp_async_wait_all();
     __syncthreads();
-    // T = (I + A)^-1 by forward substitution down each column j: T[r][j] =
-    // delta_rj - sum_{s<r} A[r][s] T[s][j].  TPC = NT / C threads share a column
-    // (adjacent lanes); thread q of the group owns the rows s = q mod TPC,
-    // sums its part of each row's series and the group adds the parts with
-    // shuffles.  Each T[s][j] is written and read only by its owner.
-    {
-      const int TPC = NT / C;              // 4, 8 or 16 (NT = 256, C = 64, 32, 16)
-      const int j = tid / TPC, q = tid % TPC;
-      for (int r = 0; r < C; ++r) {
-        float part = 0.f;
-        for (int s2 = q; s2 < r; s2 += TPC) part = fmaf(sA[r * C + s2], sT[s2 * C + j], part);
-        for (int m = TPC >> 1; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-        if (r % TPC == q) sT[r * C + j] = r < j ? 0.f : (r == j ? 1.f : -part);
+    // W = U - Wk S^T (each block read and written by its own thread)
+    for (int tile = tid; tile < nr * nc; tile += NT) {
+      const int r0 = (tile / nc) * 4, cc = (tile % nc) * 4;
+      float acc[4][4] = {};
+      tile_rows_cols<4, 4>(acc, sWk, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float4* w = reinterpret_cast<float4*>(sW + (r0 + m) * DVT + cc);
+        const float4 u = *w;
+        *w = make_float4(u.x - acc[m][0], u.y - acc[m][1], u.z - acc[m][2], u.w - acc[m][3]);
       }
     }
     __syncthreads();
-    // U = T diag(beta) V ; Wk = T diag(beta e^gamma) K ; P -> sA
-    for (int e = tid; e < C * DVT; e += NT) {
-      const int r = e / DVT, j = e % DVT;
-      float acc = 0.f;
-      for (int s = 0; s <= r; ++s) acc = fmaf(sT[r * C + s] * sB[s], sV[s * DVT + j], acc);
-      sU[e] = acc;
-    }
-    for (int e = tid; e < C * DK; e += NT) {
-      const int r = e / DK, i = e % DK;
-      float acc = 0.f;
-      for (int s = 0; s <= r; ++s) acc = fmaf(sT[r * C + s] * sBe[s], sK[s * KS + i], acc);
-      sWk[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < C * C; e += NT) {
-      const int r = e / C, s = e % C;
-      float p = 0.f;
-      if (s <= r) {
-        float dot = 0.f;
-        for (int i = 0; i < DK; ++i) dot = fmaf(sQ[r * KS + i], sK[s * KS + i], dot);
-        p = dot * expf(sG[r] - sG[s]);
+    if (more) fetch_wk(c0 + C);   // Wk is not read again in this chunk
+    // O = diag(e^gamma) Q S^T + P W; P is lower triangular, so row block r0
+    // needs W rows < r0 + 4 only
+    for (int tile = tid; tile < nr * nc; tile += NT) {
+      const int r0 = (tile / nc) * 4, cc = (tile % nc) * 4;
+      float acc[4][4] = {};
+      tile_rows_cols<4, 4>(acc, sQ, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] *= sEg[r0 + m];
+      tile_rows_cols<4, 4>(acc, sP, CS, r0, sW, DVT, cc, 0, r0 + 4, nullptr);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int r = r0 + m;
+        if (r >= L) continue;
+        IO* orow = out + ((size_t)(tok0 + r) * args.h_v + h) * DV + j0 + cc;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) st_io(orow + n, acc[m][n]);
       }
-      sA[e] = p;
-    }
-    // W = U - Wk S^T  (in place in sU; each element read and written by one thread)
-    for (int e = tid; e < C * DVT; e += NT) {
-      const int r = e / DVT, j = e % DVT;
-      float acc = 0.f;
-      for (int i = 0; i < DK; ++i) acc = fmaf(sWk[r * DK + i], sH[i * DVT + j], acc);
-      sU[e] -= acc;
     }
     __syncthreads();
-    // O = diag(e^gamma) Q S^T + P W
-    for (int e = tid; e < Lc * DVT; e += NT) {
-      const int r = e / DVT, j = e % DVT;
-      float qs = 0.f;
-      for (int i = 0; i < DK; ++i) qs = fmaf(sQ[r * KS + i], sH[i * DVT + j], qs);
-      float pw = 0.f;
-      for (int s = 0; s <= r; ++s) pw = fmaf(sA[r * C + s], sU[s * DVT + j], pw);
-      const float ov = fmaf(sEg[r], qs, pw);
-      st_io(out + ((size_t)(start + c0 + r) * args.h_v + h) * DV + j0 + j, ov);
-    }
-    __syncthreads();
-    // S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
-    const float glast = sG[C - 1];
+    if (more) fetch_qp(c0 + C);   // nor are Q and P
+    // S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W, 8 x 4
+    // blocks (rows of K beyond the chunk's end are zero, their weight too)
     const float dlast = expf(glast);
     // interval checkpoint: the state after these c0 / C + 1 chunks, each thread
     // storing the elements it just updated
     const int64_t cs = args.ckpt_every_chunks > 0 ? ckpt_slot_of(args, b, c0 / C + 1, Tlen) : -1;
     float* cst = cs >= 0 ? args.state_pool + ((size_t)cs * args.h_v + h) * (size_t)DK * DV : nullptr;
-    for (int e = tid; e < DK * DVT; e += NT) {
-      const int i = e / DVT, j = e % DVT;
-      float acc = 0.f;
-      for (int r = 0; r < Lc; ++r) acc = fmaf(sK[r * KS + i] * sDl[r], sU[r * DVT + j], acc);
-      sH[e] = fmaf(dlast, sH[e], acc);
-      if (cst) cst[(size_t)i * DV + j0 + j] = sH[e];
+    for (int tile = tid; tile < ni * nc; tile += NT) {
+      const int i0 = (tile / nc) * 8, cc = (tile % nc) * 4;
+      float acc[8][4] = {};
+      tile_cols_cols<8, 4>(acc, sK, KS, i0, sW, DVT, cc, L, sDl);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float4* hp = reinterpret_cast<float4*>(sH + (i0 + m) * DVT + cc);
+        const float4 o = *hp;
+        const float4 nv = make_float4(fmaf(dlast, o.x, acc[m][0]), fmaf(dlast, o.y, acc[m][1]),
+                                      fmaf(dlast, o.z, acc[m][2]), fmaf(dlast, o.w, acc[m][3]));
+        *hp = nv;
+        if (cst) *reinterpret_cast<float4*>(cst + (size_t)(i0 + m) * DV + j0 + cc) = nv;
+      }
     }
   }
+  cp_async_wait_all();   // nothing in flight (the last chunk fetched nothing ahead)
   __syncthreads();
   for (int e = tid; e < DK * DVT; e += NT) {
     const int i = e / DVT, j = e % DVT;
@@ -348,8 +628,8 @@ template <typename IO>
 static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
   cudaError_t e = gdn_trace_mark(tr, 0, true, s);
   if (e != cudaSuccess) return e;
-  check_cu_seqlens_kernel<<<1, 256, 0, s>>>(a.cu_seqlens, a.num_seqs, a.total_tokens,
-                                            a.ws_flag, a.d_status);
+  check_cu_seqlens_kernel<<<1, 256, 0, s>>>(a.cu_seqlens, a.num_seqs, a.total_tokens, a.chunk,
+                                            a.chunk_off, a.ws_flag, a.d_status);
   gdn_trace_count(tr, 1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -368,6 +648,19 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
   e = gdn_launch_window(a, std::is_same<IO, float>::value ? GDN_FP32 : GDN_BF16, s, tr);
   if (e != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 0, false, s)) != cudaSuccess) return e;
+  if (a.total_tokens > 0) {
+    if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
+    const size_t csmem = (size_t)ChunkSmem(a.chunk, a.d_k, a.d_v).n * sizeof(float);
+    e = cudaFuncSetAttribute(chunk_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)csmem);
+    if (e != cudaSuccess) return e;
+    dim3 cgrid((unsigned)a.max_chunks, a.h_v);
+    chunk_simt_kernel<<<cgrid, 256, csmem, s>>>(a);
+    gdn_trace_count(tr, 1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
+  }
   const int DVT = scan_dv_tile(a.d_v);
   const ScanSmem L(a.chunk, a.d_k, DVT);
   const size_t smem = (size_t)L.n * sizeof(float);
@@ -387,7 +680,7 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
 
 cudaError_t gdn_launch_check(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
   gdn::check_cu_seqlens_kernel<<<1, 256, 0, s>>>(a.cu_seqlens, a.num_seqs, a.total_tokens,
-                                                 a.ws_flag, a.d_status);
+                                                 a.chunk, nullptr, a.ws_flag, a.d_status);
   gdn_trace_count(tr, 1);
   return cudaGetLastError();
 }
@@ -412,7 +705,9 @@ cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, g
 }
 
 size_t gdn_simt_scan_smem_bytes(int chunk, int d_k, int d_v) {
-  return (size_t)gdn::ScanSmem(chunk, d_k, gdn::scan_dv_tile(d_v)).n * sizeof(float);
+  const size_t scan = (size_t)gdn::ScanSmem(chunk, d_k, gdn::scan_dv_tile(d_v)).n * sizeof(float);
+  const size_t chk = (size_t)gdn::ChunkSmem(chunk, d_k, d_v).n * sizeof(float);
+  return scan > chk ? scan : chk;
 }
 
 cudaError_t gdn_launch_prefill_simt(const GdnPrefillArgs& a, int io, cudaStream_t s,
