@@ -287,40 +287,62 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
 
 
 def bench_e2e(torch, gdn, run, steps, warmup):
-    """Host (pinned) inputs -> H2D -> gdn_prefill -> D2H of the output, all
-    inside the timed region, on one stream."""
+    """Host (pinned) inputs -> H2D -> gdn_prefill -> D2H of the output, every
+    step inside the timed region, pipelined the way a serving loop runs it:
+    two device buffer sets, the uploads on one stream, the layer on another,
+    the downloads on a third, so that step i's compute overlaps step i+1's
+    upload and step i-1's download.  Steps are ordered through the buffers'
+    events only; the layer calls themselves run one after another."""
     inp = run.inp
     io = run.io
     pin = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(dtype=dt).pin_memory()  # noqa: E731
-    hx, ha, hb = pin(inp["x"], io), pin(inp["a"], io), pin(inp["b"], io)
-    hcu = pin(inp["cu_seqlens"].astype(np.int32))
-    hslot = pin(inp["slot_idx"].astype(np.int32))
-    hinit = pin(inp["has_init"].astype(np.uint8))
-    ho = torch.empty(run.o.shape, dtype=io).pin_memory()
+    host_in = (pin(inp["x"], io), pin(inp["a"], io), pin(inp["b"], io),
+               pin(inp["cu_seqlens"].astype(np.int32)), pin(inp["slot_idx"].astype(np.int32)),
+               pin(inp["has_init"].astype(np.uint8)))
     dev = run.x.device
-    dx, da, db = (torch.empty_like(t, device=dev) for t in (hx, ha, hb))
-    dcu, dslot, dinit = (torch.empty_like(t, device=dev) for t in (hcu, hslot, hinit))
-    stream = torch.cuda.current_stream()
-    h2d = sum(t.numel() * t.element_size() for t in (hx, ha, hb, hcu, hslot, hinit))
-    d2h = ho.numel() * ho.element_size()
+    nbuf = 2
+    dev_in = [tuple(torch.empty_like(t, device=dev) for t in host_in) for _ in range(nbuf)]
+    dev_out = [torch.empty(run.o.shape, dtype=io, device=dev) for _ in range(nbuf)]
+    host_out = [torch.empty(run.o.shape, dtype=io).pin_memory() for _ in range(nbuf)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # buffer k's inputs have landed
+    ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]   # the layer on buffer k is done
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]   # buffer k's output is on the host
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out[0].numel() * host_out[0].element_size()
 
-    def step():
-        for d_, h_ in ((dx, hx), (da, ha), (db, hb), (dcu, hcu), (dslot, hslot), (dinit, hinit)):
-            d_.copy_(h_, non_blocking=True)
-        run(x=dx, a=da, b=db, cu=dcu, slot=dslot, init=dinit)
-        ho.copy_(run.o, non_blocking=True)
+    def step(i):
+        k = i % nbuf
+        s_in.wait_event(ev_cmp[k])              # the layer that read buffer k is done
+        with torch.cuda.stream(s_in):
+            for d_, h_ in zip(dev_in[k], host_in):
+                d_.copy_(h_, non_blocking=True)
+        ev_in[k].record(s_in)
+        s_cmp.wait_event(ev_in[k])
+        s_cmp.wait_event(ev_out[k])             # buffer k's previous output has been read
+        with torch.cuda.stream(s_cmp):
+            dx, da, db, dcu, dslot, dinit = dev_in[k]
+            run(x=dx, a=da, b=db, cu=dcu, slot=dslot, init=dinit, o=dev_out[k])
+        ev_cmp[k].record(s_cmp)
+        s_out.wait_event(ev_cmp[k])
+        with torch.cuda.stream(s_out):
+            host_out[k].copy_(dev_out[k], non_blocking=True)
+        ev_out[k].record(s_out)
 
-    for _ in range(max(warmup, 1)):
-        step()
+    for i in range(max(warmup, 1)):
+        step(i)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        step()
-    e.record(stream)
+    s.record(s_in)
+    for i in range(steps):
+        step(i)
+    e.record(s_out)                             # after the last download
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+    # the last step's output arrived intact
+    np.testing.assert_array_equal(host_out[(steps - 1) % nbuf].float().numpy(),
+                                  dev_out[(steps - 1) % nbuf].float().cpu().numpy())
+    return {"ms": ms, "h2d": h2d, "d2h": d2h, "pipeline": f"{nbuf} buffer sets, 3 streams"}
 
 
 def bench_gated_norm(torch, gdn, dims, T, device, steps, warmup):
@@ -720,7 +742,8 @@ def run_gdn(args):
         if e2e:
             line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],
-                           "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+                           "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                           "pipeline": e2e["pipeline"]}
         if gn:
             ggbs = gn["bytes"] / (gn["ms"] / 1e3) / 1e9
             line["gated_norm"] = {

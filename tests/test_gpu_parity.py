@@ -3,6 +3,7 @@ oracle on identical seeded inputs, element by element, with the tolerances in
 tests/_gpu.py.  Sizes span several chunks with ragged tails; the Qwen3.5-4B
 prefill (T=4096) and the 24-layer x 64-slot decode step run at full size in
 the launch configuration the benchmark times."""
+import dataclasses
 import os
 import zlib
 
@@ -175,6 +176,21 @@ def test_prefill_then_prefill_then_decode_handoff(gpu_lib):
     assert_close(state[int(full["slot_idx"][0])].cpu().numpy(), ref["state"][0], d, "state")
     np.testing.assert_array_equal(conv[int(full["slot_idx"][0])].float().cpu().numpy(),
                                   ref["window"][0])
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES) + ["qwen35_4b_fp32_state"])
+def test_prefill_with_empty_sequences_between(gpu_lib, name):
+    """Empty sequences first, between and last: the chunk table of both
+    prefill paths must map every chunk to the non-empty sequence it belongs
+    to, and the empty sequences' slots get their initial state back."""
+    d = (dataclasses.replace(QWEN35_4B, flags=gdn.GDN_FP32_STATE) if name.endswith("fp32_state")
+         else SHAPES[name])
+    lengths = [0, 17, 0, 0, 64, 1, 0, 130, 0]
+    inp = workloads.layer_inputs(d, lengths, seed=zlib.crc32(name.encode()) % 10000, init="mixed",
+                                 num_slots=len(lengths) + 2)
+    run = PrefillRun(inp)
+    run()
+    check_prefill(inp, run.results(), oracle_prefill(inp, n_threads=NCPU))
 
 
 def test_device_status_bits(gpu_lib):
