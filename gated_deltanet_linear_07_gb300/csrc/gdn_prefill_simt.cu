@@ -487,7 +487,9 @@ struct ScanSmem {
 //   O = diag(e^gamma) Q S^T + P W
 //   S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
 // The state tile S^T [DK][DVT] stays in shared memory for the whole sequence.
-template <typename IO>
+// Register blocks: RMW x 4 for the [C][DVT] products, RMS x 4 for the state
+// update (smaller blocks for narrow tiles keep every thread busy).
+template <typename IO, int RMW, int RMS>
 __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs args, int DVT) {
   extern __shared__ __align__(16) float sm[];
   if (!args.ws_flag[0]) return;
@@ -521,8 +523,8 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     sH[e] = init ? gstate[(size_t)i * DV + j0 + j] : 0.f;
   }
   IO* out = reinterpret_cast<IO*>(args.o);
-  const int nr = C / 4, nc = DVT / 4;   // 4 x 4 blocks of the [C][DVT] products
-  const int ni = DK / 8;                // 8 x 4 blocks of the [DK][DVT] state update
+  const int nr = C / RMW, nc = DVT / 4;   // RMW x 4 blocks of the [C][DVT] products
+  const int ni = DK / RMS;                // RMS x 4 blocks of the [DK][DVT] state update
 
   // Wk, Q and P of a chunk are fetched while the previous chunk still runs,
   // as soon as it has finished reading them; K and U at the chunk's start.
@@ -558,11 +560,11 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     __syncthreads();
     // W = U - Wk S^T (each block read and written by its own thread)
     for (int tile = tid; tile < nr * nc; tile += NT) {
-      const int r0 = (tile / nc) * 4, cc = (tile % nc) * 4;
-      float acc[4][4] = {};
-      tile_rows_cols<4, 4>(acc, sWk, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+      const int r0 = (tile / nc) * RMW, cc = (tile % nc) * 4;
+      float acc[RMW][4] = {};
+      tile_rows_cols<RMW, 4>(acc, sWk, KS, r0, sH, DVT, cc, 0, DK, nullptr);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < RMW; ++m) {
         float4* w = reinterpret_cast<float4*>(sW + (r0 + m) * DVT + cc);
         const float4 u = *w;
         *w = make_float4(u.x - acc[m][0], u.y - acc[m][1], u.z - acc[m][2], u.w - acc[m][3]);
@@ -571,18 +573,18 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     __syncthreads();
     if (more) fetch_wk(c0 + C);   // Wk is not read again in this chunk
     // O = diag(e^gamma) Q S^T + P W; P is lower triangular, so row block r0
-    // needs W rows < r0 + 4 only
+    // needs W rows < r0 + RMW only
     for (int tile = tid; tile < nr * nc; tile += NT) {
-      const int r0 = (tile / nc) * 4, cc = (tile % nc) * 4;
-      float acc[4][4] = {};
-      tile_rows_cols<4, 4>(acc, sQ, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+      const int r0 = (tile / nc) * RMW, cc = (tile % nc) * 4;
+      float acc[RMW][4] = {};
+      tile_rows_cols<RMW, 4>(acc, sQ, KS, r0, sH, DVT, cc, 0, DK, nullptr);
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+      for (int m = 0; m < RMW; ++m)
 #pragma unroll
         for (int n = 0; n < 4; ++n) acc[m][n] *= sEg[r0 + m];
-      tile_rows_cols<4, 4>(acc, sP, CS, r0, sW, DVT, cc, 0, r0 + 4, nullptr);
+      tile_rows_cols<RMW, 4>(acc, sP, CS, r0, sW, DVT, cc, 0, r0 + RMW, nullptr);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < RMW; ++m) {
         const int r = r0 + m;
         if (r >= L) continue;
         IO* orow = out + ((size_t)(tok0 + r) * args.h_v + h) * DV + j0 + cc;
@@ -600,11 +602,11 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
     const int64_t cs = args.ckpt_every_chunks > 0 ? ckpt_slot_of(args, b, c0 / C + 1, Tlen) : -1;
     float* cst = cs >= 0 ? args.state_pool + ((size_t)cs * args.h_v + h) * (size_t)DK * DV : nullptr;
     for (int tile = tid; tile < ni * nc; tile += NT) {
-      const int i0 = (tile / nc) * 8, cc = (tile % nc) * 4;
-      float acc[8][4] = {};
-      tile_cols_cols<8, 4>(acc, sK, KS, i0, sW, DVT, cc, L, sDl);
+      const int i0 = (tile / nc) * RMS, cc = (tile % nc) * 4;
+      float acc[RMS][4] = {};
+      tile_cols_cols<RMS, 4>(acc, sK, KS, i0, sW, DVT, cc, L, sDl);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
+      for (int m = 0; m < RMS; ++m) {
         float4* hp = reinterpret_cast<float4*>(sH + (i0 + m) * DVT + cc);
         const float4 o = *hp;
         const float4 nv = make_float4(fmaf(dlast, o.x, acc[m][0]), fmaf(dlast, o.y, acc[m][1]),
@@ -622,7 +624,24 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
   }
 }
 
-static int scan_dv_tile(int d_v) { return d_v < 64 ? d_v : 64; }
+// d_v tile of the scan: 64 wide, or 32 when 64-wide tiles would leave SMs idle
+// (fewer (sequence, head, tile) CTAs than SMs); sms <= 0: the largest tile.
+static int scan_dv_tile(int d_v, int64_t seq_heads = 0, int sms = 0) {
+  if (d_v < 64) return d_v;
+  if (sms > 0 && seq_heads * (d_v / 64) < sms) return 32;
+  return 64;
+}
+
+static int num_sms() {
+  static int n = 0;   // the device's SM count, looked up once per process
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 0;
+  }
+  return n;
+}
 
 template <typename IO>
 static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
@@ -661,15 +680,16 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
     if (e != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
   }
-  const int DVT = scan_dv_tile(a.d_v);
+  const int DVT = scan_dv_tile(a.d_v, (int64_t)a.num_seqs * a.h_v, num_sms());
   const ScanSmem L(a.chunk, a.d_k, DVT);
   const size_t smem = (size_t)L.n * sizeof(float);
-  e = cudaFuncSetAttribute(scan_simt_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  // 32-wide tiles: 2 x 4 and 4 x 4 blocks, else 4 x 4 and 8 x 4
+  auto kern = DVT == 32 ? scan_simt_kernel<IO, 2, 4> : scan_simt_kernel<IO, 4, 8>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
   dim3 grid(a.num_seqs, a.h_v, a.d_v / DVT);
-  scan_simt_kernel<IO><<<grid, 256, smem, s>>>(a, DVT);
+  kern<<<grid, 256, smem, s>>>(a, DVT);
   gdn_trace_count(tr, 1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
