@@ -6,7 +6,9 @@ build step and the seeded synthetic workloads.  There is no CPU or Python
 fallback for any step of the layer.
 """
 from ._binding import (GDN_BF16, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_BAD_SLOT,  # noqa: F401
-                       GDN_DEV_WAIT_TIMEOUT, GDN_FP32, GDN_FP32_STATE, GdnError, conv_dim, dims_from,
+                       GDN_DEV_WAIT_TIMEOUT, GDN_FP32, GDN_FP32_STATE, GDN_CHECK_FINITE,
+                       GDN_DEV_NONFINITE_FRONTEND, GDN_DEV_NONFINITE_CHUNK, GDN_DEV_NONFINITE_OUT,
+                       GdnError, conv_dim, dims_from,
                        gdn_conv1d_update, gdn_decode_step, gdn_dims, gdn_gated_rmsnorm, gdn_params,
                        gdn_prefill_checkpointed, gdn_slot_copy, gdn_prefill_gated_norm,
                        gdn_decode_step_gated_norm,

@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "gdn_check.cuh"
 #include "gdn_common.cuh"
 
 #define GDN_EXPORT extern "C" __attribute__((visibility("default")))
@@ -29,7 +30,7 @@ int check_dims(const gdn_dims* d) {
   if (!d) return GDN_EINVAL;
   if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0) return GDN_EINVAL;
   if (!(d->l2_eps >= 0.0f)) return GDN_EINVAL;
-  if (d->flags & ~GDN_FP32_STATE) return GDN_EINVAL;
+  if (d->flags & ~(GDN_FP32_STATE | GDN_CHECK_FINITE)) return GDN_EINVAL;
   if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
   if (d->conv_w != 4) return GDN_EUNSUPPORTED;
   if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
@@ -151,6 +152,31 @@ GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total
   return prefill_layout(dims, total_tokens, num_seqs).total;
 }
 
+// GDN_CHECK_FINITE: scans of what each stage of the call wrote (gdn_check.cuh).
+static cudaError_t check_stages(const GdnPrefillArgs& p, const gdn_dims* d, bool tc,
+                                cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  auto rows = [&](const void* ptr, bool bf16, int64_t n, int bit) {
+    if (e == cudaSuccess) e = gdn_check_rows(p, ptr, bf16, n, bit, s);
+  };
+  if (tc) {
+    e = gdn_check_tc_records(p, s);
+  } else {
+    rows(p.ws_q, false, (int64_t)d->h_k * d->d_k, GDN_DEV_NONFINITE_FRONTEND);
+    rows(p.ws_k, false, (int64_t)d->h_k * d->d_k, GDN_DEV_NONFINITE_FRONTEND);
+    rows(p.ws_v, false, (int64_t)d->h_v * d->d_v, GDN_DEV_NONFINITE_FRONTEND);
+    rows(p.ws_g, false, d->h_v, GDN_DEV_NONFINITE_FRONTEND);
+    rows(p.ws_beta, false, d->h_v, GDN_DEV_NONFINITE_FRONTEND);
+    rows(p.ws_u, false, (int64_t)d->h_v * d->d_v, GDN_DEV_NONFINITE_CHUNK);
+    rows(p.ws_wk, false, (int64_t)d->h_v * d->d_k, GDN_DEV_NONFINITE_CHUNK);
+    rows(p.ws_p, false, (int64_t)d->h_v * d->chunk, GDN_DEV_NONFINITE_CHUNK);
+    rows(p.ws_gam, false, d->h_v, GDN_DEV_NONFINITE_CHUNK);
+  }
+  rows(p.o, d->io == GDN_BF16, (int64_t)d->h_v * d->d_v, GDN_DEV_NONFINITE_OUT);
+  if (e == cudaSuccess) e = gdn_check_states(p, d->d_k, d->d_v, GDN_DEV_NONFINITE_OUT, s);
+  return e;
+}
+
 // The prefill behind every public variant; ckpt_every_chunks = 0 and
 // ckpt_slot = null: no interval checkpoints.
 static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const void* x,
@@ -168,6 +194,8 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   int rc = check_prefill_dims(dims);
   if (rc != GDN_OK) return rc;
   if (!params || num_seqs < 0 || total_tokens < 0 || num_slots < 0) return GDN_EINVAL;
+  const bool check_finite = (dims->flags & GDN_CHECK_FINITE) != 0;
+  if (check_finite && !d_status) return GDN_EINVAL;   // the probe reports through it
   if (total_tokens > INT32_MAX) return GDN_EUNSUPPORTED;
   if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_EINVAL;
   if (!params->conv_weight || !params->A_log || !params->dt_bias || !cu_seqlens || !slot_idx ||
@@ -224,6 +252,8 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   if (e == cudaSuccess && z && total_tokens > 0)
     e = gdn_launch_gated_rmsnorm(norm_weight, norm_eps, o, z, total_tokens * dims->h_v, dims->d_v,
                                  dims->io, o, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && check_finite)
+    e = check_stages(p, dims, use_tc(dims), reinterpret_cast<cudaStream_t>(stream));
   return cuda_rc(e);
 }
 

@@ -30,6 +30,7 @@
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets
 // GDN_DEV_WAIT_TIMEOUT, skips the dependent work and still frees its TMEM.
+#include "gdn_check.cuh"
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 
@@ -1254,6 +1255,56 @@ bool gdn_tc_prefill_supported(int h_k, int h_v, int d_k, int d_v, int chunk, int
 
 size_t gdn_tc_kq_bytes() { return gdn::tcp::Q_REC; }
 size_t gdn_tc_vh_bytes() { return gdn::tcp::VH_REC; }
+
+namespace gdn {
+namespace tcp {
+
+// GDN_CHECK_FINITE scan of the chunk records (gdn_check.cuh): block (gc, y)
+// takes chunk gc's [Q; K] record of key head y (y < h_k, the front end's
+// output) or the record of value head y - h_k (the chunk stage's output: P,
+// U^T, the 129 decay factors, Wk).
+__global__ void __launch_bounds__(256) check_records_kernel(const GdnPrefillArgs a) {
+  if (!a.ws_flag[0]) return;
+  const int gc = blockIdx.x, y = blockIdx.y;
+  const int B = a.num_seqs;
+  if (gc >= a.chunk_off[B]) return;
+  int lo = 0, hi = B - 1;   // the largest b with chunk_off[b] <= gc
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.chunk_off[mid] <= gc) lo = mid; else hi = mid - 1;
+  }
+  const int slot = a.slot_idx[lo];
+  if (slot < 0 || slot >= a.num_slots) return;
+  auto bf16_bad = [](const unsigned char* p, int n, int tid, int nt) {
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+    bool bad = false;
+    for (int e = tid; e < n; e += nt) bad |= (q[e] & 0x7f80u) == 0x7f80u;
+    return bad;
+  };
+  const int tid = threadIdx.x, nt = blockDim.x;
+  bool bad;
+  if (y < a.h_k) {
+    bad = bf16_bad(a.kq_ws + ((size_t)gc * a.h_k + y) * Q_REC, Q_REC / 2, tid, nt);
+  } else {
+    const unsigned char* rec = a.vh_ws + ((size_t)gc * a.h_v + (y - a.h_k)) * VH_REC;
+    bad = bf16_bad(rec + P_OFF, (UT_OFF - P_OFF) / 2, tid, nt) ||
+          bf16_bad(rec + UT_OFF, (EXP_OFF - UT_OFF) / 2, tid, nt) ||
+          bf16_bad(rec + WK_OFF, (VH_REC - WK_OFF) / 2, tid, nt);
+    const uint32_t* ex = reinterpret_cast<const uint32_t*>(rec + EXP_OFF);
+    for (int e = tid; e < 2 * C + 1; e += nt) bad |= (ex[e] & 0x7f800000u) == 0x7f800000u;
+  }
+  if (__syncthreads_or(bad) && tid == 0)
+    set_status(a.d_status, y < a.h_k ? GDN_DEV_NONFINITE_FRONTEND : GDN_DEV_NONFINITE_CHUNK);
+}
+
+}  // namespace tcp
+}  // namespace gdn
+
+cudaError_t gdn_check_tc_records(const GdnPrefillArgs& a, cudaStream_t s) {
+  if (a.total_tokens == 0) return cudaSuccess;
+  gdn::tcp::check_records_kernel<<<dim3((unsigned)a.max_chunks, a.h_k + a.h_v), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
   using namespace gdn::tcp;

@@ -78,6 +78,10 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_DEV_BAD_SLOT 0x1        /* slot index >= num_slots: row/sequence skipped */
 #define GDN_DEV_BAD_CU_SEQLENS 0x2  /* cu_seqlens not 0..total_tokens non-decreasing: call skipped */
 #define GDN_DEV_WAIT_TIMEOUT 0x4    /* an inter-CTA wait gave up: results invalid */
+/* With GDN_CHECK_FINITE (prefill): a NaN or Inf among what the stage wrote. */
+#define GDN_DEV_NONFINITE_FRONTEND 0x8  /* normalised q, k (and v, gates on the SIMT path) */
+#define GDN_DEV_NONFINITE_CHUNK 0x10    /* the chunk factors: P, U, Wk, decays */
+#define GDN_DEV_NONFINITE_OUT 0x20      /* the layer output o (y) or a final state */
 
 /* Bits of gdn_dims.flags.
  * GDN_FP32_STATE: prefill keeps every product with the fp32 state in fp32
@@ -88,6 +92,15 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
  *   is measured against the fp32 option on long, correlated-key sequences by
  *   the precision tests.  Decode always uses fp32 state products. */
 #define GDN_FP32_STATE 0x1
+/* GDN_CHECK_FINITE: after a prefill call (any prefill entry point) the library
+ *   scans what each stage wrote -- its workspace records or rows, the output,
+ *   the final states of the sequences with a valid slot -- and ORs
+ *   GDN_DEV_NONFINITE_FRONTEND / _CHUNK / _OUT into *d_status for each stage
+ *   that produced a NaN or Inf, so that the first such bit names the stage
+ *   where they appeared.  A debugging aid: it reads those buffers once more
+ *   (a few extra launches).  Requires d_status (null: GDN_EINVAL).  Decode
+ *   ignores it. */
+#define GDN_CHECK_FINITE 0x2
 
 typedef struct {
   int32_t h_k;     /* key/query heads */
@@ -98,7 +111,7 @@ typedef struct {
   int32_t chunk;   /* prefill chunk length: 16, 32 or 64 */
   int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
   float l2_eps;    /* added to the sum of squares inside the L2-norm root */
-  int32_t flags;   /* GDN_FP32_STATE or 0; other bits: GDN_EINVAL */
+  int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE, or 0; other bits: GDN_EINVAL */
 } gdn_dims;
 
 typedef struct {
