@@ -34,7 +34,7 @@ int check_dims(const gdn_dims* d) {
   if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
   if (d->conv_w != 4) return GDN_EUNSUPPORTED;
   if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
-  if (d->h_k > 65535) return GDN_EUNSUPPORTED;
+  if (d->h_k > 65535 || d->h_v > 65535) return GDN_EUNSUPPORTED;   // grid y extents
   // the prefill front end stages one token's conv output in shared memory
   if (conv_dim_of(d) * (int64_t)sizeof(float) > (int64_t)kMaxSmem) return GDN_EUNSUPPORTED;
   return GDN_OK;
