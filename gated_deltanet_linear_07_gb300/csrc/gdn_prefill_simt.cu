@@ -6,7 +6,8 @@
 //
 // Kernels, in stream order:
 //   1. check_cu_seqlens   one CTA; sets the workspace flag (and the device
-//                         status bit when cu_seqlens is malformed).
+//                         status bit when cu_seqlens is malformed) and writes
+//                         the chunk table (each sequence's first chunk).
 //   2. frontend           one CTA per token: causal conv (window or zero
 //                         history before the sequence start) + SiLU, L2 norm
 //                         of q and k with the 1/sqrt(d_k) query scale, gates.
@@ -29,7 +30,7 @@
 //       O = diag(e^gamma) Q S^T + P W
 //       S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
 //     Only e^{x} with x <= 0 is ever formed.  The products run as register
-//     blocks of 4 x 4 to 8 x 4 per thread on shared-memory operands.
+//     blocks of 2 x 4 to 8 x 4 per thread on shared-memory operands.
 #include <type_traits>
 
 #include "gdn_common.cuh"
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(256) window_writeback_kernel(const GdnPrefillA
 
 // ---- register-tiled products on shared-memory operands -----------------------
 // Each thread accumulates an RM x RN block: acc[m][n] += sum_k a(m, k) b(k, n).
-// "rows" operands are read one float per row (row stride padded so that the
-// rows a warp reads sit in different banks); "cols" operands four floats at a
+// "rows" operands are read one float per row (rows padded to d + 4 floats, so
+// consecutive rows start four banks apart); "cols" operands four floats at a
 // time from 16-byte aligned rows; sc, when given, scales b's row k.
 
 // a(m, k) = A[(r0 + m st) * lda + k], b(k, n) = B[(c0 + n st) * ldb + k] (both
