@@ -876,6 +876,10 @@ struct ScanSmem {
   // plain call does not reserve it (more of the SM's memory stays L1)
   static constexpr uint32_t CK = SIZE;
   static constexpr uint32_t SIZE_CK = CK + 65536;
+  // without checkpoints: the new conv window of this CTA's channels, [3][3 D]
+  // bf16, read at the start and written at the end
+  static constexpr uint32_t WIN = SIZE;
+  static constexpr uint32_t SIZE_WIN = WIN + 3 * 3 * D * 2;
 };
 // TMEM columns (fp32 accumulators, then the bf16 A operands, two per column):
 //   X [64] | O1 x 2 [64] | dH [128] | O2 [64] | H^T [64] | Wt^T [32] | W^T [32]
@@ -955,6 +959,30 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     mbar_init(hready, EPI_THREADS / 32);
     *s_abort = 0;
     fence_mbar_init();
+  }
+  // The sequence's new conv window for this CTA's channels (written at the
+  // end): head h's v channels and, from the even head of the pair, key head
+  // hk's q and k channels.  Read now, while the first chunk is being prepared.
+  const int nch_w = (h & 1) == 0 ? 3 * D : D;
+  auto win_channel = [&](int e) {
+    return e < D ? 2 * a.h_k * D + h * D + e                                 // v of head h
+                 : (e < 2 * D ? hk * D + (e - D) : a.h_k * D + hk * D + (e - 2 * D));   // q, k
+  };
+  __nv_bfloat16* s_win = reinterpret_cast<__nv_bfloat16*>(sm + ScanSmem::WIN);   // [3][3 D]
+  if (a.ckpt_every_chunks == 0) {
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
+    const __nv_bfloat16* win =
+        reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * a.conv_dim;
+    for (int e = tid; e < nch_w; e += SCAN_THREADS) {
+      const int c = win_channel(e);
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int64_t tau = Tb - 3 + r;
+        s_win[r * 3 * D + e] = tau >= 0 ? x[(size_t)(start + tau) * a.conv_dim + c]
+                                        : (init ? win[(size_t)(3 + tau) * a.conv_dim + c]
+                                                : __float2bfloat16_rn(0.f));
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1240,6 +1268,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  // The new conv window read at the start goes out.  The one reader of the old
+  // rows, chunk 0's prep item of key head hk, published before this CTA
+  // consumed chunk 0.  With checkpoints the window kernel writes every window
+  // (it also writes the checkpoints').
+  if (a.ckpt_every_chunks == 0 && !*s_abort) {
+    __nv_bfloat16* win =
+        reinterpret_cast<__nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * a.conv_dim;
+    for (int e = tid; e < nch_w; e += SCAN_THREADS) {
+      const int c = win_channel(e);
+#pragma unroll
+      for (int r = 0; r < 3; ++r) win[(size_t)r * a.conv_dim + c] = s_win[r * 3 * D + e];
+    }
+  }
   // Launched as a dependent of the prep, finish only after it (a no-op otherwise).
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -1320,7 +1361,8 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   const bool overlap = n_scan <= n_sm / 2;
   const int workers = overlap ? n_sm - (int)n_scan : n_sm;
   const int psmem = (int)PREP_SMEM + 1024;
-  const int ssmem = (int)(a.ckpt_every_chunks > 0 ? ScanSmem::SIZE_CK : ScanSmem::SIZE) + 1024;
+  const int ssmem =
+      (int)(a.ckpt_every_chunks > 0 ? ScanSmem::SIZE_CK : ScanSmem::SIZE_WIN) + 1024;
   if ((e = cudaFuncSetAttribute(prep_persistent_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess)
     return e;
@@ -1370,7 +1412,9 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
     if ((e = cudaLaunchKernelEx(&cfg, scan_kernel, a)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
   }
-  // conv windows are rewritten only after the prep has read them
-  if ((e = gdn_launch_window(a, GDN_BF16, s, tr)) != cudaSuccess) return e;
+  // With checkpoints the window kernel writes the sequences' windows and the
+  // checkpoints' after the scan; otherwise the scan wrote them itself.
+  if (a.ckpt_every_chunks > 0 && (e = gdn_launch_window(a, GDN_BF16, s, tr)) != cudaSuccess)
+    return e;
   return gdn_trace_mark(tr, 2, false, s);
 }
