@@ -60,9 +60,11 @@ def test_workspace_size_rules(lib):
     # tensor-core path (this shape): per chunk slot ([T/64] + B of them) one
     # 32 KiB [K;Q] tile per key head and a 41 KiB record per value head
     assert w1 >= (4096 // 64 + 1) * (16 * 32768 + 32 * 41984)
-    # SIMT path (fp32 I/O): normalised q, k, v and the two gates per token, fp32
+    # SIMT path (fp32 I/O): per token, fp32, the front end's normalised q, k, v and two
+    # gates, and the chunk kernel's U, Wk, P rows and cumulative decay
     d32 = gdn.make_dims(**dict(D4B, io="fp32"))
-    assert gdn.gdn_prefill_workspace_size(d32, 4096, 1) >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
+    per_token = (2 * 16 * 128 + 32 * 128 + 2 * 32) + (32 * 128 + 32 * 128 + 32 * 64 + 32)
+    assert gdn.gdn_prefill_workspace_size(d32, 4096, 1) >= 4096 * per_token * 4
     for bad in (dict(D4B, d_k=48), dict(D4B, chunk=128), dict(D4B, h_v=33),
                 dict(D4B, conv_w=3), dict(D4B, io=7), dict(D4B, h_k=1, h_v=65536, d_v=16)):
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**bad), 4096, 1) == 0
