@@ -54,6 +54,10 @@ def parse_args():
     p.add_argument("--decode-layers", type=int, default=24)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-large", action="store_true",
+                   help="skip the 4 x 32768 and the mixed varlen prefill workloads")
+    p.add_argument("--large-only", action="store_true",
+                   help="only the 4 x 32768 and the mixed varlen prefill workloads")
     return p.parse_args()
 
 
@@ -234,6 +238,71 @@ class Prefill:
                              d_status=self.status, trace=trace)
 
 
+class DevicePrefill(Prefill):
+    """A prefill workload whose inputs were drawn on the device
+    (device_layer_inputs); the call is Prefill's."""
+
+    def __init__(self, torch, gdn, dinp, device):
+        d = dinp["dims"]
+        self.torch, self.gdn, self.inp, self.dims = torch, gdn, dinp, d
+        self.io = torch.bfloat16 if d.io == "bf16" else torch.float32
+        self.host = None
+        for k in ("x", "a", "b", "cw", "A_log", "dt_bias", "cu", "slot", "init", "state", "conv"):
+            setattr(self, k, dinp[k])
+        T = dinp["x"].shape[0]
+        self.T = T
+        self.o = torch.empty((T, d.h_v, d.d_v), dtype=self.io, device=device)
+        ws = gdn.gdn_prefill_workspace_size(d, T, len(dinp["lengths"]))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def device_layer_inputs(torch, device, dims, lengths, seed, *, init="zero", b_mean=0.0,
+                        a_const=None, correlated_keys=0, state_std=0.02):
+    """The recipe of workloads.layer_inputs (same distributions and structure:
+    x, a, b ~ N(0, 1), b shifted by b_mean, a optionally constant, conv weight
+    ~ N(0, 0.5^2), A_log ~ U(0, 2.7), dt_bias ~ N(0, 0.1^2), states ~
+    N(0, state_std^2), windows ~ N(0, 1), shuffled slots, key channels of x in
+    alternating runs of one repeated vector and random segments) drawn on the
+    device with a seeded torch generator.  The large benchmark workloads take
+    minutes to draw on the host; these are timed, not compared with the
+    oracle (the parity tests draw theirs on the host)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    io = torch.bfloat16 if dims.io == "bf16" else torch.float32
+    B = len(lengths)
+    cu = np.zeros(B + 1, np.int64)
+    cu[1:] = np.cumsum(lengths)
+    T = int(cu[-1])
+    randn = lambda *shape: torch.randn(*shape, generator=g, device=device)  # noqa: E731
+    x = randn(T, dims.conv_dim)
+    if correlated_keys:
+        R = int(correlated_keys)
+        k0, k1 = dims.h_k * dims.d_k, 2 * dims.h_k * dims.d_k
+        for s in range(B):
+            for r0 in range(0, int(lengths[s]), 2 * R):
+                r1 = min(r0 + R, int(lengths[s]))
+                x[int(cu[s]) + r0:int(cu[s]) + r1, k0:k1] = randn(1, k1 - k0)
+    a = randn(T, dims.h_v)
+    if a_const is not None:
+        a.fill_(a_const)
+    b = randn(T, dims.h_v) + b_mean
+    num_slots = B
+    perm = torch.randperm(num_slots, generator=g, device=device)
+    has_init = torch.full((B,), 1 if init == "random" else 0, dtype=torch.uint8, device=device)
+    return {
+        "dims": dims, "lengths": [int(t) for t in lengths],
+        "x": x.to(io), "a": a.to(io), "b": b.to(io),
+        "cw": randn(dims.conv_dim, dims.conv_w) * 0.5,
+        "A_log": torch.rand(dims.h_v, generator=g, device=device) * 2.7,
+        "dt_bias": randn(dims.h_v) * 0.1,
+        "cu": torch.from_numpy(cu.astype(np.int32)).to(device),
+        "slot": perm[:B].to(torch.int32).contiguous(), "init": has_init,
+        "state": randn(num_slots, dims.h_v, dims.d_k, dims.d_v) * state_std,
+        "conv": randn(num_slots, dims.conv_w - 1, dims.conv_dim).to(io),
+    }
+
+
 def trace_stages(torch, gdn, run, ev, flush):
     """Attribution pass: the steps again with stage events and a launch count
     (the events sit between kernels, so this pass is not the headline).
@@ -259,7 +328,14 @@ def trace_stages(torch, gdn, run, ev, flush):
 def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     inp = workloads.prefill_4b()
     run = Prefill(torch, gdn, inp, device)
-    flush = L2Flush(torch, device)
+    out = time_prefill(torch, gdn, run, L2Flush(torch, device), steps, warmup)
+    out["inp"] = inp
+    return out
+
+
+def time_prefill(torch, gdn, run, flush, steps, warmup):
+    """K timed calls of `run` (L2 flushed before each), then the stage
+    attribution pass."""
     ns = gdn.STAGES
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     for _ in range(max(warmup, 1)):
@@ -282,8 +358,95 @@ def bench_prefill(torch, gdn, workloads, device, steps, warmup):
     step_ms = [e["s"].elapsed_time(e["e"]) for e in ev]
     stage_ms, launches = trace_stages(torch, gdn, run, ev, flush)
     status = int(run.status.item())
-    return {"inp": inp, "run": run, "step_ms": step_ms, "stage_ms": stage_ms,
+    return {"run": run, "step_ms": step_ms, "stage_ms": stage_ms,
             "launches": launches, "status": status}
+
+
+LARGE_WORKLOADS = {
+    "adversarial_4x32768": "4 sequences x 32768 tokens of the Qwen3.5-4B layer, bf16, random "
+                           "initial states and windows, key channels in alternating 512-token "
+                           "runs of one repeated vector and random segments, b ~ N(6, 1)",
+    "varlen_16": "16 sequences of U{1..8192} tokens (cu_seqlens) of the Qwen3.5-4B layer, bf16, "
+                 "zero initial state, shuffled slots; then 256 decode steps per sequence",
+}
+
+
+def bench_large(torch, gdn, workloads, device, name, steps, warmup, peak_tf, peak_src, hbm):
+    """One of the large prefill workloads: K timed calls (L2 flushed before
+    each; the inputs are larger than L2 as well), the stage split, the
+    roofline of the dominant stage and the whole-call fraction; for the
+    varlen batch also its 256 decode steps."""
+    d = workloads.QWEN35_4B
+    if name == "adversarial_4x32768":
+        lengths = [32768] * 4
+        dinp = device_layer_inputs(torch, device, d, lengths, workloads.SEED_BASE + 4,
+                                   init="random", b_mean=6.0, correlated_keys=512)
+    else:
+        lengths, _ = workloads.varlen_lengths()
+        dinp = device_layer_inputs(torch, device, d, lengths.tolist(), workloads.SEED_BASE + 5)
+    run = DevicePrefill(torch, gdn, dinp, device)
+    res = time_prefill(torch, gdn, run, L2Flush(torch, device), steps, warmup)
+    T = run.T
+    ms = statistics.median(res["step_ms"])
+    roof, stage_tflops = prefill_roofline(d, T, res["stage_ms"], peak_tf, peak_src)
+    flops = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
+    # minimum HBM bytes of the call: x, a, b in, o out, initial states read, final written
+    nb = len(lengths)
+    state_b = d.h_v * d.d_k * d.d_v * 4
+    min_bytes = T * (d.conv_dim * 2 + 2 * d.h_v * 2 + d.h_v * d.d_v * 2) + \
+        nb * state_b * (2 if name == "adversarial_4x32768" else 1)
+    out = {"metric": "GDN prefill tokens/s", "value": T / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_step": ms, "steps": steps,
+           "config": {"workload": LARGE_WORKLOADS[name], "B": nb, "T": T, "chunk": d.chunk,
+                      "io": d.io, "data": "synthetic, drawn on the device (seeded)",
+                      "l2": "flushed before every timed step; inputs larger than L2"},
+           "roofline": roof, "stages_ms": res["stage_ms"], "stages_tflops": stage_tflops,
+           "tc_roofline_frac_whole_step": flops / (ms / 1e3) / 1e12 / peak_tf,
+           "flops_per_step": flops, "min_hbm_bytes_per_step": min_bytes,
+           "hbm_floor_frac_of_tc_roofline": (flops / peak_tf / 1e12) /
+                                            (min_bytes / hbm / 1e9),
+           "gpu_launches": res["launches"], "device_status": res["status"]}
+    if name == "varlen_16":
+        out["decode_after_prefill"] = bench_varlen_decode(torch, gdn, run, steps, warmup)
+    del run, dinp
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_varlen_decode(torch, gdn, run, steps, warmup, n_steps=256):
+    """The varlen batch's 256 decode steps after its prefill: one token per
+    sequence per step on the slots the prefill wrote, back to back."""
+    d = run.dims
+    B = len(run.inp["lengths"])
+    g = torch.Generator(device=run.x.device)
+    g.manual_seed(5005)
+    xs = torch.randn(n_steps, B, d.conv_dim, generator=g, device=run.x.device).to(run.io)
+    abs_ = torch.randn(2, n_steps, B, d.h_v, generator=g, device=run.x.device).to(run.io)
+    o = torch.empty((B, d.h_v, d.d_v), dtype=run.io, device=run.x.device)
+    status = torch.zeros(1, dtype=torch.int32, device=run.x.device)
+
+    def all_steps():
+        for t in range(n_steps):
+            gdn.gdn_decode_step(d, run.cw, run.A_log, run.dt_bias, xs[t], abs_[0, t], abs_[1, t],
+                                run.slot, run.state, run.conv, o, d_status=status)
+    for _ in range(max(warmup, 1)):
+        all_steps()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(steps // 4, 3)):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        all_steps()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) / n_steps)
+    ms = statistics.median(times)
+    sb = B * 2 * d.h_v * d.d_k * d.d_v * 4
+    return {"metric": "decode state GB/s", "value": sb / (ms / 1e3) / 1e9, "unit": "GB/s",
+            "ms_per_step": ms, "rows_per_step": B, "state_bytes_per_step": sb,
+            "note": "16 slots of state (64 MiB) stay resident in L2 across the back-to-back "
+                    "steps, so this is not an HBM roofline figure",
+            "device_status": int(status.item())}
 
 
 def bench_e2e(torch, gdn, run, steps, warmup):
@@ -599,6 +762,38 @@ def replica_throughput(world, units_per_rank, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
+def prefill_roofline(d, T, stage, peak_tf, peak_src, reduce=lambda v: v):
+    """Roofline of the dominant prefill stage: the method's FLOPs that stage
+    performs (per launch) over its event time, against the bf16 peak.  The
+    chunk stage does K K^T, Q K^T, T (beta V), T (beta e^gamma K) (8 C d per
+    token and head), the scan P W and Wk S^T, Q S^T, W^T K (2 C d + 6 d^2);
+    in the overlapped launch the chunk work runs inside the scan stage's
+    interval, which then carries both shares."""
+    stage_flops = {"frontend": 0.0,
+                   "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
+                   "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
+    overlapped = "scan" in stage and "chunk" not in stage
+    if overlapped:
+        stage_flops["scan"] += stage_flops["chunk"]
+    dom = max(stage, key=stage.get) if stage else None
+    roof = None
+    if dom and stage_flops.get(dom):
+        dom_ms = reduce(stage[dom])
+        ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": ach / peak_tf,
+                "traffic": recorded_traffic("prefill_overlap" if overlapped else "prefill_" + dom),
+                "kernel": {"chunk": "prep_persistent_kernel (prefill stage 'chunk')",
+                           "scan": ("scan_kernel (prefill stage 'scan')" if "chunk" in stage else
+                                   "prep_persistent_kernel + scan_kernel, overlapped "
+                                   "(prefill stage 'scan')")}.get(dom, dom),
+                "peak_source": f"bf16_tflops ({peak_src})",
+                "launch_ms": dom_ms, "flops_per_launch": stage_flops[dom]}
+    stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()
+                    if stage_flops.get(k)}
+    return roof, stage_tflops
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(args):
@@ -612,7 +807,7 @@ def run_reference(args):
         oracle_prefill_time(inp, cores)
     times = [oracle_prefill_time(inp, cores) for _ in range(args.steps)]
     T = inp["x"].shape[0]
-    ms = 1e3 * statistics.mean(times)
+    ms = 1e3 * statistics.median(times)   # the median, as the GPU arm takes
     value = T / (ms / 1e3)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -654,7 +849,7 @@ def run_gdn(args):
     sampler.start()
     time.sleep(0.2)
     pf = None
-    if not args.no_prefill:
+    if not args.no_prefill and not args.large_only:
         pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
         barrier()
     gn = sc = ck = f32 = None
@@ -668,13 +863,22 @@ def run_gdn(args):
         barrier()
         f32 = bench_fp32_state(torch, gdn, pf["inp"], device, args.steps, args.warmup)
         barrier()
+    large = {}
+    if not args.no_large and not args.no_prefill:
+        for name in LARGE_WORKLOADS:
+            large[name] = bench_large(torch, gdn, workloads, device, name, args.steps, args.warmup,
+                                      peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+                                      peak_src, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            barrier()
     dec = None
-    if not args.no_decode:
+    if not args.no_decode and not args.large_only:
         dec = bench_decode(torch, gdn, workloads, device, args.decode_steps or args.steps,
                            args.warmup, layers=args.decode_layers)
         barrier()
     clocks = sampler.stop()
     if pf is None:
+        if rank == 0 and large:
+            print(json.dumps({"prefill_workloads": large, "clocks": clocks}), flush=True)
         if rank == 0 and dec is not None:
             print(json.dumps({"decode_only": True, "ms_per_step": statistics.median(dec["step_ms"]),
                               "layer_ms": statistics.median(dec["layer_ms"]),
@@ -693,35 +897,9 @@ def run_gdn(args):
     ms = max_ranks(statistics.median(pf["step_ms"]))   # median of the K steps
     value = replica_throughput(world, T, ms)
     flops_launch = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
-    # The method's FLOPs by the stage that performs them: the chunk stage does
-    # K K^T, Q K^T, T (beta V), T (beta e^gamma K) (8 C d per token and head),
-    # the scan does P W and Wk S^T, Q S^T, W^T K (2 C d + 6 d^2).
-    stage_flops = {"frontend": 0.0,
-                   "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
-                   "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
-    stage = pf["stage_ms"]
-    overlapped = "scan" in stage and "chunk" not in stage
-    if overlapped:
-        # Overlapped launch: the chunk work runs beside the scan inside the
-        # scan stage's interval, so that interval carries both FLOP shares.
-        stage_flops["scan"] += stage_flops["chunk"]
-    dom = max(stage, key=stage.get) if stage else None
     peak_tf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    roof = None
-    if dom and stage_flops.get(dom):
-        dom_ms = max_ranks(stage[dom])
-        ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": ach / peak_tf,
-                "traffic": recorded_traffic("prefill_overlap" if overlapped else "prefill_" + dom),
-                "kernel": {"chunk": "prep_kernel (prefill stage 'chunk')",
-                           "scan": ("scan_kernel (prefill stage 'scan')" if "chunk" in stage else
-                                   "prep_persistent_kernel + scan_kernel, overlapped "
-                                   "(prefill stage 'scan')")}.get(dom, dom),
-                "peak_source": f"bf16_tflops ({peak_src})",
-                "launch_ms": dom_ms, "flops_per_launch": stage_flops[dom]}
-    stage_tflops = {k: stage_flops[k] / (v / 1e3) / 1e12 for k, v in stage.items()
-                    if stage_flops.get(k)}
+    roof, stage_tflops = prefill_roofline(d, T, pf["stage_ms"], peak_tf, peak_src, max_ranks)
+    stage = pf["stage_ms"]
     if dec:   # collectives: every rank takes part
         dms = max_ranks(statistics.median(dec["step_ms"]))
         lms = max_ranks(statistics.median(dec["layer_ms"]))
@@ -739,6 +917,8 @@ def run_gdn(args):
             "gpu_launches": pf["launches"], "clocks": clocks,
             "device_status": pf["status"],
         }
+        if large:
+            line["prefill_workloads"] = large
         if e2e:
             line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],

@@ -499,8 +499,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
   const int C = args.chunk, DK = args.d_k, DV = args.d_v;
   const int slot = args.slot_idx[b];
   if (slot < 0 || slot >= args.num_slots) {
-    if (h == 0 && blockIdx.z == 0 && tid == 0 && slot >= args.num_slots)
-      set_status(args.d_status, GDN_DEV_BAD_SLOT);
+    if (h == 0 && blockIdx.z == 0 && tid == 0) set_status(args.d_status, GDN_DEV_BAD_SLOT);
     return;
   }
   const ScanSmem S(C, DK, DVT);

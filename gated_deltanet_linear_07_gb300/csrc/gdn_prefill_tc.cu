@@ -7,8 +7,9 @@
 // DeltaNet fast paths": everything state-independent is batched ahead of the
 // cross-chunk loop) runs as two kernels:
 //
-// prep  one CTA per (chunk, key head), all chunks of all sequences in
-//       parallel.  Causal conv + SiLU of the chunk's q, k and both value
+// prep  persistent, one CTA per SM; its 16 warps take one (chunk, key head)
+//       item at a time, all chunks of all sequences.  Causal conv + SiLU of
+//       the chunk's q, k and both value
 //       heads' v (3-token halo from x or from the slot's window), L2 norms,
 //       gates and the in-chunk cumulative log-decay gamma; then on the tensor
 //       cores  [K;Q] K^T  (one M=128 MMA gives K K^T and Q K^T), the exact
@@ -26,7 +27,8 @@
 //         dH   = (W^T diag(e^{gamma_C - gamma})) K
 //         o    = diag(e^gamma) O1^T + O2^T,   H^T <- e^{gamma_C} H^T + dH
 //       Chunk inputs stream in with bulk async copies two chunks deep; one
-//       thread issues the MMAs; eight epilogue warps own TMEM lanes.
+//       thread issues the MMAs; sixteen chain warps own TMEM lanes and keep
+//       the fp32 state in registers; four output warps write o off the chain.
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets
 // GDN_DEV_WAIT_TIMEOUT, skips the dependent work and still frees its TMEM.
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(1024) setup_kernel(const GdnPrefillArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// prep: one CTA (512 threads) per (chunk, key head).
+// prep: persistent CTAs (512 threads), one (chunk, key head) item at a time.
 
 // Warp-level TF32 tensor-core product for the 16 x 16 blocks of the chunk
 // inverse: fragments of mma.m16n8k8 (row.col), fp32 accumulate.
@@ -897,7 +899,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   const int slot = a.slot_idx[b];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (slot < 0 || slot >= a.num_slots) {
-    if (h == 0 && tid == 0 && slot >= a.num_slots) set_status(a.d_status, GDN_DEV_BAD_SLOT);
+    if (h == 0 && tid == 0) set_status(a.d_status, GDN_DEV_BAD_SLOT);
     return;
   }
   const int64_t start = a.cu_seqlens[b];

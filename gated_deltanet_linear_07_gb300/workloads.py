@@ -203,10 +203,16 @@ def adversarial(seed: int = SEED_BASE + 4, B: int = 4, T: int = 32768,
                         correlated_keys=512)
 
 
+def varlen_lengths(seed: int = SEED_BASE + 5, B: int = 16, max_len: int = 8192):
+    """The sequence lengths of the mixed varlen batch, U{1..max_len}, and the
+    generator that drew them (its later draws are the decode tokens)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(1, max_len + 1, size=B), rng
+
+
 def varlen(seed: int = SEED_BASE + 5, B: int = 16, max_len: int = 8192,
            decode_steps: int = 256) -> dict:
-    rng = np.random.Generator(np.random.PCG64(seed))
-    lengths = rng.integers(1, max_len + 1, size=B)
+    lengths, rng = varlen_lengths(seed, B, max_len)
     inp = layer_inputs(QWEN35_4B, lengths, seed + 1, init="zero", num_slots=B)
     dims = inp["dims"]
     inp["decode_x"] = _io(_normal(rng, (decode_steps, B, dims.conv_dim)), dims)

@@ -75,7 +75,8 @@ typedef enum {
 typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 /* Bits of *d_status. */
-#define GDN_DEV_BAD_SLOT 0x1        /* slot index >= num_slots: row/sequence skipped */
+#define GDN_DEV_BAD_SLOT 0x1        /* slot index out of range (prefill: < 0 or >= num_slots;
+                                       decode: >= num_slots): row/sequence skipped */
 #define GDN_DEV_BAD_CU_SEQLENS 0x2  /* cu_seqlens not 0..total_tokens non-decreasing: call skipped */
 #define GDN_DEV_WAIT_TIMEOUT 0x4    /* an inter-CTA wait gave up: results invalid */
 /* With GDN_CHECK_FINITE (prefill): a NaN or Inf among what the stage wrote. */
@@ -172,8 +173,10 @@ size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
  *   x [total_tokens][conv_dim], a, b [total_tokens][h_v] IO (device)
  *   cu_seqlens [num_seqs+1] int32 (device): 0 = cu[0] <= cu[1] <= ... =
  *              total_tokens, else GDN_DEV_BAD_CU_SEQLENS and nothing runs
- *   slot_idx [num_seqs] int32 (device), distinct; out of range ->
- *              GDN_DEV_BAD_SLOT and that sequence is skipped
+ *   slot_idx [num_seqs] int32 (device), distinct; out of range (< 0 or
+ *              >= num_slots) -> GDN_DEV_BAD_SLOT and that sequence is
+ *              skipped: its o rows, state and window are left as they were
+ *              (prefill has no padding sequences)
  *   has_initial_state [num_seqs] uint8 (device) or NULL (= all zero): when
  *              zero the sequence starts from S = 0 and an all-zero window,
  *              ignoring what its slot holds

@@ -14,7 +14,8 @@ import gated_deltanet_linear_07_gb300 as gdn
 import oracle
 from gated_deltanet_linear_07_gb300 import workloads
 from gated_deltanet_linear_07_gb300.workloads import QWEN35_4B, TINY, Dims
-from tests._gpu import (DecodeRun, PrefillRun, assert_close, dev, io_dtype, oracle_decode,
+from tests._gpu import (DecodeRun, PrefillRun, assert_close, assert_close_rows, assert_close_seqs,
+                        dev, io_dtype, oracle_decode,
                         oracle_prefill)
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +59,7 @@ def test_fused_prefill_matches_oracle(gpu_lib, name):
     np.testing.assert_array_equal(dz.float().cpu().numpy(), z)          # z is not touched
     ref_o = oracle_prefill(inp)["o"]
     ref = oracle.gated_rmsnorm(ref_o, z, w, eps=1e-6)
-    worst = assert_close(got["o"], ref, d, f"{name} y")
+    worst = assert_close_seqs(got["o"], ref, inp["cu_seqlens"], d, f"{name} y")
     print(f"fused prefill {name}: worst normalised error {worst:.3e}")
 
 
@@ -106,7 +107,7 @@ def test_fused_decode_matches_oracle(gpu_lib, name):
     ref = oracle_decode(inp)
     rows = ref["rows"]
     y = oracle.gated_rmsnorm(ref["o"], z[rows], w, eps=1e-6)
-    worst = assert_close(got["o"][rows], y, d, f"{name} decode y")
+    worst = assert_close_rows(got["o"][rows], y, d, f"{name} decode y row")
     pad = [n for n in range(24) if inp["slot_idx"][n] < 0]
     assert pad and not got["o"][pad].any(), "padding rows must be zero"
     print(f"fused decode {name}: worst normalised error {worst:.3e}")

@@ -11,7 +11,7 @@ import gated_deltanet_linear_07_gb300 as gdn
 import oracle
 from gated_deltanet_linear_07_gb300 import workloads
 from gated_deltanet_linear_07_gb300.workloads import QWEN35_4B, TINY, Dims
-from tests._gpu import assert_close, dev, io_dtype
+from tests._gpu import assert_close_rows, dev, io_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def test_gated_rmsnorm_matches_oracle(gpu_lib, name, in_place):
     torch.cuda.synchronize()
     got = dy.float().cpu().numpy()
     ref = oracle.gated_rmsnorm(o, z, w, eps=1e-6)
-    assert_close(got, ref, d, f"{name} y")
+    assert_close_rows(got, ref, d, f"{name} y row")
     assert not got[0].any()
     if not in_place:   # the inputs are not touched
         np.testing.assert_array_equal(do.float().cpu().numpy(), o)
@@ -69,7 +69,7 @@ def test_gated_rmsnorm_qwen35_4b_full_output(gpu_lib):
     torch.cuda.synchronize()
     got = dy.float().cpu().numpy()
     ref = oracle.gated_rmsnorm(o, z, w)
-    worst = assert_close(got, ref, d, "y")
+    worst = assert_close_rows(got, ref, d, "y row")
     # per row the result is only bf16 rounding away from the float64 one
     rows = np.abs(ref).max(axis=-1, keepdims=True) + 1e-30
     assert np.percentile(np.abs(got - ref) / rows, 99.9) < 1e-2

@@ -48,9 +48,9 @@ def test_tiny_token_by_token_decode_matches_prefill_oracle(gpu_lib):
                             dev(inp["b"][t:t + 1], io), slot, state, conv, o)
         outs.append(o)
     got = torch.cat(outs).float().cpu().numpy()
-    from tests._gpu import assert_close
-    assert_close(got, ref["o"], d, "o")
-    assert_close(state[0].cpu().numpy(), ref["state"][0], d, "state")
+    from tests._gpu import assert_close_heads
+    assert_close_heads(got, ref["o"], d, "o", head_axis=1)
+    assert_close_heads(state[0].cpu().numpy(), ref["state"][0], d, "state", head_axis=0)
     np.testing.assert_array_equal(conv[0].float().cpu().numpy(), ref["window"][0])
 
 
@@ -171,9 +171,10 @@ def test_prefill_then_prefill_then_decode_handoff(gpu_lib):
                             dev(full["b"][t:t + 1], io), slot, state, conv, o)
         outs.append(o)
     got = torch.cat(outs).float().cpu().numpy()
-    from tests._gpu import assert_close
-    assert_close(got, ref["o"], d, "o")
-    assert_close(state[int(full["slot_idx"][0])].cpu().numpy(), ref["state"][0], d, "state")
+    from tests._gpu import assert_close_heads
+    assert_close_heads(got, ref["o"], d, "o", head_axis=1)
+    assert_close_heads(state[int(full["slot_idx"][0])].cpu().numpy(), ref["state"][0], d, "state",
+                       head_axis=0)
     np.testing.assert_array_equal(conv[int(full["slot_idx"][0])].float().cpu().numpy(),
                                   ref["window"][0])
 
@@ -210,8 +211,8 @@ def test_device_status_bits(gpu_lib):
     g = run.results()
     assert g["status"] & gdn.GDN_DEV_BAD_SLOT
     ref = oracle_prefill(bad2 | {"slot_idx": np.array([1, 2], np.int32)})
-    from tests._gpu import assert_close
-    assert_close(g["state_pool"][1], ref["state"][0], d, "state seq 0")
+    from tests._gpu import assert_close_heads
+    assert_close_heads(g["state_pool"][1], ref["state"][0], d, "state seq 0", head_axis=0)
     # decode with an out-of-range slot
     dinp = workloads.decode_inputs(d, n_rows=3, num_slots=4, seed=1)
     dinp["slot_idx"] = np.array([0, 7, 2], np.int32)
@@ -220,6 +221,28 @@ def test_device_status_bits(gpu_lib):
     g = run.results()
     assert g["status"] & gdn.GDN_DEV_BAD_SLOT
     assert not g["o"][1].any()
+
+
+@pytest.mark.parametrize("dims", [TINY, QWEN35_4B], ids=["simt", "tensor_core"])
+def test_prefill_negative_slot_sets_status_and_skips(gpu_lib, dims):
+    """Prefill has no padding sequences: a negative slot is out of range like
+    one past the pool, sets GDN_DEV_BAD_SLOT and leaves that sequence's o rows,
+    and every slot, as they were; the other sequence runs normally."""
+    inp = workloads.layer_inputs(dims, [70, 9], seed=12, init="random", num_slots=3)
+    bad = dict(inp, slot_idx=np.array([-1, 2], np.int32))
+    run = PrefillRun(bad)
+    run()
+    g = run.results()
+    assert g["status"] & gdn.GDN_DEV_BAD_SLOT
+    assert np.isnan(g["o"][:70]).all(), "the skipped sequence's o rows must not be written"
+    for sl in (0, 1):
+        np.testing.assert_array_equal(g["state_pool"][sl], inp["state_pool"][sl])
+        np.testing.assert_array_equal(g["conv_pool"][sl], inp["conv_pool"][sl])
+    ref = oracle_prefill(dict(bad, slot_idx=np.array([0, 2], np.int32)))
+    from tests._gpu import assert_close_heads
+    assert_close_heads(g["o"][70:], ref["o"][70:], dims, "o seq 1", head_axis=1)
+    assert_close_heads(g["state_pool"][2], ref["state"][1], dims, "state seq 1", head_axis=0)
+    np.testing.assert_array_equal(g["conv_pool"][2], ref["window"][1].astype(np.float32))
 
 
 # ---- full-size workloads, as the benchmark launches them ------------------
@@ -248,8 +271,9 @@ def test_decode_24_layers_64_slots_full_size_sampled(gpu_lib):
         ref = oracle_decode(inp, rows=rows)
         g = r.results()
         sl = inp["slot_idx"]
-        from tests._gpu import assert_close
-        assert_close(g["o"][rows], ref["o"], inp["dims"], f"layer {layer} o")
-        assert_close(g["state_pool"][sl[rows]], ref["state"], inp["dims"], f"layer {layer} state")
+        from tests._gpu import assert_close_rows
+        assert_close_rows(g["o"][rows], ref["o"], inp["dims"], f"layer {layer} o row")
+        assert_close_rows(g["state_pool"][sl[rows]], ref["state"], inp["dims"],
+                          f"layer {layer} state row")
         np.testing.assert_array_equal(g["conv_pool"][sl[rows]], ref["window"].astype(np.float32))
         assert g["status"] == 0
