@@ -136,6 +136,9 @@ struct GdnPrefillArgs {
   uint8_t* kq_ws;       // [max_chunks][h_k] [K;Q] tile images
   uint8_t* vh_ws;       // [max_chunks][h_v] P | U^T | decay factors | Wk records
   int32_t* chunk_ready; // [max_chunks][h_k] set to 1 when the prep published the chunk
+  // 1: the scan runs beside the prep and waits for each chunk's ready flag;
+  // 0: the scan starts after the prep kernel has finished (no flags needed)
+  int32_t publish;
   // interval checkpoints (0 / null: none): every ckpt_every_chunks chunks strictly
   // inside sequence b, the state and window go to slot ckpt_slot[b] + k - 1
   int32_t ckpt_every_chunks;

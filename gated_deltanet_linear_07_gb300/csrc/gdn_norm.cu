@@ -77,11 +77,14 @@ __global__ void __launch_bounds__(256) gated_rmsnorm_kernel(const float* __restr
     const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      // SiLU(z) = h + h tanh(h), h = z / 2 (saturates cleanly in both tails)
-      const float h = 0.5f * zv[i + k];
-      float t;
-      asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
-      yv[i + k] = ov[i + k] * inv * wv[k] * fmaf(h, t, h);
+      // SiLU(z) = z / (1 + 2^(-z log2 e)) with the exponential and the
+      // quotient on the special-function unit: relative accuracy of a few ulp
+      // for every z (the form h + h tanh(h) loses it for negative z, where
+      // the two terms cancel); -> 0 for z -> -inf, z for z -> +inf.
+      const float zk = zv[i + k];
+      float e;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * zk));
+      yv[i + k] = ov[i + k] * inv * wv[k] * __fdividef(zk, 1.0f + e);
     }
   }
   if (live) V::store(reinterpret_cast<IO*>(y) + off, yv);

@@ -32,6 +32,9 @@
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets
 // GDN_DEV_WAIT_TIMEOUT, skips the dependent work and still frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gdn_check.cuh"
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
@@ -96,6 +99,23 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// 2-D tiled TMA load (tensor map in kernel-parameter space) of the box at
+// (x = c0 elements, y = c1 rows) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
@@ -296,6 +316,14 @@ struct PrepSmem {
   static constexpr uint32_t EG = BETA + 512;                  // fp32 [2][64], e^{gamma}
   static constexpr uint32_t BAR = EG + 512;                   // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
+  // The item's x rows, brought in by TMA one item ahead: for each of the four
+  // 128-channel segments (q, k, v of value head 2 hk, v of 2 hk + 1) the rows
+  // t0 - 3 .. t0 + 63 as a dense [67][128] bf16 box (256-byte rows).
+  static constexpr uint32_t XT = (SIZE + 1023) / 1024 * 1024;
+  static constexpr uint32_t XT_ROWS = 67;
+  static constexpr uint32_t XT_SEG = 17408;                   // 67 x 256 bytes, rounded to 1 KiB
+  static constexpr uint32_t XT_BYTES = 4 * XT_ROWS * 256;     // transaction bytes per item
+  static constexpr uint32_t SIZE_X = XT + 4 * XT_SEG;
   static constexpr int AST = 68;             // fp32 row stride of A and T
   static constexpr int THREADS = 256;
 };
@@ -309,22 +337,10 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ off, int B, 
   return lo;
 }
 
-// L2 prefetch of one work item's inputs: the x rows [r0, t1) of key head hk's
-// q, k and two v segments (r0 includes the 3-token halo) and the a / b rows
-// [t0, t1), one 128-byte line per request, spread over n threads (thread
-// index i).  The caller keeps the rows inside the input.
-__device__ __forceinline__ void prefetch_rows(const GdnPrefillArgs& a, int hk, int64_t r0,
-                                              int64_t t0, int64_t t1, int i, int n) {
-  const size_t cd2 = (size_t)a.conv_dim * 2;
-  const unsigned char* x = reinterpret_cast<const unsigned char*>(a.x);
-  const size_t seg_q = (size_t)hk * D * 2, seg_k = (size_t)(a.h_k + hk) * D * 2,
-               seg_v = (size_t)(2 * a.h_k + 2 * hk) * D * 2;
-  const int nl = (int)(t1 - r0) * 8;   // 2 + 2 + 4 lines per row
-  for (int l = i; l < nl; l += n) {
-    const int r = l >> 3, q = l & 7;
-    const size_t off = q < 2 ? seg_q + 128 * q : (q < 4 ? seg_k + 128 * (q - 2) : seg_v + 128 * (q - 4));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + (size_t)(r0 + r) * cd2 + off) : "memory");
-  }
+// L2 prefetch of the gates a / b of one work item (rows [t0, t1)), one
+// 128-byte line per request, spread over n threads (thread index i).
+__device__ __forceinline__ void prefetch_gates(const GdnPrefillArgs& a, int64_t t0, int64_t t1,
+                                               int i, int n) {
   const size_t g0 = (size_t)t0 * a.h_v * 2, g1 = (size_t)t1 * a.h_v * 2;  // bytes of a / b rows
   for (size_t o = (g0 & ~(size_t)127) + 128 * (size_t)i; o < g1; o += 128 * (size_t)n) {
     const size_t q = o < g0 ? g0 : o;
@@ -332,32 +348,65 @@ __device__ __forceinline__ void prefetch_rows(const GdnPrefillArgs& a, int hk, i
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const unsigned char*>(a.b) + q) : "memory");
   }
 }
-// The same for work item `item` (chunk-major (chunk, key head) index), found
-// through the chunk table.
-__device__ __forceinline__ void prefetch_item(const GdnPrefillArgs& a, int item, int i, int n) {
-  const int32_t gc = item / a.h_k;
-  const int hk = item % a.h_k;
-  const int b = find_seq(a.chunk_off, a.num_seqs, gc);
-  const int64_t start = a.cu_seqlens[b];
-  const int64_t t0 = start + (int64_t)(gc - a.chunk_off[b]) * C;
-  const int64_t t1 = min(t0 + C, (int64_t)a.cu_seqlens[b + 1]);
-  prefetch_rows(a, hk, t0 - 3 > start ? t0 - 3 : start, t0, t1, i, n);
+
+// Where work item `item` (chunk-major (chunk, key head) index) lives: its
+// sequence b, key head hk, global chunk gc and first token t0.
+struct ItemPos {
+  int32_t gc;
+  int hk, b;
+  int64_t t0;
+};
+__device__ __forceinline__ ItemPos item_pos(const GdnPrefillArgs& a, int item) {
+  ItemPos p;
+  p.gc = item / a.h_k;
+  p.hk = item % a.h_k;
+  p.b = find_seq(a.chunk_off, a.num_seqs, p.gc);
+  p.t0 = a.cu_seqlens[p.b] + (int64_t)(p.gc - a.chunk_off[p.b]) * C;
+  return p;
+}
+// The first item at or after `item`, stepping by n, whose sequence has a valid
+// slot (items of skipped sequences are not prepared), or n_items.
+__device__ __forceinline__ int next_valid_item(const GdnPrefillArgs& a, int item, int n, int n_items) {
+  for (; item < n_items; item += n) {
+    const int b = find_seq(a.chunk_off, a.num_seqs, item / a.h_k);
+    const int slot = a.slot_idx[b];
+    if (slot >= 0 && slot < a.num_slots) break;
+  }
+  return item;
+}
+// TMA of one item's x rows t0 - 3 .. t0 + 63 of its four channel segments
+// into the x tile (rows outside the input read as zero; rows before the
+// sequence's start are replaced by the window in the front end).  Issued by
+// one thread; completes on `bar` with PrepSmem::XT_BYTES.
+__device__ __forceinline__ void issue_x_tile(const GdnPrefillArgs& a, const CUtensorMap* map,
+                                             int item, uint32_t xt, uint64_t* bar) {
+  const ItemPos p = item_pos(a, item);
+  const int y = (int)(p.t0 - 3);
+  mbar_expect_tx(bar, PrepSmem::XT_BYTES);
+  tma_load_2d(xt, map, p.hk * D, y, bar);                                  // q
+  tma_load_2d(xt + PrepSmem::XT_SEG, map, (a.h_k + p.hk) * D, y, bar);     // k
+  tma_load_2d(xt + 2 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * p.hk) * D, y, bar);      // v, 2 hk
+  tma_load_2d(xt + 3 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * p.hk + 1) * D, y, bar);  // v, 2 hk + 1
 }
 
 // One (chunk, key head) work item, run by the 16 warps of the CTA (thread index
-// tid, <= 128 registers each) on ~107 KB of shared memory `sm`, two MMA
-// mbarriers (completing once per item; parity ph) and 256 TMEM columns from
-// `tmem`.  One item at a time per SM: the scan starts once the first chunk is
-// published, and a 16-warp item takes about 60 % of the time of two 8-warp
-// items sharing an SM (which would give more items per second, but the scan
-// consumes them no faster than this).  grp synchronises the 16 warps, head4
-// the 4 warps of one value head in the phases that run on warps 0..7 only.
+// tid, <= 128 registers each) on ~180 KB of shared memory `sm`, two MMA
+// mbarriers (completing once per item; parity ph), the x-tile mbarrier
+// (parity xph) and 256 TMEM columns from `tmem`.  The item's x rows are
+// already in flight to the x tile (TMA, issued during the previous item);
+// once the front end has read them this item issues the next item's tile
+// (`next`, or none when next < 0).  One item at a time per SM: the scan
+// starts once the first chunk is published, and a 16-warp item takes about
+// 60 % of the time of two 8-warp items sharing an SM.  grp synchronises the
+// 16 warps, head4 the 4 warps of one value head in the phases that run on
+// warps 0..7 only.
 constexpr int NW = 16;
 constexpr int WPS = NW / 4;             // warps per front-end segment
 constexpr int TPW = C / WPS;            // tokens per front-end warp
-__device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, int hk, int b,
-                                          int slot, unsigned char* sm, int tid, WarpSet& grp,
-                                          WarpSet& head4, uint64_t* bar, uint32_t ph, uint32_t tmem,
+__device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtensorMap* xmap,
+                                          int32_t gc, int hk, int b, int slot, unsigned char* sm,
+                                          int tid, WarpSet& grp, WarpSet& head4, uint64_t* bar,
+                                          uint32_t ph, uint64_t* xbar, uint32_t xph, uint32_t tmem,
                                           int next) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
@@ -375,8 +424,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
   // ---- front end: conv + SiLU + L2 norm; warp = (segment, TPW tokens), lane = 4 channels ----
+  if (!mbar_wait(xbar, xph, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   {
-    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* win =
         reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * cd;
     const int seg = warp / WPS;         // 0: q, 1: k, 2 / 3: v of value head 2 hk / 2 hk + 1
@@ -405,11 +454,14 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
       f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
       f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
     };
-    // Row rr of the chunk (rr < 0: the 3-token history), or zeros where masked.
+    // Row rr of the chunk (rr < 0: the 3-token history), or zeros where masked:
+    // from the x tile (row rr + 3), or for the history before the sequence's
+    // first token from the slot's window.
+    const uint32_t xrow = s_base + PrepSmem::XT + seg * PrepSmem::XT_SEG + 8 * lane;
     auto load_row = [&](int rr) -> uint2 {
       const int64_t p = (int64_t)c * C + rr;
       uint2 v = make_uint2(0, 0);
-      if (rr < L && p >= 0) v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + rr) * cd + ch));
+      if (rr < L && p >= 0) v = ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
       else if (rr < L && init) v = __ldg(reinterpret_cast<const uint2*>(win + (size_t)(3 + p) * cd + ch));
       return v;
     };
@@ -505,8 +557,12 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
     }
   }
   // The v warps (no norm) finish first: those of value head 2 hk prefetch the
-  // next item, two of those of value head 2 hk + 1 compute the gates.
-  if (next >= 0 && warp >= 2 * WPS && warp < 3 * WPS) prefetch_item(a, next, tid - 64 * WPS, 32 * WPS);
+  // next item's gates, two of those of value head 2 hk + 1 compute these.
+  if (next >= 0 && warp >= 2 * WPS && warp < 3 * WPS) {
+    const ItemPos np = item_pos(a, next);
+    prefetch_gates(a, np.t0, min(np.t0 + C, (int64_t)a.cu_seqlens[np.b + 1]), tid - 64 * WPS,
+                   32 * WPS);
+  }
   // ---- gates of the two value heads ----
   if (warp == 3 * WPS || warp == 3 * WPS + 1) {
     const int g = warp - 3 * WPS;
@@ -554,6 +610,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   tc_fence_before();
   if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
+  // every warp has read the x tile: the next item's rows may land in it
+  if (tid == 32 && next >= 0) issue_x_tile(a, xmap, next, s_base + PrepSmem::XT, xbar);
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
@@ -773,17 +831,24 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
   // made visible device-wide, generic stores fenced), then the ready flag with
   // release.  One gpu-scope fence after the group barrier covers every thread's
   // stores (cumulativity), so only thread 0 waits for them.
+  // Without a scan beside the prep nothing is published: the copies only have
+  // to finish reading shared memory before the next item rewrites it (the
+  // kernel waits for their writes before it exits).
   if (tid == 32) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
       bulk_s2g(vrec0 + g * VH_REC + UT_OFF, s_base + STG + 16384 * g, 16384);
       bulk_s2g(vrec0 + g * VH_REC + WK_OFF, s_base + STG + 32768 + 16384 * g, 16384);
     }
-    bulk_wait_all();
-    fence_proxy_async_global();
+    if (a.publish) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+    } else {
+      bulk_wait_read();
+    }
   }
   if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  if (tid == 0) {
+  if (a.publish && tid == 0) {
     __threadfence();
     st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
   }
@@ -791,15 +856,16 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, int32_t gc, i
 
 // Persistent prep: one CTA per SM, its 16 warps on one (chunk, key head) item
 // at a time.  It lets dependent grids (the scan) launch at once.
-constexpr uint32_t PREP_SMEM = (PrepSmem::SIZE + 1023) / 1024 * 1024;
+constexpr uint32_t PREP_SMEM = (PrepSmem::SIZE_X + 1023) / 1024 * 1024;
 
-__global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefillArgs a) {
+__global__ void __launch_bounds__(512, 1)
+    prep_persistent_kernel(const GdnPrefillArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_tmem;
-  // 2 MMA barriers, the 16-warp barrier, 2 head barriers
-  __shared__ __align__(8) uint64_t s_bar[5];
+  // 2 MMA barriers, the 16-warp barrier, 2 head barriers, the x tile
+  __shared__ __align__(8) uint64_t s_bar[6];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(&s_tmem, 256);
@@ -811,7 +877,9 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
     mbar_init(&s_bar[2], 16);
     mbar_init(&s_bar[3], 4);
     mbar_init(&s_bar[4], 4);
+    mbar_init(&s_bar[5], 1);
     fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -829,20 +897,24 @@ __global__ void __launch_bounds__(512, 1) prep_persistent_kernel(const GdnPrefil
   const int32_t nch = a.chunk_off[a.num_seqs];
   const int n_items = nch * a.h_k;
   const int n = (int)gridDim.x;
-  uint32_t ph = 0;
+  uint32_t ph = 0, xph = 0;
   // Static round-robin over the (chunk, key head) items in chunk-major order:
   // in round r, CTA i takes item r n + i, so each round finishes the earliest
-  // chunks first.
-  for (int item = (int)blockIdx.x; item < n_items; item += n) {
-    const int32_t gc = item / a.h_k;
-    const int hk = item % a.h_k;
-    const int b = find_seq(a.chunk_off, a.num_seqs, gc);
-    const int slot = a.slot_idx[b];
-    if (slot < 0 || slot >= a.num_slots) continue;  // the scan reports it and waits for nothing
-    const int next = item + n < n_items ? item + n : -1;
-    prep_item(a, gc, hk, b, slot, sm, tid, grp16, head4, s_bar, ph, s_tmem, next);
+  // chunks first.  Items of sequences with an invalid slot are skipped (the
+  // scan reports those and waits for nothing).
+  int item = next_valid_item(a, (int)blockIdx.x, n, n_items);
+  if (tid == 32 && item < n_items) issue_x_tile(a, &xmap, item, smem_u32(sm) + PrepSmem::XT, &s_bar[5]);
+  while (item < n_items) {
+    const int nxt = next_valid_item(a, item + n, n, n_items);
+    const ItemPos p = item_pos(a, item);
+    prep_item(a, &xmap, p.gc, p.hk, p.b, a.slot_idx[p.b], sm, tid, grp16, head4, s_bar, ph,
+              &s_bar[5], xph, s_tmem, nxt < n_items ? nxt : -1);
     ph ^= 1u;
+    xph ^= 1u;
+    item = nxt;
   }
+  // the last item's record copies are complete before the CTA exits
+  if (tid == 32) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(s_tmem, 256);
@@ -1005,7 +1077,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         const uint32_t rel = ((c >> 1) - 1) & 1;   // phase of the release two chunks back
         if (*s_abort) break;
         const uint32_t dst = s_base + s * ScanSmem::BUF;
-        {  // the chunk's records are published by the prep (possibly still running)
+        if (a.publish) {  // the chunk's records are published by the prep, still running
           const int32_t* fl = a.chunk_ready + (size_t)(gc0 + c) * a.h_k + hk;
           uint32_t it = 0;
           while (ld_acquire_gpu(fl) == 0 && ++it < FLAG_LIMIT) __nanosleep(64);
@@ -1349,9 +1421,44 @@ cudaError_t gdn_check_tc_records(const GdnPrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* tr) {
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of x [total_tokens][conv_dim] bf16 for the prep's tiles: boxes of
+// 128 channels x 67 rows, dense (no swizzle), zero fill outside the input.
+static cudaError_t make_x_map(const GdnPrefillArgs& a, CUtensorMap* map) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.conv_dim,
+                              (cuuint64_t)(a.total_tokens > 0 ? a.total_tokens : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.conv_dim * 2};
+  const cuuint32_t box[2] = {128, gdn::tcp::PrepSmem::XT_ROWS};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a_in, cudaStream_t s, gdn_trace* tr) {
   using namespace gdn::tcp;
   cudaError_t e = cudaSuccess;
+  GdnPrefillArgs a = a_in;
+  CUtensorMap xmap;
+  if ((e = make_x_map(a, &xmap)) != cudaSuccess) return e;
   int dev = 0, n_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -1361,6 +1468,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   // as they are published.  Otherwise the prep gets every SM first.
   const int64_t n_scan = (int64_t)a.num_seqs * a.h_v;
   const bool overlap = n_scan <= n_sm / 2;
+  a.publish = overlap ? 1 : 0;
   const int workers = overlap ? n_sm - (int)n_scan : n_sm;
   const int psmem = (int)PREP_SMEM + 1024;
   const int ssmem =
@@ -1392,7 +1500,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
 
   if (!overlap) {
     if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a, xmap)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
     if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
@@ -1402,7 +1510,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
   } else {
     // stage 2 covers prep and scan together: no event may sit between them
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a, xmap)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_seqs, a.h_v);

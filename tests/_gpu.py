@@ -9,7 +9,12 @@ state; per (row, value head) for decode):
   bf16 I/O:  |err| <= 2e-2 * max|ref|
 Scoping the scale to a block keeps a wrong short sequence or a strongly
 decayed head, whose values are small, from hiding under the batch's largest
-values.
+values.  One exception: the outputs of a sequence shorter than one chunk (64
+tokens) take the max over all of that sequence's heads.  There a head's
+output can be a handful of tokens of beta v (q.k) with q nearly orthogonal to
+k; the bf16 rounding of the normalised q and k (relative 2^-9 per element)
+then leaves an error of ~2^-9 |q||k| / sqrt(d_k) on a dot product that is
+itself much smaller, so the head's own max is no scale for it.
 Integer and byte results (which slots were written, untouched slots, the conv
 windows, which are raw copies of inputs) must match exactly.
 """
@@ -67,14 +72,24 @@ def assert_close_heads(got, ref, dims, what, head_axis):
     return float((err / np.where(scale > 0, scale, 1.0)).max())
 
 
+SHORT_SEQ = 64   # outputs of shorter sequences are scaled per sequence (see above)
+
+
+def assert_close_seq_out(got, ref, dims, what):
+    """One sequence's token-major outputs [T][h_v][d_v]: per value head, or
+    over all heads when the sequence is shorter than SHORT_SEQ tokens."""
+    if len(ref) < SHORT_SEQ:
+        return assert_close(got, ref, dims, what)
+    return assert_close_heads(got, ref, dims, what, head_axis=1)
+
+
 def assert_close_seqs(got, ref, cu, dims, what):
     """Token-major outputs [T][h_v][d_v] of a varlen batch, checked per
-    (sequence, value head)."""
+    (sequence, value head) (per sequence when it is short)."""
     worst = 0.0
     for s in range(len(cu) - 1):
         lo, hi = int(cu[s]), int(cu[s + 1])
-        worst = max(worst, assert_close_heads(got[lo:hi], ref[lo:hi], dims, f"{what} seq {s}",
-                                              head_axis=1))
+        worst = max(worst, assert_close_seq_out(got[lo:hi], ref[lo:hi], dims, f"{what} seq {s}"))
     return worst
 
 
@@ -145,8 +160,8 @@ def check_prefill(inp, got, ref, head_mask=None):
     if head_mask is None:
         for s in range(B):
             lo, hi = cu[s], cu[s + 1]
-            worst = max(worst, assert_close_heads(got["o"][lo:hi], ref["o"][lo:hi], d,
-                                                  f"o seq {s}", head_axis=1))
+            worst = max(worst, assert_close_seq_out(got["o"][lo:hi], ref["o"][lo:hi], d,
+                                                    f"o seq {s}"))
             worst = max(worst, assert_close_heads(got["state_pool"][inp["slot_idx"][s]],
                                                   ref["state"][s], d, f"state seq {s}",
                                                   head_axis=0))
