@@ -101,6 +101,19 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, __nv_bfloat16 v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<uint16_t*>(&v))
+               : "memory");
+}
+// Named barrier among `n` threads (whole, converged warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
@@ -323,7 +336,11 @@ struct PrepSmem {
   static constexpr uint32_t XT_ROWS = 67;
   static constexpr uint32_t XT_SEG = 17408;                   // 67 x 256 bytes, rounded to 1 KiB
   static constexpr uint32_t XT_BYTES = 4 * XT_ROWS * 256;     // transaction bytes per item
-  static constexpr uint32_t SIZE_X = XT + 4 * XT_SEG;
+  static constexpr uint32_t SIZE_X0 = XT + 4 * XT_SEG;
+  // B operands of the second MMAs: BU_0 | BU_1 | [BW_0; BW_1], bf16 tiles
+  // (K-major; the blocks above the diagonal are zeroed once per kernel)
+  static constexpr uint32_t BT = SIZE_X0;
+  static constexpr uint32_t SIZE_X = BT + 32768;
   static constexpr int AST = 68;             // fp32 row stride of A and T
   static constexpr int THREADS = 256;
 };
@@ -402,12 +419,16 @@ __device__ __forceinline__ void issue_x_tile(const GdnPrefillArgs& a, const CUte
 // warps 0..7 only.
 constexpr int NW = 16;
 constexpr int WPS = NW / 4;             // warps per front-end segment
+// The thread that issues the item's record copies (a v warp's: the v warps
+// finish the front end first) and, in the next item, waits for them to have
+// read shared memory before anyone writes tiles there again.
+constexpr int CP_TID = 2 * WPS * 32;
 constexpr int TPW = C / WPS;            // tokens per front-end warp
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtensorMap* xmap,
                                           int32_t gc, int hk, int b, int slot, unsigned char* sm,
                                           int tid, WarpSet& grp, WarpSet& head4, uint64_t* bar,
                                           uint32_t ph, uint64_t* xbar, uint32_t xph, uint32_t tmem,
-                                          int next) {
+                                          int next, uint64_t* stg_free) {
   const int c = gc - a.chunk_off[b];
   const int64_t start = a.cu_seqlens[b];
   const int64_t Tb = a.cu_seqlens[b + 1] - start;
@@ -480,6 +501,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     for (int i = 0; i < 4; ++i) cur[i] = load_row(r0 + i);
 #pragma unroll 1
     for (int hh = 0; hh < TPW / 4; ++hh) {
+      if (hh == 0) {
+        // the previous item's record copies have read the shared memory this
+        // item's tiles go to (signalled by the thread that issued them)
+        if (tid == CP_TID) {
+          bulk_wait_read();
+          mbar_arrive(stg_free);
+        }
+        if (!mbar_wait(stg_free, xph, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+      }
       const int rb = r0 + 4 * hh;
       uint2 nxt[4];
 #pragma unroll
@@ -671,20 +701,45 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   tc_fence_before();
   if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  // ---- T = (I + A)^-1 in place, per value head: warps 0..3 and 4..7 ----
-  // With 16 x 16 blocks b: T_bb = (I + A_bb)^-1 by forward substitution (fp32),
-  // then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then the lower-left
-  // 32 x 32 block -T_[23][23] A_[23][01] T_[01][01] (products on the tensor
-  // cores in TF32).  Only products of exact blocks, no matrix powers: finite
-  // for fully correlated keys.
-  float tv[4][8];   // this thread's T entries for the B operands (read before they are overwritten)
-  if (warp < 8) {
-    const int g = warp >> 2, gt = tid & 127, wb = warp & 3;
+  // ---- T = (I + A)^-1 per value head g on warps 8 g .. 8 g + 7, and the B operands ----
+  // With 16 x 16 blocks: D_i = (I + A_ii)^-1 by forward substitution (fp32),
+  // then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then the lower-left
+  // 32 x 32 block -T_[23][23] R with R = A_[23][01] T_[01][01] (products on the
+  // tensor cores in TF32).  Only products of exact blocks, no matrix powers:
+  // finite for fully correlated keys.  T overwrites A block by block; each
+  // block's producer also writes its entries of the second MMAs' bf16 B
+  // operands BU_g = T diag(beta) and BW_g = T diag(beta e^gamma) (the blocks
+  // above the diagonal stay zero from the kernel's start).  The stages of a
+  // head meet at its own named barrier.
+  {
+    const int g = warp >> 3, wl = warp & 7;
+    const uint32_t hbar = 1 + g;
     float* AT = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH);
     constexpr int RS = PrepSmem::RST;
     float* Rt = reinterpret_cast<float*>(sm + PrepSmem::R) + g * (4 * 16 * RS);
-    {  // diagonal block wb: lane j (< 16) computes column j
-      const int o = 16 * wb, j = lane & 15;
+    const float* bt = beta + g * 64;
+    const float* et = eg + g * 64;
+    const uint32_t bu = s_base + PrepSmem::BT + 8192 * g;   // BU_g: K-major, 64 rows
+    const uint32_t bw = s_base + PrepSmem::BT + 16384;      // [BW_0; BW_1]: K-major, 128 rows
+    // B entries of -(16 x 16 fragment d) at block (bi, bj)
+    auto put_frag = [&](int bi, int bj, const float (&d)[2][4]) {
+      const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * bj + 8 * nt + 2 * tig;
+        const float b0 = bt[c], b1 = bt[c + 1];
+        const float w0 = b0 * et[c], w1 = b1 * et[c + 1];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * bi + gid + 8 * hh;
+          const float t0 = -d[nt][2 * hh], t1 = -d[nt][2 * hh + 1];
+          st_shared_b32(bu + kmaj_off(64, r, c), pack_bf16(t0 * b0, t1 * b1));
+          st_shared_b32(bw + kmaj_off(128, 64 * g + r, c), pack_bf16(t0 * w0, t1 * w1));
+        }
+      }
+    };
+    if (wl < 4) {  // D_wl: lane j (< 16) solves column j
+      const int o = 16 * wl, j = lane & 15;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
@@ -694,21 +749,29 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           const float4 f = *reinterpret_cast<const float4*>(AT + (o + r) * S + o + 4 * q);
           arow[4 * q] = f.x; arow[4 * q + 1] = f.y; arow[4 * q + 2] = f.z; arow[4 * q + 3] = f.w;
         }
-        float acc = 0.f;
+        float acc0 = 0.f, acc1 = 0.f;   // two chains: half the dependent latency
 #pragma unroll
-        for (int s2 = 0; s2 < r; ++s2) acc = fmaf(arow[s2], x[s2], acc);
-        x[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
+        for (int s2 = 0; s2 < r; ++s2) {
+          if (s2 & 1) acc1 = fmaf(arow[s2], x[s2], acc1);
+          else acc0 = fmaf(arow[s2], x[s2], acc0);
+        }
+        x[r] = r < j ? 0.f : (r == j ? 1.f : -(acc0 + acc1));
       }
       __syncwarp();
       if (lane < 16) {
+        const float b0 = bt[o + j], w0 = b0 * et[o + j];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) AT[(o + r) * S + o + j] = x[r];
+        for (int r = 0; r < 16; ++r) {
+          AT[(o + r) * S + o + j] = x[r];
+          st_shared_b16(bu + kmaj_off(64, o + r, o + j), __float2bfloat16_rn(x[r] * b0));
+          st_shared_b16(bw + kmaj_off(128, 64 * g + o + r, o + j), __float2bfloat16_rn(x[r] * w0));
+        }
       }
     }
-    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-    if (wb < 2) {  // T_10 (warp 0) and T_32 (warp 1)
-      const int i = 1 + 2 * wb;   // block row; column block i - 1
-      float* Rw = Rt + wb * 16 * RS;
+    named_bar_sync(hbar, 256);
+    if (wl < 2) {  // T_10 (wl 0) and T_32 (wl 1)
+      const int i = 1 + 2 * wl;   // block row; column block i - 1
+      float* Rw = Rt + wl * 16 * RS;
       float d[2][4] = {};
       mma16x16(d, AT + 16 * i * S + 16 * (i - 1), S, AT + 16 * (i - 1) * S + 16 * (i - 1), S, lane);
       store16x16(Rw, RS, d, 1.f, lane);
@@ -716,53 +779,22 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       float e[2][4] = {};
       mma16x16(e, AT + 16 * i * S + 16 * i, S, Rw, RS, lane);
       store16x16(AT + 16 * i * S + 16 * (i - 1), S, e, -1.f, lane);
+      put_frag(i, i - 1, e);
     }
-    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-    const int bi = 2 + (wb >> 1), bj = wb & 1;   // this warp's block of the lower-left 32 x 32
-    {  // R_ij = A_i0 T_0j + A_i1 T_1j  (T_01 = 0)
+    named_bar_sync(hbar, 256);
+    const int bi = 2 + (wl >> 1), bj = wl & 1;   // this warp's block of the lower-left 32 x 32
+    if (wl < 4) {  // R_ij = A_i0 T_0j + A_i1 T_1j  (T_01 = 0)
       float d[2][4] = {};
       if (bj == 0) mma16x16(d, AT + 16 * bi * S, S, AT, S, lane);
       mma16x16(d, AT + 16 * bi * S + 16, S, AT + 16 * S + 16 * bj, S, lane);
-      store16x16(Rt + wb * 16 * RS, RS, d, 1.f, lane);
+      store16x16(Rt + wl * 16 * RS, RS, d, 1.f, lane);
     }
-    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-    {  // T_ij = -(sum_{k = 2..i} T_ik R_kj)
+    named_bar_sync(hbar, 256);
+    if (wl < 4) {  // T_ij = -(sum_{k = 2..i} T_ik R_kj): only its B entries are needed
       float d[2][4] = {};
       if (bi == 3) mma16x16(d, AT + 48 * S + 32, S, Rt + bj * 16 * RS, RS, lane);
       mma16x16(d, AT + 16 * bi * S + 16 * bi, S, Rt + ((bi - 2) * 2 + bj) * 16 * RS, RS, lane);
-      store16x16(AT + 16 * bi * S + 16 * bj, S, d, -1.f, lane);
-    }
-    if (!warpset_sync(head4, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = gt + 128 * q;
-      const int r = chunk >> 3, s0 = 8 * (chunk & 7);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) tv[q][k] = (s0 + k) <= r ? AT[r * S + s0 + k] : 0.f;
-    }
-  }
-  // both heads' T read: the B-operand tiles overwrite the whole region
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  if (warp < 8) {
-    const int g = warp >> 2, gt = tid & 127;
-    const uint32_t bu = s_base + PrepSmem::AT + 8192 * g;
-    const uint32_t bw = s_base + PrepSmem::AT + 16384 + 8192 * g;  // rows 64g.. of [BW_0; BW_1]
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = gt + 128 * q;
-      const int r = chunk >> 3, s0 = 8 * (chunk & 7);
-      float vu[8], vw[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        vu[k] = tv[q][k] * beta[g * 64 + s0 + k];
-        vw[k] = vu[k] * eg[g * 64 + s0 + k];
-      }
-      st_shared_v4(bu + kmaj_off(64, r, s0),
-                   make_uint4(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]),
-                              pack_bf16(vu[4], vu[5]), pack_bf16(vu[6], vu[7])));
-      st_shared_v4(bw + kmaj_off(64, r, s0),
-                   make_uint4(pack_bf16(vw[0], vw[1]), pack_bf16(vw[2], vw[3]),
-                              pack_bf16(vw[4], vw[5]), pack_bf16(vw[6], vw[7])));
+      put_frag(bi, bj, d);
     }
   }
   fence_async_smem();
@@ -774,15 +806,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     for (int g = 0; g < 2; ++g)
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
-                 sdesc_kmaj(s_base + PrepSmem::AT + 8192 * g, 64, ks),
+                 sdesc_kmaj(s_base + PrepSmem::BT + 8192 * g, 64, ks),
                  idesc_bf16(128, 64, true, false), ks > 0);
     for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
-      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::AT + 16384, 128, ks),
+      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BT + 16384, 128, ks),
                sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 128, false, true),
                ks > 0);
     mma_commit(&bar[1]);
   }
-  if (tid == 32) {  // Q rows then K rows of the [K;Q] tile (tile images) to the workspace
+  if (tid == CP_TID) {  // Q rows then K rows of the [K;Q] tile (tile images) to the workspace
     unsigned char* qrec = a.kq_ws + ((size_t)gc * a.h_k + hk) * Q_REC;
     bulk_s2g(qrec, s_base + PrepSmem::KQ + 8192, 8192);
     bulk_s2g(qrec + 8192, s_base + PrepSmem::KQ + 16384 + 8192, 8192);
@@ -791,7 +823,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
   // Staged as the records' tile images in shared memory that the second MMAs
-  // have finished reading (V and A/T), then written as four 16 KB bulk copies.
+  // have finished reading (V, and A/T, dead since the inverse), then written
+  // as four 16 KB bulk copies.  The next item waits for the copies to have
+  // read the staging area only where it first writes its own tiles there.
   constexpr uint32_t STG = PrepSmem::V;   // U^T_0 | U^T_1 | Wk_0 | Wk_1, 16 KB each
   {
     const bool ok = mbar_wait(&bar[1], ph, WAIT_LIMIT);
@@ -800,8 +834,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
     // 16 tasks of (lane quarter, 64 columns), one per warp
     if (ok) {
-      const int task = warp;
-      const int kind = task >> 2;                // 0,1: U^T_g   2,3: Wk column halves
+      const int kind = warp >> 2;                // 0,1: U^T_g   2,3: Wk column halves
       const uint32_t col = 64 * kind;
       uint32_t tile;
       int row, R, c0;
@@ -827,30 +860,30 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   fence_async_smem();
   tc_fence_before();
   if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  // Publish the item: every record byte written (bulk stores completed and
-  // made visible device-wide, generic stores fenced), then the ready flag with
-  // release.  One gpu-scope fence after the group barrier covers every thread's
-  // stores (cumulativity), so only thread 0 waits for them.
-  // Without a scan beside the prep nothing is published: the copies only have
-  // to finish reading shared memory before the next item rewrites it (the
-  // kernel waits for their writes before it exits).
-  if (tid == 32) {
+  if (tid == CP_TID) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
       bulk_s2g(vrec0 + g * VH_REC + UT_OFF, s_base + STG + 16384 * g, 16384);
       bulk_s2g(vrec0 + g * VH_REC + WK_OFF, s_base + STG + 32768 + 16384 * g, 16384);
     }
-    if (a.publish) {
+  }
+  // Publish the item when the scan runs beside the prep: every record byte
+  // written (bulk stores completed and made visible device-wide, generic
+  // stores fenced), then the ready flag with release.  One gpu-scope fence
+  // after the group barrier covers every thread's stores (cumulativity), so
+  // only thread 0 waits for them.  Without a scan beside the prep nothing is
+  // published and the next item starts at once (the kernel waits for the
+  // copies' writes before it exits).
+  if (a.publish) {
+    if (tid == CP_TID) {
       bulk_wait_all();
       fence_proxy_async_global();
-    } else {
-      bulk_wait_read();
     }
-  }
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-  if (a.publish && tid == 0) {
-    __threadfence();
-    st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
+    if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+    if (tid == 0) {
+      __threadfence();
+      st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
+    }
   }
 }
 
@@ -864,8 +897,9 @@ __global__ void __launch_bounds__(512, 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_tmem;
-  // 2 MMA barriers, the 16-warp barrier, 2 head barriers, the x tile
-  __shared__ __align__(8) uint64_t s_bar[6];
+  // 2 MMA barriers, the 16-warp barrier, 2 head barriers, the x tile, the
+  // staging area
+  __shared__ __align__(8) uint64_t s_bar[7];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(&s_tmem, 256);
@@ -878,9 +912,13 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&s_bar[3], 4);
     mbar_init(&s_bar[4], 4);
     mbar_init(&s_bar[5], 1);
+    mbar_init(&s_bar[6], 1);   // the staging area is free (once per item)
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   }
+  // the B operand tiles start at zero: their blocks above the diagonal stay so
+  for (uint32_t o = 16u * tid; o < 32768u; o += 16u * 512u)
+    *reinterpret_cast<uint4*>(sm + PrepSmem::BT + o) = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -908,13 +946,13 @@ __global__ void __launch_bounds__(512, 1)
     const int nxt = next_valid_item(a, item + n, n, n_items);
     const ItemPos p = item_pos(a, item);
     prep_item(a, &xmap, p.gc, p.hk, p.b, a.slot_idx[p.b], sm, tid, grp16, head4, s_bar, ph,
-              &s_bar[5], xph, s_tmem, nxt < n_items ? nxt : -1);
+              &s_bar[5], xph, s_tmem, nxt < n_items ? nxt : -1, &s_bar[6]);
     ph ^= 1u;
     xph ^= 1u;
     item = nxt;
   }
   // the last item's record copies are complete before the CTA exits
-  if (tid == 32) bulk_wait_all();
+  if (tid == CP_TID) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(s_tmem, 256);

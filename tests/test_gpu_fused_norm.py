@@ -1,11 +1,18 @@
 """GPU parity of the layer with the gated RMSNorm of its output
 (gdn_prefill_gated_norm, gdn_decode_step_gated_norm, called through the C ABI)
-against the float64 oracle: the oracle's layer output o, then the oracle's
-gated RMSNorm of it, within the stated tolerances of tests/_gpu.py.  The
-states and windows these calls leave are bit for bit those of the plain
+against the float64 oracle, within the stated tolerances of tests/_gpu.py.
+The states and windows these calls leave are bit for bit those of the plain
 calls, since the norm touches only the output; the tensor-core and SIMT
 prefill paths (varlen, mixed initial states) and the decode step, whose
-epilogue computes the norm itself, with padding rows, are covered."""
+epilogue computes the norm itself, with padding rows, are covered.
+
+Prefill is checked stage by stage: the plain call's o against the oracle's
+layer, and the fused call's y against the oracle's norm of that same o.  The
+norm rescales every (token, head) row to unit RMS, so a row whose bf16 output
+is a small difference (the first tokens of a sequence, q nearly orthogonal to
+k) carries the layer's rounding into y at full scale; comparing y with the
+oracle's norm of the oracle's o would test that rounding a second time.  The
+decode step works in fp32 throughout and is compared end to end."""
 import numpy as np
 import pytest
 import torch
@@ -15,8 +22,7 @@ import oracle
 from gated_deltanet_linear_07_gb300 import workloads
 from gated_deltanet_linear_07_gb300.workloads import QWEN35_4B, TINY, Dims
 from tests._gpu import (DecodeRun, PrefillRun, assert_close, assert_close_rows, assert_close_seqs,
-                        dev, io_dtype, oracle_decode,
-                        oracle_prefill)
+                        check_prefill, dev, io_dtype, oracle_decode, oracle_prefill)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,8 +63,8 @@ def test_fused_prefill_matches_oracle(gpu_lib, name):
     np.testing.assert_array_equal(got["state_pool"], base["state_pool"])
     np.testing.assert_array_equal(got["conv_pool"], base["conv_pool"])
     np.testing.assert_array_equal(dz.float().cpu().numpy(), z)          # z is not touched
-    ref_o = oracle_prefill(inp)["o"]
-    ref = oracle.gated_rmsnorm(ref_o, z, w, eps=1e-6)
+    check_prefill(inp, base, oracle_prefill(inp))        # the layer
+    ref = oracle.gated_rmsnorm(base["o"], z, w, eps=1e-6)  # the norm of its o
     worst = assert_close_seqs(got["o"], ref, inp["cu_seqlens"], d, f"{name} y")
     print(f"fused prefill {name}: worst normalised error {worst:.3e}")
 
@@ -70,6 +76,9 @@ def test_fused_prefill_qwen35_4b_full_size_sampled(gpu_lib):
     d = inp["dims"]
     T = inp["x"].shape[0]
     z, w = _gate_inputs(d, T, seed=62)
+    plain = PrefillRun(inp)
+    plain()
+    base = plain.results()
     run = PrefillRun(inp)
     gdn.gdn_prefill_gated_norm(d, run.cw, run.A_log, run.dt_bias, run.x, run.a, run.b, run.cu,
                                run.slot, run.init, run.state, run.conv, dev(z, torch.bfloat16),
@@ -84,7 +93,8 @@ def test_fused_prefill_qwen35_4b_full_size_sampled(gpu_lib):
     for s in range(len(inp["lengths"])):
         for h in heads:
             lo, hi = cu[s], cu[s + 1]
-            y = oracle.gated_rmsnorm(ref["o"][lo:hi, h], z[lo:hi, h], w)
+            assert_close(base["o"][lo:hi, h], ref["o"][lo:hi, h], d, f"o seq {s} head {h}")
+            y = oracle.gated_rmsnorm(base["o"][lo:hi, h], z[lo:hi, h], w)
             assert_close(got["o"][lo:hi, h], y, d, f"y seq {s} head {h}")
 
 
