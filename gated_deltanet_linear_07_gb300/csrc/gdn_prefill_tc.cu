@@ -33,6 +33,7 @@
 // Every mbarrier wait is bounded; on timeout the kernel sets
 // GDN_DEV_WAIT_TIMEOUT, skips the dependent work and still frees its TMEM.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "gdn_check.cuh"
@@ -69,16 +70,18 @@ __device__ __forceinline__ float silu_fast(float z) {
   return 0.5f * z * (1.0f + t);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+// The tensor-core operands of both kernels are fp16 (10-bit mantissa, range
+// +-65504): the state is multiplied by rounded factors every chunk, and
+// fp16 keeps that rounding 8x below bf16's.
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-
-__device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
-  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+__device__ __forceinline__ void f16x8_to_float(const uint4& u, float (&f)[8]) {
+  const __half2* p = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float2 t = __bfloat1622float2(p[i]);
+    const float2 t = __half22float2(p[i]);
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
   }
@@ -104,7 +107,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void st_shared_b16(uint32_t addr, __nv_bfloat16 v) {
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, __half v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<uint16_t*>(&v))
                : "memory");
 }
@@ -563,8 +566,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           // token i's value sits in lane 8 i; rows past the chunk end get 0
           const float inv = r < L ? __shfl_sync(0xffffffffu, invl, 8 * i) : 0.f;
           const float2 inv2 = make_float2(inv, inv);
-          const __nv_bfloat162 v0 = __float22bfloat162_rn(__fmul2_rn(y[i][0], inv2));
-          const __nv_bfloat162 v1 = __float22bfloat162_rn(__fmul2_rn(y[i][1], inv2));
+          const __half2 v0 = __float22half2_rn(__fmul2_rn(y[i][0], inv2));
+          const __half2 v1 = __float22half2_rn(__fmul2_rn(y[i][1], inv2));
           const int row = seg == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
           st_shared_v2(s_base + PrepSmem::KQ + kmaj_off(128, row, 4 * lane),
                        make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
@@ -574,8 +577,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = rb + i;
-          const __nv_bfloat162 v0 = __float22bfloat162_rn(y[i][0]);
-          const __nv_bfloat162 v1 = __float22bfloat162_rn(y[i][1]);
+          const __half2 v0 = __float22half2_rn(y[i][0]);
+          const __half2 v1 = __float22half2_rn(y[i][1]);
           const uint2 val = r < L ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
                                                *reinterpret_cast<const uint32_t*>(&v1))
                                   : make_uint2(0, 0);
@@ -645,7 +648,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
-               sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 64, false, false),
+               sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 64, false, false),
                ks > 0);
     mma_commit(&bar[0]);
   }
@@ -693,8 +696,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
             pv[e] = s2 <= r ? fast_exp2(gr - gm[s2]) * d[8 * ck + e] : 0.f;
           }
           *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * hf + 8 * ck)) =
-              make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                         pack_bf16(pv[6], pv[7]));
+              make_uint4(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]), pack_f16(pv[4], pv[5]),
+                         pack_f16(pv[6], pv[7]));
         }
       }
     }
@@ -733,8 +736,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
         for (int hh = 0; hh < 2; ++hh) {
           const int r = 16 * bi + gid + 8 * hh;
           const float t0 = -d[nt][2 * hh], t1 = -d[nt][2 * hh + 1];
-          st_shared_b32(bu + kmaj_off(64, r, c), pack_bf16(t0 * b0, t1 * b1));
-          st_shared_b32(bw + kmaj_off(128, 64 * g + r, c), pack_bf16(t0 * w0, t1 * w1));
+          st_shared_b32(bu + kmaj_off(64, r, c), pack_f16(t0 * b0, t1 * b1));
+          st_shared_b32(bw + kmaj_off(128, 64 * g + r, c), pack_f16(t0 * w0, t1 * w1));
         }
       }
     };
@@ -763,8 +766,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           AT[(o + r) * S + o + j] = x[r];
-          st_shared_b16(bu + kmaj_off(64, o + r, o + j), __float2bfloat16_rn(x[r] * b0));
-          st_shared_b16(bw + kmaj_off(128, 64 * g + o + r, o + j), __float2bfloat16_rn(x[r] * w0));
+          st_shared_b16(bu + kmaj_off(64, o + r, o + j), __float2half_rn(x[r] * b0));
+          st_shared_b16(bw + kmaj_off(128, 64 * g + o + r, o + j), __float2half_rn(x[r] * w0));
         }
       }
     }
@@ -807,10 +810,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
                  sdesc_kmaj(s_base + PrepSmem::BT + 8192 * g, 64, ks),
-                 idesc_bf16(128, 64, true, false), ks > 0);
+                 idesc_f16(128, 64, true, false), ks > 0);
     for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
       mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BT + 16384, 128, ks),
-               sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_bf16(128, 128, false, true),
+               sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, true),
                ks > 0);
     mma_commit(&bar[1]);
   }
@@ -851,8 +854,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
         for (int ck = 0; ck < 4; ++ck) {
           const float* f = &v[8 * ck];
           st_shared_v4(s_base + tile + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck),
-                       make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                                  pack_bf16(f[6], f[7])));
+                       make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
+                                  pack_f16(f[6], f[7])));
         }
       }
     }
@@ -1142,9 +1145,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t ID_XO = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t ID_DH = idesc_bf16(128, 128, false, true);
-      constexpr uint32_t ID_O2 = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t ID_XO = idesc_f16(128, 64, false, false);
+      constexpr uint32_t ID_DH = idesc_f16(128, 128, false, true);
+      constexpr uint32_t ID_O2 = idesc_f16(128, 64, false, false);
       bool ck_reading = false;   // a checkpoint copy may still be reading the staging area
       int ck_next = ck_every - 1;           // chunk after which the next checkpoint falls
       int64_t ck_slot = ck_base;            // and its slot
@@ -1227,7 +1230,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     {
       uint32_t hp[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) hp[e] = pack_bf16(H[2 * e], H[2 * e + 1]);
+      for (int e = 0; e < 16; ++e) hp[e] = pack_f16(H[2 * e], H[2 * e + 1]);
       tmem_st16(t_ht, hp);
     }
     // warp 2 certifies, through its hready arrivals, what the MMA issuer would
@@ -1263,12 +1266,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           float u[8];
-          bf16x8_to_float(q == 0 ? ut0 : ut1, u);
+          f16x8_to_float(q == 0 ? ut0 : ut1, u);
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const float w0 = u[e] - X[8 * q + e], w1 = u[e + 1] - X[8 * q + e + 1];
-            wp[4 * q + e / 2] = pack_bf16(w0, w1);
-            wtp[4 * q + e / 2] = pack_bf16(w0 * edv[8 * q + e], w1 * edv[8 * q + e + 1]);
+            wp[4 * q + e / 2] = pack_f16(w0, w1);
+            wtp[4 * q + e / 2] = pack_f16(w0 * edv[8 * q + e], w1 * edv[8 * q + e + 1]);
           }
         }
         tmem_st8(t_wt, wtp);
@@ -1308,7 +1311,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       {
         uint32_t hp[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) hp[e] = pack_bf16(H[2 * e], H[2 * e + 1]);
+        for (int e = 0; e < 16; ++e) hp[e] = pack_f16(H[2 * e], H[2 * e + 1]);
         tmem_st16(t_ht, hp);
       }
       if (ckpt_on && (c + 1) % ck_every == 0 && c + 1 < nch) {   // stage it, [i][j] as in the pool
@@ -1428,21 +1431,21 @@ __global__ void __launch_bounds__(256) check_records_kernel(const GdnPrefillArgs
   }
   const int slot = a.slot_idx[lo];
   if (slot < 0 || slot >= a.num_slots) return;
-  auto bf16_bad = [](const unsigned char* p, int n, int tid, int nt) {
+  auto f16_bad = [](const unsigned char* p, int n, int tid, int nt) {   // fp16 Inf / NaN
     const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
     bool bad = false;
-    for (int e = tid; e < n; e += nt) bad |= (q[e] & 0x7f80u) == 0x7f80u;
+    for (int e = tid; e < n; e += nt) bad |= (q[e] & 0x7c00u) == 0x7c00u;
     return bad;
   };
   const int tid = threadIdx.x, nt = blockDim.x;
   bool bad;
   if (y < a.h_k) {
-    bad = bf16_bad(a.kq_ws + ((size_t)gc * a.h_k + y) * Q_REC, Q_REC / 2, tid, nt);
+    bad = f16_bad(a.kq_ws + ((size_t)gc * a.h_k + y) * Q_REC, Q_REC / 2, tid, nt);
   } else {
     const unsigned char* rec = a.vh_ws + ((size_t)gc * a.h_v + (y - a.h_k)) * VH_REC;
-    bad = bf16_bad(rec + P_OFF, (UT_OFF - P_OFF) / 2, tid, nt) ||
-          bf16_bad(rec + UT_OFF, (EXP_OFF - UT_OFF) / 2, tid, nt) ||
-          bf16_bad(rec + WK_OFF, (VH_REC - WK_OFF) / 2, tid, nt);
+    bad = f16_bad(rec + P_OFF, (UT_OFF - P_OFF) / 2, tid, nt) ||
+          f16_bad(rec + UT_OFF, (EXP_OFF - UT_OFF) / 2, tid, nt) ||
+          f16_bad(rec + WK_OFF, (VH_REC - WK_OFF) / 2, tid, nt);
     const uint32_t* ex = reinterpret_cast<const uint32_t*>(rec + EXP_OFF);
     for (int e = tid; e < 2 * C + 1; e += nt) bad |= (ex[e] & 0x7f800000u) == 0x7f800000u;
   }

@@ -88,10 +88,14 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * GDN_FP32_STATE: prefill keeps every product with the fp32 state in fp32
  *   arithmetic (the SIMT path, any supported shape and chunk).  Without it the
  *   tensor-core path, where it applies (d_k = d_v = 128, chunk 64, bf16 I/O,
- *   h_v = 2 h_k), feeds the state to the MMAs rounded to bf16 (its products
- *   accumulate in fp32); the error that rounding leaves in the state and in o
- *   is measured against the fp32 option on long, correlated-key sequences by
- *   the precision tests.  Decode always uses fp32 state products. */
+ *   h_v = 2 h_k), feeds the state and every other MMA operand to the tensor
+ *   cores rounded to fp16 (10-bit mantissa; products accumulate in fp32), so
+ *   its operands must stay within fp16 range (|value| < 65504: normalised
+ *   q, k, the gates' factors, v = SiLU(conv(x)) and the state, all far below
+ *   that for realistic activations); the error that rounding leaves in the
+ *   state and in o is measured against the fp32 option on long,
+ *   correlated-key sequences by the precision tests.  Decode always uses
+ *   fp32 state products. */
 #define GDN_FP32_STATE 0x1
 /* GDN_CHECK_FINITE: after a prefill call (any prefill entry point) the library
  *   scans what each stage wrote -- its workspace records or rows, the output,

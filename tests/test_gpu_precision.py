@@ -1,7 +1,8 @@
 """State-operand precision: the prefill with GDN_FP32_STATE (every product with
 the fp32 state in fp32, the SIMT path) against the float64 oracle, and the
-ablation of that option against the tensor-core path (the state fed to the
-MMAs as bf16) on the adversarial long-sequence workload.
+ablation of that option against the tensor-core path (the state and the
+other MMA operands fed to the tensor cores as fp16) on the adversarial
+long-sequence workload.
 
 The fp32-state prefill is held to the fp32 tolerance of tests/_gpu.py on its
 final states (|err| <= 1e-3 max|ref| + 1e-5) even with bf16 I/O; its outputs,
@@ -76,7 +77,7 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
                        window0=ov["window0"], state0=ov["state0"], head_mask=mask,
                        n_threads=NCPU)
     errs = {}
-    for name, d in (("tensor-core, bf16 state operands", QWEN35_4B),
+    for name, d in (("tensor-core, fp16 operands", QWEN35_4B),
                     ("fp32 state, chunk 64", FP32_STATE),
                     ("fp32 state, chunk 32", dataclasses.replace(FP32_STATE, chunk=32))):
         inp = _with_dims(base, d)
@@ -91,6 +92,6 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
         del run
     for name, (eo, es) in errs.items():
         print(f"adversarial {sub}: {name:34s} worst normalised error o {eo:.2e} state {es:.2e}")
-    tc = errs["tensor-core, bf16 state operands"][1]
+    tc = errs["tensor-core, fp16 operands"][1]
     assert errs["fp32 state, chunk 64"][1] < tc
     assert errs["fp32 state, chunk 32"][1] < tc
