@@ -30,7 +30,7 @@ int check_dims(const gdn_dims* d) {
   if (!d) return GDN_EINVAL;
   if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0) return GDN_EINVAL;
   if (!(d->l2_eps >= 0.0f)) return GDN_EINVAL;
-  if (d->flags & ~(GDN_FP32_STATE | GDN_CHECK_FINITE)) return GDN_EINVAL;
+  if (d->flags & ~(GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT)) return GDN_EINVAL;
   if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
   if (d->conv_w != 4) return GDN_EUNSUPPORTED;
   if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
@@ -221,6 +221,11 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   p.conv_weight = params->conv_weight; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
   p.state_pool = state_pool; p.conv_pool = conv_pool; p.o = o; p.d_status = d_status;
   p.ckpt_every_chunks = ckpt_every_chunks; p.ckpt_slot = ckpt_slot;
+  // Waits between CTAs and warps give up after 4 s (a chunk takes microseconds);
+  // the test knob shortens that to 2 ms and withholds one chunk's flag.
+  const bool test_timeout = (dims->flags & GDN_TEST_WAIT_TIMEOUT) != 0;
+  p.wait_ns = test_timeout ? 2000000ull : 4000000000ull;
+  p.withhold_last_chunk = test_timeout ? 1 : 0;
   char* ws = reinterpret_cast<char*>(workspace);
   p.ws_flag = reinterpret_cast<int32_t*>(ws + L.flag);
   p.ws_q = reinterpret_cast<float*>(ws + L.q);

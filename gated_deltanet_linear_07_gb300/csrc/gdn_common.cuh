@@ -139,6 +139,11 @@ struct GdnPrefillArgs {
   // 1: the scan runs beside the prep and waits for each chunk's ready flag;
   // 0: the scan starts after the prep kernel has finished (no flags needed)
   int32_t publish;
+  // every inter-CTA or inter-warp wait gives up after this many nanoseconds
+  uint64_t wait_ns;
+  // GDN_TEST_WAIT_TIMEOUT: the prep does not publish the last chunk of
+  // sequence 0, key head 0 (the scan's wait for it runs out)
+  int32_t withhold_last_chunk;
   // interval checkpoints (0 / null: none): every ckpt_every_chunks chunks strictly
   // inside sequence b, the state and window go to slot ckpt_slot[b] + k - 1
   int32_t ckpt_every_chunks;

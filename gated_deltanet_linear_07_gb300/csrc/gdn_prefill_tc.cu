@@ -58,9 +58,6 @@ constexpr uint32_t K_IN_QREC = 64 * 128 * 2;
 constexpr uint32_t P_OFF = 0, UT_OFF = 8192, EXP_OFF = 24576, WK_OFF = 25600;
 constexpr uint32_t VH_REC = 41984;           // per (chunk, value head)
 constexpr uint32_t VH_HEAD = 25600;          // P | UT | EXP, copied in one piece
-constexpr uint32_t WAIT_LIMIT = 1u << 22;   // suspending try_wait iterations
-constexpr uint32_t SPIN_LIMIT = 1u << 26;   // non-blocking test_wait iterations
-constexpr uint32_t FLAG_LIMIT = 1u << 25;   // polls of a global ready flag (64 ns apart)
 constexpr float LOG2E = 1.4426950408889634f;
 
 __device__ __forceinline__ float silu_fast(float z) {
@@ -155,20 +152,12 @@ struct WarpSet {
   uint32_t bar;     // shared-memory address of the mbarrier
   uint32_t phase;
 };
-__device__ __forceinline__ bool warpset_sync(WarpSet& w, int lane) {
+__device__ __forceinline__ bool warpset_sync(WarpSet& w, int lane, uint64_t budget_ns) {
   __syncwarp();
   if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(w.bar) : "memory");
-  uint32_t ok = 0;
-  for (uint32_t i = 0; i < WAIT_LIMIT && !ok; ++i)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(w.bar), "r"(w.phase)
-        : "memory");
+  const bool ok = mbar_wait_addr(w.bar, w.phase, budget_ns);
   w.phase ^= 1u;
-  return ok != 0;
+  return ok;
 }
 
 // Bulk async copies (no tensor map): global -> shared with mbarrier
@@ -448,7 +437,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
   // ---- front end: conv + SiLU + L2 norm; warp = (segment, TPW tokens), lane = 4 channels ----
-  if (!mbar_wait(xbar, xph, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!mbar_wait(xbar, xph, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   {
     const __nv_bfloat16* win =
         reinterpret_cast<const __nv_bfloat16*>(a.conv_pool) + (size_t)slot * 3 * cd;
@@ -511,7 +500,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           bulk_wait_read();
           mbar_arrive(stg_free);
         }
-        if (!mbar_wait(stg_free, xph, WAIT_LIMIT)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+        if (!mbar_wait(stg_free, xph, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
       }
       const int rb = r0 + 4 * hh;
       uint2 nxt[4];
@@ -641,7 +630,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   fence_async_smem();
   tc_fence_before();
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   // every warp has read the x tile: the next item's rows may land in it
   if (tid == 32 && next >= 0) issue_x_tile(a, xmap, next, s_base + PrepSmem::XT, xbar);
@@ -657,7 +646,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   {
     const int q = warp & 3, g = (warp >> 2) & 1;
     const int m = 32 * q + lane;
-    const bool ok = mbar_wait(&bar[0], ph, WAIT_LIMIT);
+    const bool ok = mbar_wait(&bar[0], ph, a.wait_ns);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const float* gm = gam + g * 64;
@@ -703,7 +692,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     }
   }
   tc_fence_before();
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   // ---- T = (I + A)^-1 per value head g on warps 8 g .. 8 g + 7, and the B operands ----
   // With 16 x 16 blocks: D_i = (I + A_ii)^-1 by forward substitution (fp32),
   // then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then the lower-left
@@ -802,7 +791,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   fence_async_smem();
   tc_fence_before();
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   if (tid == 0) {
 #pragma unroll
@@ -831,7 +820,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   // read the staging area only where it first writes its own tiles there.
   constexpr uint32_t STG = PrepSmem::V;   // U^T_0 | U^T_1 | Wk_0 | Wk_1, 16 KB each
   {
-    const bool ok = mbar_wait(&bar[1], ph, WAIT_LIMIT);
+    const bool ok = mbar_wait(&bar[1], ph, a.wait_ns);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
     const int m = 32 * (warp & 3) + lane;        // TMEM lane of this thread
@@ -862,7 +851,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   fence_async_smem();
   tc_fence_before();
-  if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+  if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   if (tid == CP_TID) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
@@ -882,8 +871,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       bulk_wait_all();
       fence_proxy_async_global();
     }
-    if (!warpset_sync(grp, lane)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
-    if (tid == 0) {
+    if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+    // (GDN_TEST_WAIT_TIMEOUT: the last chunk of sequence 0, key head 0 stays unpublished)
+    const bool withheld = a.withhold_last_chunk && b == 0 && hk == 0 && gc == a.chunk_off[1] - 1;
+    if (tid == 0 && !withheld) {
       __threadfence();
       st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
     }
@@ -1120,24 +1111,30 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         const uint32_t dst = s_base + s * ScanSmem::BUF;
         if (a.publish) {  // the chunk's records are published by the prep, still running
           const int32_t* fl = a.chunk_ready + (size_t)(gc0 + c) * a.h_k + hk;
-          uint32_t it = 0;
-          while (ld_acquire_gpu(fl) == 0 && ++it < FLAG_LIMIT) __nanosleep(64);
-          if (it >= FLAG_LIMIT) { fail(); break; }
+          bool late = false;
+          if (ld_acquire_gpu(fl) == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(fl) == 0) {
+              __nanosleep(64);
+              if (globaltimer_ns() - t0 > a.wait_ns) { late = true; break; }
+            }
+          }
+          if (late) { fail(); break; }
           fence_proxy_async_global();
         }
         const unsigned char* vrec = a.vh_ws + ((size_t)(gc0 + c) * a.h_v + h) * VH_REC;
         const unsigned char* qrec = a.kq_ws + ((size_t)(gc0 + c) * a.h_k + hk) * Q_REC;
-        if (c >= 2 && !mbar_wait(&empty_b1[s], rel, WAIT_LIMIT)) { fail(); break; }
+        if (c >= 2 && !mbar_wait(&empty_b1[s], rel, a.wait_ns)) { fail(); break; }
         mbar_expect_tx(&full_b1[s], ScanSmem::BUF - ScanSmem::REST);
         bulk_g2s(dst + ScanSmem::B_B1, vrec + WK_OFF, 8192, &full_b1[s]);          // Wk K-block 0
         bulk_g2s(dst + ScanSmem::B_B1 + 16384, vrec + WK_OFF + 8192, 8192, &full_b1[s]);  // 1
         bulk_g2s(dst + ScanSmem::B_B1 + 8192, qrec, 8192, &full_b1[s]);            // Q K-block 0
         bulk_g2s(dst + ScanSmem::B_B1 + 24576, qrec + 8192, 8192, &full_b1[s]);    // block 1
-        if (c >= 2 && !mbar_wait(&empty[s], rel, WAIT_LIMIT)) { fail(); break; }
+        if (c >= 2 && !mbar_wait(&empty[s], rel, a.wait_ns)) { fail(); break; }
         mbar_expect_tx(&full[s], ScanSmem::REST);
         bulk_g2s(dst, vrec, VH_HEAD, &full[s]);                                   // P|UT|EXP
         bulk_g2s(dst + ScanSmem::B_K, qrec + K_IN_QREC, K_IN_QREC, &full[s]);      // K
-        if (c >= 2 && !mbar_wait(&ofree[s], rel, WAIT_LIMIT)) { fail(); break; }
+        if (c >= 2 && !mbar_wait(&ofree[s], rel, a.wait_ns)) { fail(); break; }
         mbar_expect_tx(&full_eg[s], 256);
         bulk_g2s(s_base + ScanSmem::EG + 256 * s, vrec + EXP_OFF, 256, &full_eg[s]);
       }
@@ -1162,7 +1159,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         // other warps are busy, so the chain warps certify the rest.  hready (from
         // chain warp 2) also means that [Wk; Q] of this chunk has landed and that
         // O1's buffer has been read; wready that P | U | EXP | K has landed.
-        if (!mbar_spin(hready, c & 1, SPIN_LIMIT)) { fail(); break; }
+        if (!mbar_spin(hready, c & 1, a.wait_ns)) { fail(); break; }
         tc_fence_after();
         if (ckpt_on && c - 1 == ck_next) {   // the checkpoint after chunk c - 1 (c < nch)
           if (ck_slot >= a.num_slots) {
@@ -1187,7 +1184,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
           mma_bf16_ts(tmem + TO1 + 64 * s, tmem + THT + 8 * ks,
                       sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(&empty_b1[s]);
-        if (!mbar_spin(wready, c & 1, SPIN_LIMIT)) { fail(); break; }
+        if (!mbar_spin(wready, c & 1, a.wait_ns)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
@@ -1200,7 +1197,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         }
         mma_commit(bar_dh);
         // O2 rewrites what the output warps read for the previous chunk
-        if (c >= 1 && !mbar_wait(&ofree[s ^ 1], ((c - 1) >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
+        if (c >= 1 && !mbar_wait(&ofree[s ^ 1], ((c - 1) >> 1) & 1, a.wait_ns)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
@@ -1235,7 +1232,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     }
     // warp 2 certifies, through its hready arrivals, what the MMA issuer would
     // otherwise wait for: the next chunk's [Wk; Q] landed, its O1 buffer read
-    if (warp == 2 && nch > 0 && !mbar_wait(&full_b1[0], 0, WAIT_LIMIT)) fail();
+    if (warp == 2 && nch > 0 && !mbar_wait(&full_b1[0], 0, a.wait_ns)) fail();
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -1245,12 +1242,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       const int s = c & 1;
       const uint32_t buf = s_base + s * ScanSmem::BUF;
       const uint32_t ex = buf + ScanSmem::B_EXP;   // e^{gamma} [64] | e^{gamma_C - gamma} [64] | e^{gamma_C}
-      if (!mbar_wait(&full[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
+      if (!mbar_wait(&full[s], (c >> 1) & 1, a.wait_ns)) { fail(); break; }
       // U and the decay are loaded while X is computed (the decay factors per row
       // after X: holding them across the wait costs registers).
       const uint4 ut0 = ld_shared_v4(buf + a_ut0), ut1 = ld_shared_v4(buf + (a_ut0 ^ 16u));
       const float dec = ld_shared_f32(ex + 4 * 128);
-      if (!mbar_wait(bar_x, c & 1, WAIT_LIMIT)) { fail(); break; }
+      if (!mbar_wait(bar_x, c & 1, a.wait_ns)) { fail(); break; }
       tc_fence_after();
       // W^T = U^T - X for r in this group's quarter, and Wt^T = W^T diag(e^{gamma_C - gamma})
       {
@@ -1286,14 +1283,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       }
       if (warp == 2 && c + 1 < nch) {   // idle until dH: certify the next chunk's inputs
         const int s1 = (c + 1) & 1;
-        if (!mbar_wait(&full_b1[s1], ((c + 1) >> 1) & 1, WAIT_LIMIT) ||
-            (c + 1 >= 2 && !mbar_wait(&ofree[s1], (((c + 1) >> 1) - 1) & 1, WAIT_LIMIT))) {
+        if (!mbar_wait(&full_b1[s1], ((c + 1) >> 1) & 1, a.wait_ns) ||
+            (c + 1 >= 2 && !mbar_wait(&ofree[s1], (((c + 1) >> 1) - 1) & 1, a.wait_ns))) {
           fail();
           break;
         }
       }
 
-      if (!mbar_wait(bar_dh, c & 1, WAIT_LIMIT)) { fail(); break; }
+      if (!mbar_wait(bar_dh, c & 1, a.wait_ns)) { fail(); break; }
       tc_fence_after();
       // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
       {
@@ -1347,8 +1344,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       const int s = c & 1;
       const uint32_t ex = s_base + ScanSmem::EG + 256 * s;   // e^{gamma} [64]
       const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
-      if (!mbar_wait(&full_eg[s], (c >> 1) & 1, WAIT_LIMIT) ||
-          !mbar_wait(&bar_o[s], (c >> 1) & 1, WAIT_LIMIT)) { fail(); break; }
+      if (!mbar_wait(&full_eg[s], (c >> 1) & 1, a.wait_ns) ||
+          !mbar_wait(&bar_o[s], (c >> 1) & 1, a.wait_ns)) { fail(); break; }
       tc_fence_after();
 #pragma unroll 1
       for (int g = 0; g < C / 16; ++g) {
@@ -1509,6 +1506,8 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a_in, cudaStream_t s, gd
   // as they are published.  Otherwise the prep gets every SM first.
   const int64_t n_scan = (int64_t)a.num_seqs * a.h_v;
   const bool overlap = n_scan <= n_sm / 2;
+  // (GDN_TEST_WAIT_TIMEOUT withholds a published flag: only where flags exist)
+  if (!overlap) a.withhold_last_chunk = 0;
   a.publish = overlap ? 1 : 0;
   const int workers = overlap ? n_sm - (int)n_scan : n_sm;
   const int psmem = (int)PREP_SMEM + 1024;

@@ -98,12 +98,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false when the limit runs out (the caller records the timeout and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+// Nanoseconds of the global timer.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// try_wait with a suspend-time hint: the thread may sleep until the phase
+// completes or hint_ns pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar_addr, uint32_t parity,
+                                                  uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t SUSPEND_HINT_NS = 200000;   // longest single sleep of a waiting thread
+// Wait for the phase with the given parity to complete, for at most budget_ns
+// of global time after the first unsuccessful test.  Returns false when the
+// budget runs out (the caller records the timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait_addr(uint32_t bar_addr, uint32_t parity,
+                                               uint64_t budget_ns) {
+  if (mbar_try_wait_for(bar_addr, parity, SUSPEND_HINT_NS)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_for(bar_addr, parity, SUSPEND_HINT_NS))
+    if (globaltimer_ns() - t0 > budget_ns) return false;
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  return mbar_wait_addr(smem_u32(bar), parity, budget_ns);
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
@@ -117,12 +145,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded spin on the non-blocking test: for hand-offs on the critical path,
-// where a suspended try_wait resumes too late.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
+// Spin on the non-blocking test, for hand-offs on the critical path where a
+// suspended try_wait resumes too late; the global timer is read every 256
+// tests and the spin gives up after budget_ns.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_test_wait(bar, parity)) return true;
-  return false;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > budget_ns) return false;
+  }
 }
 
 // Descriptor of the same tile `bytes` further on (the start-address field is

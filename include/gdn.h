@@ -106,6 +106,17 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
  *   (a few extra launches).  Requires d_status (null: GDN_EINVAL).  Decode
  *   ignores it. */
 #define GDN_CHECK_FINITE 0x2
+/* GDN_TEST_WAIT_TIMEOUT (test only): exercises the bounded waits of the
+ *   tensor-core prefill.  Every wait between CTAs and warps, bounded in global
+ *   time (%globaltimer) at 4 s otherwise, gives up after 2 ms, and the prep
+ *   kernel does not publish the last chunk of sequence 0 for key head 0, so
+ *   the scan CTAs of value heads 0 and 1 of sequence 0 time out waiting for
+ *   it: they set GDN_DEV_WAIT_TIMEOUT, skip their remaining work (those
+ *   heads' outputs and final states are not valid), free their tensor memory
+ *   and return; the GPU context stays usable.  It takes effect only where the
+ *   scan runs beside the prep (at most half as many (sequence, value head)
+ *   chains as SMs); elsewhere it is ignored, as it is by the SIMT path. */
+#define GDN_TEST_WAIT_TIMEOUT 0x4
 
 typedef struct {
   int32_t h_k;     /* key/query heads */
@@ -116,7 +127,8 @@ typedef struct {
   int32_t chunk;   /* prefill chunk length: 16, 32 or 64 */
   int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
   float l2_eps;    /* added to the sum of squares inside the L2-norm root */
-  int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE, or 0; other bits: GDN_EINVAL */
+  int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT, or 0;
+                      other bits: GDN_EINVAL */
 } gdn_dims;
 
 typedef struct {
