@@ -319,7 +319,11 @@ struct PrepSmem {
   static constexpr uint32_t GAM = R + 2 * 4 * 16 * RST * 4;   // fp32 [2][64], log2 units
   static constexpr uint32_t BETA = GAM + 512;                 // fp32 [2][64]
   static constexpr uint32_t EG = BETA + 512;                  // fp32 [2][64], e^{gamma}
-  static constexpr uint32_t BAR = EG + 512;                   // 2 mbarriers + tmem address
+  static constexpr uint32_t DD = EG + 512;                    // fp32 [2][64], e^{gamma_C - gamma}
+  // fp32 [128] L2-norm factors (keys 0..63: 1/|k_r|, queries 64..127:
+  // d_k^-1/2 / |q_r|), then [2] e^{gamma_C} of the two heads
+  static constexpr uint32_t NRM = DD + 512;
+  static constexpr uint32_t BAR = NRM + 1024;                 // 2 mbarriers + tmem address
   static constexpr uint32_t SIZE = BAR + 64;
   // The item's x rows, brought in by TMA one item ahead: for each of the four
   // 128-channel segments (q, k, v of value head 2 hk, v of 2 hk + 1) the rows
@@ -433,10 +437,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   float* gam = reinterpret_cast<float*>(sm + PrepSmem::GAM);
   float* beta = reinterpret_cast<float*>(sm + PrepSmem::BETA);
   float* eg = reinterpret_cast<float*>(sm + PrepSmem::EG);
+  float* dd = reinterpret_cast<float*>(sm + PrepSmem::DD);
+  float* nrm = reinterpret_cast<float*>(sm + PrepSmem::NRM);
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
-  // ---- front end: conv + SiLU + L2 norm; warp = (segment, TPW tokens), lane = 4 channels ----
+  // ---- front end: conv + SiLU; warp = (segment, TPW tokens), lane = 4 channels ----
+  // q and k go into the [K;Q] tile as they are: their L2 norms come from the
+  // diagonal of the Gram matrix the first MMA computes, and the factors
+  // 1/|q_r|, 1/|k_s| are applied where the products are used.
   if (!mbar_wait(xbar, xph, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   {
     const __nv_bfloat16* win =
@@ -461,26 +470,35 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       w2[2][p2] = make_float2(f0.z, f1.z);
       w2[3][p2] = make_float2(f0.w, f1.w);
     }
-    const float scale = seg == 0 ? rsqrtf((float)D) : 1.0f;
     const float2 half2 = make_float2(0.5f, 0.5f);
     auto unpack = [](const uint2& u, float2 (&f)[2]) {
       f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
       f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
     };
-    // Row rr of the chunk (rr < 0: the 3-token history), or zeros where masked:
-    // from the x tile (row rr + 3), or for the history before the sequence's
-    // first token from the slot's window.
+    // This lane's 8 bytes of chunk row r in its tile: q / k rows of the K-major
+    // [K;Q] tile (rows 64.. queries, 0.. keys), v the MN-major V tile (token r
+    // as the K index); in both the 16-byte piece index is XOR-ed with r % 8.
+    const uint32_t tile = seg < 2 ? s_base + PrepSmem::KQ + (lane >> 4) * 16384u +
+                                        (seg == 0 ? 64u * 128u : 0u)
+                                  : s_base + PrepSmem::V + (seg - 2) * 16384u + (lane >> 4) * 8192u;
+    const uint32_t cidx = (uint32_t)(lane & 15) >> 1;
+    const uint32_t obase = tile + (uint32_t)r0 * 128u + 8u * (uint32_t)(lane & 1);
+    auto out_addr = [&](int i) {   // token r0 + i (r0 is a multiple of 16: r % 8 = i % 8)
+      return obase + (uint32_t)i * 128u + ((cidx ^ (uint32_t)(i & 7)) << 4);
+    };
+    // Rows rr = r0 - 3 .. r0 + TPW - 1 of the chunk: from the x tile (row rr + 3);
+    // in a sequence's first chunk the history before its first token comes from
+    // the slot's window (or zeros), and rows past the chunk's end are zeros.
     const uint32_t xrow = s_base + PrepSmem::XT + seg * PrepSmem::XT_SEG + 8 * lane;
+    const bool interior = c > 0 && L == C;   // every row from the tile
     auto load_row = [&](int rr) -> uint2 {
+      if (interior) return ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
       const int64_t p = (int64_t)c * C + rr;
       uint2 v = make_uint2(0, 0);
       if (rr < L && p >= 0) v = ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
       else if (rr < L && init) v = __ldg(reinterpret_cast<const uint2*>(win + (size_t)(3 + p) * cd + ch));
       return v;
     };
-    // Each row is loaded once: the rolling window carries the last three rows
-    // from one 4-token step to the next, and the next step's 4 rows are in
-    // flight while the current ones are computed.
     float2 xf[4][2];
     {
       const uint2 h0 = load_row(r0 - 3), h1 = load_row(r0 - 2), h2 = load_row(r0 - 1);
@@ -491,7 +509,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     uint2 cur[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = load_row(r0 + i);
-#pragma unroll 1
+#pragma unroll
     for (int hh = 0; hh < TPW / 4; ++hh) {
       if (hh == 0) {
         // the previous item's record copies have read the shared memory this
@@ -506,7 +524,6 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       uint2 nxt[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) nxt[i] = hh < TPW / 4 - 1 ? load_row(rb + 4 + i) : make_uint2(0, 0);
-      float2 y[4][2];   // SiLU(conv) of the step's 4 tokens, channel pairs
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -515,6 +532,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           xf[q][1] = xf[q + 1][1];
         }
         unpack(cur[i], xf[3]);
+        float2 y[2];   // SiLU(conv) of token rb + i, channel pairs
 #pragma unroll
         for (int p2 = 0; p2 < 2; ++p2) {
           float2 z = __fmul2_rn(w2[0][p2], xf[0][p2]);
@@ -526,53 +544,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           float2 t;
           asm("tanh.approx.f32 %0, %1;" : "=f"(t.x) : "f"(h2.x));
           asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
-          y[i][p2] = __ffma2_rn(h2, t, h2);
+          y[p2] = __ffma2_rn(h2, t, h2);
         }
-      }
-      if (seg < 2) {
-        // Squared norms of the 4 tokens over the warp's 32 lanes with 6
-        // exchanges instead of 20: at xor 16 and xor 8 each lane hands over the
-        // tokens its partner keeps, so afterwards lane l holds token
-        // 2 (l >> 4 & 1) + (l >> 3 & 1); three more levels finish that sum.
-        float ps[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 s2 = __ffma2_rn(y[i][1], y[i][1], __fmul2_rn(y[i][0], y[i][0]));
-          ps[i] = s2.x + s2.y;
-        }
-        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
-        const float g0 = __shfl_xor_sync(0xffffffffu, b4 ? ps[0] : ps[2], 16);
-        const float g1 = __shfl_xor_sync(0xffffffffu, b4 ? ps[1] : ps[3], 16);
-        const float q0 = (b4 ? ps[2] : ps[0]) + g0;   // token 2 b4
-        const float q1 = (b4 ? ps[3] : ps[1]) + g1;   // token 2 b4 + 1
-        float tot = (b3 ? q1 : q0) + __shfl_xor_sync(0xffffffffu, b3 ? q0 : q1, 8);
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        const float invl = rsqrtf(tot + a.l2_eps) * scale;   // this lane's token
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = rb + i;
-          // token i's value sits in lane 8 i; rows past the chunk end get 0
-          const float inv = r < L ? __shfl_sync(0xffffffffu, invl, 8 * i) : 0.f;
-          const float2 inv2 = make_float2(inv, inv);
-          const __half2 v0 = __float22half2_rn(__fmul2_rn(y[i][0], inv2));
-          const __half2 v1 = __float22half2_rn(__fmul2_rn(y[i][1], inv2));
-          const int row = seg == 0 ? 64 + r : r;   // rows 0..63 keys, 64..127 queries
-          st_shared_v2(s_base + PrepSmem::KQ + kmaj_off(128, row, 4 * lane),
-                       make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
-                                  *reinterpret_cast<const uint32_t*>(&v1)));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = rb + i;
-          const __half2 v0 = __float22half2_rn(y[i][0]);
-          const __half2 v1 = __float22half2_rn(y[i][1]);
-          const uint2 val = r < L ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
-                                               *reinterpret_cast<const uint32_t*>(&v1))
-                                  : make_uint2(0, 0);
-          st_shared_v2(s_base + PrepSmem::V + (seg - 2) * 16384 + mnmaj_off(64, 4 * lane, r), val);
-        }
+        const __half2 v0 = __float22half2_rn(y[0]);
+        const __half2 v1 = __float22half2_rn(y[1]);
+        const uint2 val = interior || rb + i < L
+                              ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
+                                           *reinterpret_cast<const uint32_t*>(&v1))
+                              : make_uint2(0, 0);
+        st_shared_v2(out_addr(4 * hh + i), val);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
@@ -621,12 +601,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     beta[g * 64 + 2 * lane + 1] = be[1];
     eg[g * 64 + 2 * lane] = e0;
     eg[g * 64 + 2 * lane + 1] = e1;
-    float* rec = reinterpret_cast<float*>(vrec0 + g * VH_REC + EXP_OFF);
-    rec[2 * lane] = e0;
-    rec[2 * lane + 1] = e1;
-    rec[64 + 2 * lane] = d0;
-    rec[64 + 2 * lane + 1] = d1;
-    if (lane == 0) rec[128] = fast_exp2(glast);
+    dd[g * 64 + 2 * lane] = d0;
+    dd[g * 64 + 2 * lane + 1] = d1;
+    if (lane == 0) nrm[128 + g] = fast_exp2(glast);
   }
   fence_async_smem();
   tc_fence_before();
@@ -635,11 +612,41 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   // every warp has read the x tile: the next item's rows may land in it
   if (tid == 32 && next >= 0) issue_x_tile(a, xmap, next, s_base + PrepSmem::XT, xbar);
   if (tid == 0) {
-    for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] K^T -> TMEM columns [0, 64)
+    for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] [K;Q]^T -> TMEM columns [0, 128)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
-               sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 64, false, false),
+               sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, false),
                ks > 0);
     mma_commit(&bar[0]);
+  }
+  // ---- L2 norms from the diagonal of D1 (warps 0..3: lane m holds row m) ----
+  // n_m = (|x_m|^2 + eps)^-1/2 (x = k_m for m < 64, q_{m-64} scaled by d_k^-1/2
+  // otherwise); the records' decay factors take them along: e^{gamma_r} / |q_r|
+  // scales the scan's Q-side product, e^{gamma_C - gamma_r} / |k_r| its K side.
+  {
+    const bool ok = mbar_wait(&bar[0], ph, a.wait_ns);
+    if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+    tc_fence_after();
+    if (warp < 4) {
+      const int m = 32 * warp + lane;
+      float d[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * warp, d);   // column m is d[lane]
+      float dg = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dg = e == lane ? d[e] : dg;
+      const float nf = rsqrtf(dg + a.l2_eps) * (m >= 64 ? rsqrtf((float)D) : 1.0f);
+      nrm[m] = nf;
+      const int r = m & 63;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        float* rec = reinterpret_cast<float*>(vrec0 + g * VH_REC + EXP_OFF);
+        if (m >= 64) rec[r] = eg[g * 64 + r] * nf;
+        else rec[64 + r] = dd[g * 64 + r] * nf;
+        if (m == 0) rec[128] = nrm[128 + g];
+      }
+    }
+    tc_fence_before();
+    if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
+    tc_fence_after();
   }
   // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); warp = (32-column
   //      half, head, lanes) ----
@@ -652,7 +659,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     const float* gm = gam + g * 64;
     const int r = m & 63;
     const float gr = gm[r];
-    const float br = beta[g * 64 + r];
+    const float nr = nrm[m];   // 1/|k_r| (A rows) or d_k^-1/2 / |q_r| (P rows)
+    const float br = beta[g * 64 + r] * nr;
     float* Arow = reinterpret_cast<float*>(sm + PrepSmem::AT + g * PrepSmem::AH) + r * S;
     unsigned char* ptile = vrec0 + g * VH_REC + P_OFF;
     {
@@ -671,7 +679,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int s2 = 32 * hf + 4 * c4 + e;
-            av[e] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[4 * c4 + e] : 0.f;
+            av[e] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[4 * c4 + e] * nrm[s2] : 0.f;
           }
           *reinterpret_cast<float4*>(Arow + 32 * hf + 4 * c4) = make_float4(av[0], av[1], av[2], av[3]);
         }
@@ -682,7 +690,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int s2 = 32 * hf + 8 * ck + e;
-            pv[e] = s2 <= r ? fast_exp2(gr - gm[s2]) * d[8 * ck + e] : 0.f;
+            pv[e] = s2 <= r ? nr * fast_exp2(gr - gm[s2]) * d[8 * ck + e] * nrm[s2] : 0.f;
           }
           *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * hf + 8 * ck)) =
               make_uint4(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]), pack_f16(pv[4], pv[5]),
@@ -720,7 +728,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       for (int nt = 0; nt < 2; ++nt) {
         const int c = 16 * bj + 8 * nt + 2 * tig;
         const float b0 = bt[c], b1 = bt[c + 1];
-        const float w0 = b0 * et[c], w1 = b1 * et[c + 1];
+        const float w0 = b0 * et[c] * nrm[c], w1 = b1 * et[c + 1] * nrm[c + 1];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int r = 16 * bi + gid + 8 * hh;
@@ -751,7 +759,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       }
       __syncwarp();
       if (lane < 16) {
-        const float b0 = bt[o + j], w0 = b0 * et[o + j];
+        const float b0 = bt[o + j], w0 = b0 * et[o + j] * nrm[o + j];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           AT[(o + r) * S + o + j] = x[r];

@@ -80,7 +80,7 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_DEV_BAD_CU_SEQLENS 0x2  /* cu_seqlens not 0..total_tokens non-decreasing: call skipped */
 #define GDN_DEV_WAIT_TIMEOUT 0x4    /* an inter-CTA wait gave up: results invalid */
 /* With GDN_CHECK_FINITE (prefill): a NaN or Inf among what the stage wrote. */
-#define GDN_DEV_NONFINITE_FRONTEND 0x8  /* normalised q, k (and v, gates on the SIMT path) */
+#define GDN_DEV_NONFINITE_FRONTEND 0x8  /* the front end's q, k (and v, gates on the SIMT path) */
 #define GDN_DEV_NONFINITE_CHUNK 0x10    /* the chunk factors: P, U, Wk, decays */
 #define GDN_DEV_NONFINITE_OUT 0x20      /* the layer output o (y) or a final state */
 
