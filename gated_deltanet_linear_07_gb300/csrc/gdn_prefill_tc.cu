@@ -263,36 +263,33 @@ __global__ void __launch_bounds__(1024) setup_kernel(const GdnPrefillArgs a) {
 // ---------------------------------------------------------------------------
 // prep: persistent CTAs (512 threads), one (chunk, key head) item at a time.
 
-// Warp-level TF32 tensor-core product for the 16 x 16 blocks of the chunk
-// inverse: fragments of mma.m16n8k8 (row.col), fp32 accumulate.
-__device__ __forceinline__ uint32_t f2tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+// Warp-level tensor-core product for the 16 x 16 blocks of the chunk inverse:
+// fp16 operands (the same 10-bit mantissa as TF32, half the instructions:
+// one m16n8k16 step covers K = 16), fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              const uint32_t (&b)[2]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 // d (16 x 16, as two 16 x 8 accumulator fragments) += P Q for 16 x 16 fp32
-// blocks P (row stride sp) and Q (row stride sq) in shared memory.
+// blocks P (row stride sp, even) and Q (row stride sq) in shared memory.
 __device__ __forceinline__ void mma16x16(float (&d)[2][4], const float* P, int sp, const float* Q,
                                          int sq, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
+  auto pk = [](float2 v) { return pack_f16(v.x, v.y); };
+  const uint32_t a[4] = {pk(*reinterpret_cast<const float2*>(P + gid * sp + 2 * tig)),
+                         pk(*reinterpret_cast<const float2*>(P + (gid + 8) * sp + 2 * tig)),
+                         pk(*reinterpret_cast<const float2*>(P + gid * sp + 2 * tig + 8)),
+                         pk(*reinterpret_cast<const float2*>(P + (gid + 8) * sp + 2 * tig + 8))};
 #pragma unroll
-  for (int kt = 0; kt < 2; ++kt) {
-    const uint32_t a[4] = {f2tf32(P[gid * sp + 8 * kt + tig]), f2tf32(P[(gid + 8) * sp + 8 * kt + tig]),
-                           f2tf32(P[gid * sp + 8 * kt + tig + 4]),
-                           f2tf32(P[(gid + 8) * sp + 8 * kt + tig + 4])};
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const uint32_t b[2] = {f2tf32(Q[(8 * kt + tig) * sq + 8 * nt + gid]),
-                             f2tf32(Q[(8 * kt + tig + 4) * sq + 8 * nt + gid])};
-      mma_tf32(d[nt], a, b);
-    }
+  for (int nt = 0; nt < 2; ++nt) {
+    const float* q = Q + 8 * nt + gid;
+    const uint32_t b[2] = {pack_f16(q[(2 * tig) * sq], q[(2 * tig + 1) * sq]),
+                           pack_f16(q[(2 * tig + 8) * sq], q[(2 * tig + 9) * sq])};
+    mma_f16_16816(d[nt], a, b);
   }
 }
 // Store sign * d into a 16 x 16 fp32 block (row stride st).
@@ -442,6 +439,23 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   const uint32_t s_base = smem_u32(sm);
   unsigned char* vrec0 = a.vh_ws + ((size_t)gc * a.h_v + 2 * hk) * VH_REC;
 
+  // The gate warps load a and b of the two value heads now and use them after
+  // the front end, so that the loads' latency hides behind it.
+  const bool gate_warp = warp == 3 * WPS || warp == 3 * WPS + 1;
+  uint32_t gab[2] = {0u, 0u};   // (a, b) of tokens 2 lane + k, bf16 pairs
+  if (gate_warp) {
+    const int h = 2 * hk + warp - 3 * WPS;
+    const uint16_t* av = reinterpret_cast<const uint16_t*>(a.a);
+    const uint16_t* bv = reinterpret_cast<const uint16_t*>(a.b);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = 2 * lane + k;
+      if (r < L) {
+        const size_t idx = (size_t)(t0 + r) * a.h_v + h;
+        gab[k] = (uint32_t)__ldg(av + idx) | ((uint32_t)__ldg(bv + idx) << 16);
+      }
+    }
+  }
   // ---- front end: conv + SiLU; warp = (segment, TPW tokens), lane = 4 channels ----
   // q and k go into the [K;Q] tile as they are: their L2 norms come from the
   // diagonal of the Gram matrix the first MMA computes, and the factors
@@ -566,19 +580,16 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
                    32 * WPS);
   }
   // ---- gates of the two value heads ----
-  if (warp == 3 * WPS || warp == 3 * WPS + 1) {
+  if (gate_warp) {
     const int g = warp - 3 * WPS;
     const int h = 2 * hk + g;
-    const __nv_bfloat16* av = reinterpret_cast<const __nv_bfloat16*>(a.a);
-    const __nv_bfloat16* bv = reinterpret_cast<const __nv_bfloat16*>(a.b);
     float gv[2], be[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int r = 2 * lane + k;
       if (r < L) {
-        const size_t idx = (size_t)(t0 + r) * a.h_v + h;
-        gv[k] = gate_g(__bfloat162float(av[idx]), a.A_log[h], a.dt_bias[h]);
-        be[k] = sigmoidf_(__bfloat162float(bv[idx]));
+        gv[k] = gate_g(__uint_as_float(gab[k] << 16), a.A_log[h], a.dt_bias[h]);
+        be[k] = sigmoidf_(__uint_as_float(gab[k] & 0xffff0000u));
       } else {
         gv[k] = 0.f;
         be[k] = 0.f;
@@ -672,25 +683,36 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
         for (int e = 0; e < 32; ++e) d[e] = 0.f;
       }
+      // the column factors gamma_s and 1/|k_s|, four at a time (float4 broadcasts)
+      auto col4 = [&](int c, float (&g4)[4], float (&n4)[4]) {
+        const float4 gq = *reinterpret_cast<const float4*>(gm + 32 * hf + c);
+        const float4 nq = *reinterpret_cast<const float4*>(nrm + 32 * hf + c);
+        g4[0] = gq.x; g4[1] = gq.y; g4[2] = gq.z; g4[3] = gq.w;
+        n4[0] = nq.x; n4[1] = nq.y; n4[2] = nq.z; n4[3] = nq.w;
+      };
       if (m < 64) {   // A[r][s] = beta_r e^{gamma_r - gamma_s} (k_r . k_s), s < r
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          float av[4];
+          float av[4], g4[4], n4[4];
+          col4(4 * c4, g4, n4);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int s2 = 32 * hf + 4 * c4 + e;
-            av[e] = s2 < r ? br * fast_exp2(gr - gm[s2]) * d[4 * c4 + e] * nrm[s2] : 0.f;
+            av[e] = s2 < r ? br * fast_exp2(gr - g4[e]) * d[4 * c4 + e] * n4[e] : 0.f;
           }
           *reinterpret_cast<float4*>(Arow + 32 * hf + 4 * c4) = make_float4(av[0], av[1], av[2], av[3]);
         }
       } else {        // P[r][s] = e^{gamma_r - gamma_s} (q_r . k_s), s <= r
 #pragma unroll
         for (int ck = 0; ck < 4; ++ck) {
-          float pv[8];
+          float pv[8], g4[2][4], n4[2][4];
+          col4(8 * ck, g4[0], n4[0]);
+          col4(8 * ck + 4, g4[1], n4[1]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int s2 = 32 * hf + 8 * ck + e;
-            pv[e] = s2 <= r ? nr * fast_exp2(gr - gm[s2]) * d[8 * ck + e] * nrm[s2] : 0.f;
+            pv[e] = s2 <= r ? nr * fast_exp2(gr - g4[e >> 2][e & 3]) * d[8 * ck + e] * n4[e >> 2][e & 3]
+                            : 0.f;
           }
           *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * hf + 8 * ck)) =
               make_uint4(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]), pack_f16(pv[4], pv[5]),
