@@ -67,6 +67,25 @@ __device__ __forceinline__ float silu_fast(float z) {
   return 0.5f * z * (1.0f + t);
 }
 
+// Gates on the special-function unit (ex2 / lg2 approximations, a few ulp):
+// g = -e^{A_log} softplus(a + dt_bias) with softplus(z) = max(z, 0) +
+// ln(1 + e^{-|z|}), and beta = 1 / (1 + e^{-b}).  Their relative error
+// (~1e-6) moves the in-chunk decays by far less than the operands' rounding.
+__device__ __forceinline__ float lg2_fast(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gate_g_fast(float a, float A_log, float dt_bias) {
+  const float z = a + dt_bias;
+  const float sp = fmaxf(z, 0.0f) +
+                   0.6931471805599453f * lg2_fast(1.0f + fast_exp2(-1.4426950408889634f * fabsf(z)));
+  return -fast_exp2(1.4426950408889634f * A_log) * sp;
+}
+__device__ __forceinline__ float sigmoid_fast(float b) {
+  return __fdividef(1.0f, 1.0f + fast_exp2(-1.4426950408889634f * b));
+}
+
 // The tensor-core operands of both kernels are fp16 (10-bit mantissa, range
 // +-65504): the state is multiplied by rounded factors every chunk, and
 // fp16 keeps that rounding 8x below bf16's.
@@ -588,8 +607,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     for (int k = 0; k < 2; ++k) {
       const int r = 2 * lane + k;
       if (r < L) {
-        gv[k] = gate_g(__uint_as_float(gab[k] << 16), a.A_log[h], a.dt_bias[h]);
-        be[k] = sigmoidf_(__uint_as_float(gab[k] & 0xffff0000u));
+        gv[k] = gate_g_fast(__uint_as_float(gab[k] << 16), a.A_log[h], a.dt_bias[h]);
+        be[k] = sigmoid_fast(__uint_as_float(gab[k] & 0xffff0000u));
       } else {
         gv[k] = 0.f;
         be[k] = 0.f;
