@@ -352,7 +352,9 @@ struct PrepSmem {
   // B operands of the second MMAs: BU_0 | BU_1 | [BW_0; BW_1], bf16 tiles
   // (K-major; the blocks above the diagonal are zeroed once per kernel)
   static constexpr uint32_t BT = SIZE_X0;
-  static constexpr uint32_t SIZE_X = BT + 32768;
+  // the CTA's item schedule (SCHED entries of 24 bytes) and 16 warp counts
+  static constexpr uint32_t SCH = BT + 32768;
+  static constexpr uint32_t SIZE_X = SCH + 512 * 16 + 64;
   static constexpr int AST = 68;             // fp32 row stride of A and T
   static constexpr int THREADS = 256;
 };
@@ -378,44 +380,77 @@ __device__ __forceinline__ void prefetch_gates(const GdnPrefillArgs& a, int64_t 
   }
 }
 
-// Where work item `item` (chunk-major (chunk, key head) index) lives: its
-// sequence b, key head hk, global chunk gc and first token t0.
-struct ItemPos {
-  int32_t gc;
-  int hk, b;
-  int64_t t0;
+// One work item of a CTA's schedule: the (chunk, key head) pair and where it
+// lives, precomputed into shared memory so that the item loop never waits on
+// a lookup in the chunk table.
+struct ItemInfo {
+  int32_t t0;     // first token
+  int32_t gc;     // global chunk
+  int32_t slot;   // the sequence's (valid) slot
+  uint32_t bits;  // L (bits 0..7) | key head (8..23) | first chunk of its sequence (24) |
+                  // initial state (25) | sequence 0 (26)
+  __device__ int L() const { return (int)(bits & 0xffu); }
+  __device__ int hk() const { return (int)((bits >> 8) & 0xffffu); }
+  __device__ bool first() const { return (bits >> 24) & 1u; }
+  __device__ bool init() const { return (bits >> 25) & 1u; }
+  __device__ bool seq0() const { return (bits >> 26) & 1u; }
 };
-__device__ __forceinline__ ItemPos item_pos(const GdnPrefillArgs& a, int item) {
-  ItemPos p;
-  p.gc = item / a.h_k;
-  p.hk = item % a.h_k;
-  p.b = find_seq(a.chunk_off, a.num_seqs, p.gc);
-  p.t0 = a.cu_seqlens[p.b] + (int64_t)(p.gc - a.chunk_off[p.b]) * C;
-  return p;
-}
-// The first item at or after `item`, stepping by n, whose sequence has a valid
-// slot (items of skipped sequences are not prepared), or n_items.
-__device__ __forceinline__ int next_valid_item(const GdnPrefillArgs& a, int item, int n, int n_items) {
-  for (; item < n_items; item += n) {
-    const int b = find_seq(a.chunk_off, a.num_seqs, item / a.h_k);
-    const int slot = a.slot_idx[b];
-    if (slot >= 0 && slot < a.num_slots) break;
-  }
-  return item;
-}
+static_assert(sizeof(ItemInfo) == 16, "schedule entry layout");
+constexpr int SCHED = 512;   // schedule entries per refill (one candidate per thread)
 // TMA of one item's x rows t0 - 3 .. t0 + 63 of its four channel segments
 // into the x tile (rows outside the input read as zero; rows before the
 // sequence's start are replaced by the window in the front end).  Issued by
 // one thread; completes on `bar` with PrepSmem::XT_BYTES.
 __device__ __forceinline__ void issue_x_tile(const GdnPrefillArgs& a, const CUtensorMap* map,
-                                             int item, uint32_t xt, uint64_t* bar) {
-  const ItemPos p = item_pos(a, item);
-  const int y = (int)(p.t0 - 3);
+                                             const ItemInfo& p, uint32_t xt, uint64_t* bar) {
+  const int y = p.t0 - 3;
   mbar_expect_tx(bar, PrepSmem::XT_BYTES);
-  tma_load_2d(xt, map, p.hk * D, y, bar);                                  // q
-  tma_load_2d(xt + PrepSmem::XT_SEG, map, (a.h_k + p.hk) * D, y, bar);     // k
-  tma_load_2d(xt + 2 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * p.hk) * D, y, bar);      // v, 2 hk
-  tma_load_2d(xt + 3 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * p.hk + 1) * D, y, bar);  // v, 2 hk + 1
+  const int hk = p.hk();
+  tma_load_2d(xt, map, hk * D, y, bar);                                  // q
+  tma_load_2d(xt + PrepSmem::XT_SEG, map, (a.h_k + hk) * D, y, bar);     // k
+  tma_load_2d(xt + 2 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * hk) * D, y, bar);      // v, 2 hk
+  tma_load_2d(xt + 3 * PrepSmem::XT_SEG, map, (2 * a.h_k + 2 * hk + 1) * D, y, bar);  // v, 2 hk + 1
+}
+// Refill the CTA's schedule with its candidates k0 .. k0 + SCHED - 1 (item
+// blockIdx.x + k n of the chunk-major order), keeping the valid ones in order:
+// each thread looks one candidate up, a ballot and a block-wide prefix sum
+// place it.  Returns the number of entries.  Called by all threads, between
+// block barriers.
+__device__ int fill_schedule(const GdnPrefillArgs& a, ItemInfo* sched, int32_t* s_cnt, int k0,
+                             int n, int n_items, int tid) {
+  const int item = (int)blockIdx.x + (k0 + tid) * n;
+  ItemInfo e{};
+  bool valid = false;
+  if (item < n_items) {
+    const int32_t gc = item / a.h_k;
+    const int b = find_seq(a.chunk_off, a.num_seqs, gc);
+    const int slot = a.slot_idx[b];
+    valid = slot >= 0 && slot < a.num_slots;
+    if (valid) {
+      const int32_t c = gc - a.chunk_off[b];
+      const int64_t start = a.cu_seqlens[b];
+      const int64_t Tb = a.cu_seqlens[b + 1] - start;
+      const bool init = a.has_init ? a.has_init[b] != 0 : false;
+      e.t0 = (int32_t)(start + (int64_t)c * C);
+      e.gc = gc;
+      e.slot = slot;
+      e.bits = (uint32_t)min((int64_t)C, Tb - (int64_t)c * C) | ((uint32_t)(item % a.h_k) << 8) |
+               ((c == 0 ? 1u : 0u) << 24) | ((init ? 1u : 0u) << 25) | ((b == 0 ? 1u : 0u) << 26);
+    }
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t vote = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) s_cnt[warp] = __popc(vote);
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < SCHED / 32; ++w) {
+    const int cw = s_cnt[w];
+    base += w < warp ? cw : 0;
+    total += cw;
+  }
+  if (valid) sched[base + __popc(vote & ((1u << lane) - 1u))] = e;
+  __syncthreads();
+  return total;
 }
 
 // One (chunk, key head) work item, run by the 16 warps of the CTA (thread index
@@ -437,16 +472,16 @@ constexpr int WPS = NW / 4;             // warps per front-end segment
 constexpr int CP_TID = 2 * WPS * 32;
 constexpr int TPW = C / WPS;            // tokens per front-end warp
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtensorMap* xmap,
-                                          int32_t gc, int hk, int b, int slot, unsigned char* sm,
+                                          const ItemInfo& it, const ItemInfo* next, unsigned char* sm,
                                           int tid, WarpSet& grp, WarpSet& head4, uint64_t* bar,
                                           uint32_t ph, uint64_t* xbar, uint32_t xph, uint32_t tmem,
-                                          int next, uint64_t* stg_free) {
-  const int c = gc - a.chunk_off[b];
-  const int64_t start = a.cu_seqlens[b];
-  const int64_t Tb = a.cu_seqlens[b + 1] - start;
-  const int64_t t0 = start + (int64_t)c * C;
-  const int L = (int)min((int64_t)C, Tb - (int64_t)c * C);
-  const bool init = a.has_init ? a.has_init[b] != 0 : false;
+                                          uint64_t* stg_free) {
+  const int32_t gc = it.gc;
+  const int hk = it.hk(), slot = it.slot;
+  const bool first = it.first();
+  const int64_t t0 = it.t0;
+  const int L = it.L();
+  const bool init = it.init();
   const int cd = a.conv_dim;
   const int warp = tid >> 5, lane = tid & 31;
   constexpr int S = PrepSmem::AST;
@@ -523,13 +558,12 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     // in a sequence's first chunk the history before its first token comes from
     // the slot's window (or zeros), and rows past the chunk's end are zeros.
     const uint32_t xrow = s_base + PrepSmem::XT + seg * PrepSmem::XT_SEG + 8 * lane;
-    const bool interior = c > 0 && L == C;   // every row from the tile
+    const bool interior = !first && L == C;   // every row from the tile
     auto load_row = [&](int rr) -> uint2 {
       if (interior) return ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
-      const int64_t p = (int64_t)c * C + rr;
       uint2 v = make_uint2(0, 0);
-      if (rr < L && p >= 0) v = ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
-      else if (rr < L && init) v = __ldg(reinterpret_cast<const uint2*>(win + (size_t)(3 + p) * cd + ch));
+      if (rr < L && (rr >= 0 || !first)) v = ld_shared_v2(xrow + (uint32_t)(rr + 3) * 256u);
+      else if (rr < L && init) v = __ldg(reinterpret_cast<const uint2*>(win + (size_t)(3 + rr) * cd + ch));
       return v;
     };
     float2 xf[4][2];
@@ -593,11 +627,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   }
   // The v warps (no norm) finish first: those of value head 2 hk prefetch the
   // next item's gates, two of those of value head 2 hk + 1 compute these.
-  if (next >= 0 && warp >= 2 * WPS && warp < 3 * WPS) {
-    const ItemPos np = item_pos(a, next);
-    prefetch_gates(a, np.t0, min(np.t0 + C, (int64_t)a.cu_seqlens[np.b + 1]), tid - 64 * WPS,
-                   32 * WPS);
-  }
+  if (next && warp >= 2 * WPS && warp < 3 * WPS)
+    prefetch_gates(a, next->t0, (int64_t)next->t0 + next->L(), tid - 64 * WPS, 32 * WPS);
   // ---- gates of the two value heads ----
   if (gate_warp) {
     const int g = warp - 3 * WPS;
@@ -640,7 +671,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
   tc_fence_after();
   // every warp has read the x tile: the next item's rows may land in it
-  if (tid == 32 && next >= 0) issue_x_tile(a, xmap, next, s_base + PrepSmem::XT, xbar);
+  if (tid == 32 && next) issue_x_tile(a, xmap, *next, s_base + PrepSmem::XT, xbar);
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] [K;Q]^T -> TMEM columns [0, 128)
       mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
@@ -922,7 +953,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     }
     if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     // (GDN_TEST_WAIT_TIMEOUT: the last chunk of sequence 0, key head 0 stays unpublished)
-    const bool withheld = a.withhold_last_chunk && b == 0 && hk == 0 && gc == a.chunk_off[1] - 1;
+    const bool withheld = a.withhold_last_chunk && it.seq0() && hk == 0 && gc == a.chunk_off[1] - 1;
     if (tid == 0 && !withheld) {
       __threadfence();
       st_release_gpu(a.chunk_ready + (size_t)gc * a.h_k + hk, 1);
@@ -983,16 +1014,21 @@ __global__ void __launch_bounds__(512, 1)
   // in round r, CTA i takes item r n + i, so each round finishes the earliest
   // chunks first.  Items of sequences with an invalid slot are skipped (the
   // scan reports those and waits for nothing).
-  int item = next_valid_item(a, (int)blockIdx.x, n, n_items);
-  if (tid == 32 && item < n_items) issue_x_tile(a, &xmap, item, smem_u32(sm) + PrepSmem::XT, &s_bar[5]);
-  while (item < n_items) {
-    const int nxt = next_valid_item(a, item + n, n, n_items);
-    const ItemPos p = item_pos(a, item);
-    prep_item(a, &xmap, p.gc, p.hk, p.b, a.slot_idx[p.b], sm, tid, grp16, head4, s_bar, ph,
-              &s_bar[5], xph, s_tmem, nxt < n_items ? nxt : -1, &s_bar[6]);
-    ph ^= 1u;
-    xph ^= 1u;
-    item = nxt;
+  // The schedule is refilled every SCHED candidates; the first item of each
+  // fill has its x tile issued here, every other one by the item before it.
+  ItemInfo* sched = reinterpret_cast<ItemInfo*>(sm + PrepSmem::SCH);
+  int32_t* s_cnt = reinterpret_cast<int32_t*>(sm + PrepSmem::SCH + SCHED * sizeof(ItemInfo));
+  for (int k0 = 0; (int)blockIdx.x + k0 * n < n_items; k0 += SCHED) {
+    __syncthreads();   // every thread is done with the previous fill's entries
+    const int cnt = fill_schedule(a, sched, s_cnt, k0, n, n_items, tid);
+    if (cnt > 0 && tid == 32) issue_x_tile(a, &xmap, sched[0], smem_u32(sm) + PrepSmem::XT, &s_bar[5]);
+    for (int i = 0; i < cnt; ++i) {
+      const ItemInfo it = sched[i];
+      prep_item(a, &xmap, it, i + 1 < cnt ? &sched[i + 1] : nullptr, sm, tid, grp16, head4, s_bar,
+                ph, &s_bar[5], xph, s_tmem, &s_bar[6]);
+      ph ^= 1u;
+      xph ^= 1u;
+    }
   }
   // the last item's record copies are complete before the CTA exits
   if (tid == CP_TID) bulk_wait_all();
