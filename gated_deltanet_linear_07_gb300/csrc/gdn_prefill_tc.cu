@@ -203,6 +203,10 @@ __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// All but the four most recently committed copies have read their source.
+__device__ __forceinline__ void bulk_wait_read_but4() {
+  asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -579,10 +583,11 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
     for (int hh = 0; hh < TPW / 4; ++hh) {
       if (hh == 0) {
-        // the previous item's record copies have read the shared memory this
-        // item's tiles go to (signalled by the thread that issued them)
+        // the previous item's [Q; K] record copies have read the tile this
+        // item's q and k go to (signalled by the thread that issued them; its
+        // four U / Wk copies, committed after them, may still be reading)
         if (tid == CP_TID) {
-          bulk_wait_read();
+          bulk_wait_read_but4();
           mbar_arrive(stg_free);
         }
         if (!mbar_wait(stg_free, xph, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
@@ -705,10 +710,16 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
         if (m == 0) rec[128] = nrm[128 + g];
       }
     }
+    // the previous item's U / Wk copies have read their staging (the A/T and
+    // B-operand areas this item rewrites from here on)
+    if (tid == CP_TID) bulk_wait_read();
     tc_fence_before();
     if (!warpset_sync(grp, lane, a.wait_ns)) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
     tc_fence_after();
   }
+  // the B operand tiles start at zero: their blocks above the diagonal stay so
+  for (uint32_t o = 16u * tid; o < 32768u; o += 16u * 512u)
+    *reinterpret_cast<uint4*>(sm + PrepSmem::BT + o) = make_uint4(0, 0, 0, 0);
   // ---- A (rows 0..63 of D1: K K^T) and P (rows 64..127: Q K^T); warp = (32-column
   //      half, head, lanes) ----
   {
@@ -894,11 +905,13 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     bulk_s2g(qrec + K_IN_QREC + 8192, s_base + PrepSmem::KQ + 16384, 8192);
   }
   // ---- U^T and [Wk_0; Wk_1] from TMEM to the workspace ----
-  // Staged as the records' tile images in shared memory that the second MMAs
-  // have finished reading (V, and A/T, dead since the inverse), then written
-  // as four 16 KB bulk copies.  The next item waits for the copies to have
-  // read the staging area only where it first writes its own tiles there.
-  constexpr uint32_t STG = PrepSmem::V;   // U^T_0 | U^T_1 | Wk_0 | Wk_1, 16 KB each
+  // Staged as the records' tile images in shared memory that nothing reads
+  // again this item (the B operands, read by the finished second MMAs, and
+  // A/T, dead since the inverse), then written as four 16 KB bulk copies.
+  // The next item rewrites those areas only after its front end, the first
+  // MMA and the norms, and waits for the copies' reads just before.
+  constexpr uint32_t STG_U = PrepSmem::BT;   // U^T_0 | U^T_1
+  constexpr uint32_t STG_W = PrepSmem::AT;   // Wk_0 | Wk_1
   {
     const bool ok = mbar_wait(&bar[1], ph, a.wait_ns);
     if (!ok) set_status(a.d_status, GDN_DEV_WAIT_TIMEOUT);
@@ -911,9 +924,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       uint32_t tile;
       int row, R, c0;
       if (kind < 2) {            // U^T_g row j = m
-        tile = STG + 16384 * kind; row = m; R = 128; c0 = 0;
+        tile = STG_U + 16384 * kind; row = m; R = 128; c0 = 0;
       } else {                   // Wk of head m/64, row r = m%64, columns i in this half
-        tile = STG + 32768 + 16384 * (m >> 6); row = m & 63; R = 64; c0 = 64 * (kind - 2);
+        tile = STG_W + 16384 * (m >> 6); row = m & 63; R = 64; c0 = 64 * (kind - 2);
       }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -935,8 +948,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   if (tid == CP_TID) {
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
-      bulk_s2g(vrec0 + g * VH_REC + UT_OFF, s_base + STG + 16384 * g, 16384);
-      bulk_s2g(vrec0 + g * VH_REC + WK_OFF, s_base + STG + 32768 + 16384 * g, 16384);
+      bulk_s2g(vrec0 + g * VH_REC + UT_OFF, s_base + STG_U + 16384 * g, 16384);
+      bulk_s2g(vrec0 + g * VH_REC + WK_OFF, s_base + STG_W + 16384 * g, 16384);
     }
   }
   // Publish the item when the scan runs beside the prep: every record byte
@@ -990,9 +1003,6 @@ __global__ void __launch_bounds__(512, 1)
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   }
-  // the B operand tiles start at zero: their blocks above the diagonal stay so
-  for (uint32_t o = 16u * tid; o < 32768u; o += 16u * 512u)
-    *reinterpret_cast<uint4*>(sm + PrepSmem::BT + o) = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
