@@ -274,12 +274,18 @@ int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
  * GPU that loads the library holds those bytes until the process exits.  It
  * calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Returns GDN_EWORKSPACE, with nothing enqueued, when the call would need
- *     more than GDN_NOALLOC_SCRATCH_BYTES of workspace
- *     (gdn_prefill_workspace_size() > GDN_NOALLOC_SCRATCH_BYTES; about 1900
- *     tokens at the Qwen3.5-4B layer shape).
+ *     more than GDN_NOALLOC_SCRATCH_BYTES of workspace.  The rule is
+ *     gdn_prefill_workspace_size(dims, total_tokens, num_seqs) <=
+ *     GDN_NOALLOC_SCRATCH_BYTES; at the Qwen3.5-4B layer shape that is about
+ *     1.87 MB per chunk slot on the tensor-core path (ceil(len / 64) slots per
+ *     sequence, so 2176 tokens for one sequence, fewer as sequences are added)
+ *     and about 74 KB per token with GDN_FP32_STATE (896 tokens).
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The device must not be reset (cudaDeviceReset, or any teardown of its
+ *     primary context) while the library is loaded: the array may then live
+ *     at another address and the cached one would be stale.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents (nothing in it needs to start at zero).  Calls whose
  *     kernels overlap on the GPU (different streams, or different host
