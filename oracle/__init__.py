@@ -10,7 +10,8 @@ Parity pins (tests/test_oracle_pins.py) tie every function here to something
 other than itself: brute-force evaluation of the unrolled recurrence, an
 independent chunked (WY) evaluation, closed forms (pure decay, exact recall,
 repeated-key overwrite), library routines for the conv/SiLU/softplus/sigmoid
-front end, and invariants.
+front end, a hand-worked example and channel selection for the decay/beta
+projection, and invariants.
 """
 from __future__ import annotations
 
@@ -62,6 +63,8 @@ def _load():
                                      p, i64, p, p, p, dbl, p, p, p, ctypes.c_int]
     lib.oracle_gdn_layer.restype = ctypes.c_int
     lib.oracle_gated_rmsnorm.argtypes = [i64, i64, p, p, p, dbl, p]
+    lib.oracle_gate_projection.argtypes = [i64, i64, i64, p, p, p, p]
+    lib.oracle_gate_projection.restype = ctypes.c_int
     lib.oracle_gated_rmsnorm.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -238,3 +241,19 @@ def gated_rmsnorm(o, z, weight, eps=1e-6):
     if rc:
         raise RuntimeError(f"oracle_gated_rmsnorm failed ({rc})")
     return y
+
+
+def gate_projection(hidden, w_ba, h_v):
+    """The decay and beta input projections as one matmul: hidden [n][d_model]
+    and w_ba [2 h_v][d_model] (decay rows first, then beta rows) -> (a, b),
+    each [n][h_v] float64, a = hidden w_ba[:h_v]^T and b = hidden w_ba[h_v:]^T."""
+    lib = _load()
+    hidden, w_ba = _f32(hidden), _f32(w_ba)
+    n, d_model = hidden.shape
+    assert w_ba.shape == (2 * h_v, d_model)
+    a = np.zeros((n, h_v))
+    b = np.zeros((n, h_v))
+    rc = lib.oracle_gate_projection(n, d_model, h_v, _ptr(hidden), _ptr(w_ba), _ptr(a), _ptr(b))
+    if rc:
+        raise RuntimeError(f"oracle_gate_projection failed ({rc})")
+    return a, b

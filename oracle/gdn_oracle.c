@@ -357,3 +357,27 @@ int oracle_gated_rmsnorm(int64_t rows, int64_t d_v, const float* o, const float*
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* The decay and beta input projections as one matmul (oxydllm notes, */
+/* Performance, "Gated DeltaNet fast paths": the small beta/decay     */
+/* projections fuse into one matmul).  With W = [W_a; W_b], 2 h_v     */
+/* rows of d_model weights:                                           */
+/*   a[t][h] = sum_i hidden[t][i] W[h][i]         (decay input)       */
+/*   b[t][h] = sum_i hidden[t][i] W[h_v + h][i]   (beta input)        */
+/* for every token t and value head h < h_v, summed in index order.   */
+int oracle_gate_projection(int64_t n, int64_t d_model, int64_t h_v, const float* hidden,
+                           const float* w, double* a, double* b) {
+  if (n < 0 || d_model <= 0 || h_v <= 0 || !hidden || !w || !a || !b) return -1;
+  for (int64_t t = 0; t < n; ++t) {
+    const float* x = hidden + t * d_model;
+    for (int64_t r = 0; r < 2 * h_v; ++r) {
+      const float* wr = w + r * d_model;
+      double acc = 0.0;
+      for (int64_t i = 0; i < d_model; ++i) acc += (double)x[i] * (double)wr[i];
+      if (r < h_v) a[t * h_v + r] = acc;
+      else b[t * h_v + (r - h_v)] = acc;
+    }
+  }
+  return 0;
+}

@@ -108,6 +108,14 @@ int oracle_gdn_layer(int64_t h_k, int64_t h_v, int64_t d_k, int64_t d_v,
 int oracle_gated_rmsnorm(int64_t rows, int64_t d_v, const float* o, const float* z,
                          const float* w, double eps, double* y);
 
+/* The decay and beta input projections as one matmul: hidden [n][d_model]
+ * and W [2 h_v][d_model] (rows 0 .. h_v - 1 the decay projection W_a, rows
+ * h_v .. 2 h_v - 1 the beta projection W_b) give a = hidden W_a^T and
+ * b = hidden W_b^T, each [n][h_v] float64.  Returns 0, or -1 on bad
+ * arguments. */
+int oracle_gate_projection(int64_t n, int64_t d_model, int64_t h_v, const float* hidden,
+                           const float* w, double* a, double* b);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,6 +39,15 @@ MUTATIONS = {
     "norm_weight_plus_one": ("inv * (double)w[j] * silu", "inv * (1.0 + (double)w[j]) * silu"),
     # gated norm: sigmoid gate instead of SiLU
     "norm_sigmoid_gate": ("(double)w[j] * silu((double)zrow[j])", "(double)w[j] * sigmoid((double)zrow[j])"),
+    # projection: beta rows taken first
+    "projection_rows_swapped": ("if (r < h_v) a[t * h_v + r] = acc;\n      else b[t * h_v + (r - h_v)] = acc;",
+                                "if (r < h_v) b[t * h_v + r] = acc;\n      else a[t * h_v + (r - h_v)] = acc;"),
+    # projection: the weight read transposed (column r of a [d_model][2 h_v] matrix)
+    "projection_weight_transposed": ("acc += (double)x[i] * (double)wr[i];",
+                                     "acc += (double)x[i] * (double)w[i * 2 * h_v + r];"),
+    # projection: the last channel dropped
+    "projection_last_channel": ("for (int64_t i = 0; i < d_model; ++i) acc += (double)x[i] * (double)wr[i];",
+                                "for (int64_t i = 0; i + 1 < d_model; ++i) acc += (double)x[i] * (double)wr[i];"),
     # output read without the current token's write
     "output_before_write": (
         "for (int64_t i = 0; i < d_k; ++i) acc += S[j * d_k + i] * q[i];",

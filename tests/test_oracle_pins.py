@@ -352,6 +352,66 @@ def test_gated_norm_unit_rms_scale_invariance_and_weight_linearity():
     np.testing.assert_allclose(y2, 2.0 * y1, rtol=1e-12)
 
 
+# ---------------------------------------------------------------- decay / beta projection
+
+def test_gate_projection_worked_example():
+    """A 2-token, 3-wide hidden state and h_v = 2 (four weight rows: two decay
+    rows, then two beta rows), worked out by hand from the definition
+    a[t][h] = sum_i hidden[t][i] W[h][i], b[t][h] = sum_i hidden[t][i] W[2 + h][i]."""
+    hidden = np.array([[1.0, 2.0, 3.0],
+                       [-1.0, 0.5, 4.0]])
+    w = np.array([[1.0, 0.0, 0.0],     # a, head 0: the first channel
+                  [0.0, 1.0, -1.0],    # a, head 1: second minus third
+                  [2.0, 2.0, 2.0],     # b, head 0: twice the sum
+                  [0.0, 0.0, 0.25]])   # b, head 1: a quarter of the third
+    a, b = oracle.gate_projection(hidden, w, 2)
+    np.testing.assert_array_equal(a, [[1.0, -1.0], [-1.0, -3.5]])
+    np.testing.assert_array_equal(b, [[12.0, 0.75], [7.0, 1.0]])
+
+
+def test_gate_projection_unit_rows_select_channels():
+    """Weight rows that are unit vectors e_{p(r)} pick channel p(r) of every
+    token exactly: decay rows the first h_v picks, beta rows the rest."""
+    rng = RNG(51)
+    n, d_model, h_v = 37, 96, 8
+    hidden = rng.standard_normal((n, d_model)).astype(np.float32)
+    pick = rng.permutation(d_model)[:2 * h_v]
+    w = np.zeros((2 * h_v, d_model), np.float32)
+    w[np.arange(2 * h_v), pick] = 1.0
+    a, b = oracle.gate_projection(hidden, w, h_v)
+    np.testing.assert_array_equal(a, hidden[:, pick[:h_v]].astype(np.float64))
+    np.testing.assert_array_equal(b, hidden[:, pick[h_v:]].astype(np.float64))
+
+
+def test_gate_projection_linear_in_both_operands():
+    """Additive in the hidden state and in the weights, token by token: the
+    projection of a sum is the sum of the projections (to float64 rounding),
+    and a token's outputs depend on that token's row only."""
+    rng = RNG(52)
+    n, d_model, h_v = 19, 160, 4
+    # multiples of 1/8 below 64 in magnitude: every input and every sum of two
+    # is exact in the single precision the oracle takes its inputs in
+    h1, h2 = (rng.integers(-511, 512, (n, d_model)) / 8.0 for _ in range(2))
+    w1, w2 = (rng.integers(-511, 512, (2 * h_v, d_model)) / 8.0 for _ in range(2))
+    a12, b12 = oracle.gate_projection(h1 + h2, w1, h_v)
+    a1, b1 = oracle.gate_projection(h1, w1, h_v)
+    a2, b2 = oracle.gate_projection(h2, w1, h_v)
+    scale = np.abs(np.concatenate([a1, a2, b1, b2])).max()
+    np.testing.assert_allclose(a12, a1 + a2, atol=1e-12 * scale * d_model)
+    np.testing.assert_allclose(b12, b1 + b2, atol=1e-12 * scale * d_model)
+    aw, bw = oracle.gate_projection(h1, w1 + w2, h_v)
+    a3, b3 = oracle.gate_projection(h1, w2, h_v)
+    np.testing.assert_allclose(aw, a1 + a3, atol=1e-12 * scale * d_model)
+    np.testing.assert_allclose(bw, b1 + b3, atol=1e-12 * scale * d_model)
+    hz = h1.copy()
+    hz[5] = 0.0
+    az, bz = oracle.gate_projection(hz, w1, h_v)
+    assert not az[5].any() and not bz[5].any()
+    keep = np.arange(n) != 5
+    np.testing.assert_array_equal(az[keep], a1[keep])
+    np.testing.assert_array_equal(bz[keep], b1[keep])
+
+
 # ---------------------------------------------------------------- slots and checkpoints
 
 def test_slot_copy_moves_exactly_the_named_slots():
