@@ -179,6 +179,7 @@ KERNEL_SOURCES = {
     "prefill_overlap": ("gdn_prefill_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"),
     "gated_norm": ("gdn_norm.cu", "gdn_common.cuh"),
     "slot_copy": ("gdn_slots.cu", "gdn_common.cuh"),
+    "gate_projection": ("gdn_proj.cu", "gdn_tc.cuh", "gdn_common.cuh"),
 }
 
 
@@ -533,6 +534,49 @@ def bench_gated_norm(torch, gdn, dims, T, device, steps, warmup):
     return {"ms": ms, "bytes": nbytes, "rows": T * dims.h_v}
 
 
+def bench_gate_projection(torch, gdn, workloads, dims, T, device, steps, warmup):
+    """The decay and beta input projections of a T-token batch as one launch
+    (gdn_gate_projection: hidden [T, 2560] bf16, both weights in one [2 h_v,
+    2560] matrix), and the same two products as two separate library matmuls
+    (cuBLAS through torch) for comparison; L2 flushed before every timed call."""
+    inp = workloads.gate_projection_inputs(T, h_v=dims.h_v)
+    bf = torch.bfloat16
+    hidden = torch.from_numpy(inp["hidden"]).to(device=device, dtype=bf)
+    w = torch.from_numpy(inp["w_ba"]).to(device=device, dtype=bf)
+    h_v = dims.h_v
+    a = torch.empty((T, h_v), dtype=bf, device=device)
+    b = torch.empty_like(a)
+    a2, b2 = torch.empty_like(a), torch.empty_like(a)
+    w_a, w_b = w[:h_v].t(), w[h_v:].t()
+    flush = L2Flush(torch, device)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def timed(fn):
+        for _ in range(max(warmup, 3)):
+            fn()
+        ev = [(mk(), mk()) for _ in range(steps)]
+        for e0, e1 in ev:
+            flush()
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    ms = timed(lambda: gdn.gdn_gate_projection(dims, hidden, w, a=a, b=b, d_status=status))
+    ms_two = timed(lambda: (torch.matmul(hidden, w_a, out=a2), torch.matmul(hidden, w_b, out=b2)))
+    # the two results agree to the bf16 rounding of the outputs
+    torch.cuda.synchronize()
+    agree = max(float((a.float() - a2.float()).abs().max()), float((b.float() - b2.float()).abs().max()))
+    out_bytes = 2 * a.numel() * a.element_size()
+    h_bytes = hidden.numel() * hidden.element_size()
+    w_bytes = w.numel() * w.element_size()
+    return {"ms": ms, "ms_two": ms_two, "bytes": h_bytes + w_bytes + out_bytes,
+            "bytes_two": 2 * h_bytes + w_bytes + out_bytes, "d_model": inp["d_model"],
+            "max_abs_diff_vs_library": agree, "status": int(status.item())}
+
+
 def bench_slot_copy(torch, gdn, dims, device, steps, warmup, pairs=64):
     """Copy `pairs` whole slots (state and conv window) to `pairs` others in one
     call; the pool (2 x pairs slots, ~270 MB at the Qwen3.5-4B shape) is larger
@@ -852,10 +896,13 @@ def run_gdn(args):
     if not args.no_prefill and not args.large_only:
         pf = bench_prefill(torch, gdn, workloads, device, args.steps, args.warmup)
         barrier()
-    gn = sc = ck = f32 = None
+    gn = gp = sc = ck = f32 = None
     if pf is not None:
         gn = bench_gated_norm(torch, gdn, pf["inp"]["dims"], pf["inp"]["x"].shape[0], device,
                               args.steps, args.warmup)
+        barrier()
+        gp = bench_gate_projection(torch, gdn, workloads, pf["inp"]["dims"],
+                                   pf["inp"]["x"].shape[0], device, args.steps, args.warmup)
         barrier()
         sc = bench_slot_copy(torch, gdn, pf["inp"]["dims"], device, args.steps, args.warmup)
         barrier()
@@ -936,6 +983,25 @@ def run_gdn(args):
                              "frac": ggbs / hbm, "traffic": recorded_traffic("gated_norm"),
                              "kernel": "gated_rmsnorm_kernel", "peak_source": f"hbm_gbs ({peak_src})",
                              "launch_ms": gn["ms"]}}
+        if gp:
+            pgbs = gp["bytes"] / (gp["ms"] / 1e3) / 1e9
+            line["gate_projection"] = {
+                "metric": "decay/beta input projections as one matmul, GB/s", "value": pgbs,
+                "unit": "GB/s", "ms_per_call": gp["ms"],
+                "config": {"workload": f"hidden [{T}, {gp['d_model']}] bf16 x [{2 * d.h_v}, "
+                                       f"{gp['d_model']}] bf16 -> a, b [{T}, {d.h_v}] bf16",
+                           "bytes_per_call": gp["bytes"],
+                           "l2": "flushed before every timed call (256 MiB written, then 256 MiB read)"},
+                "roofline": {"bound": "hbm", "achieved": pgbs, "peak": hbm, "unit": "GB/s",
+                             "frac": pgbs / hbm, "traffic": recorded_traffic("gate_projection"),
+                             "kernel": "gate_projection_kernel",
+                             "peak_source": f"hbm_gbs ({peak_src})", "launch_ms": gp["ms"]},
+                "vs_two_library_matmuls": {
+                    "ms": gp["ms_two"], "launches": 2, "bytes": gp["bytes_two"],
+                    "saved_launches": 1, "saved_bytes": gp["bytes_two"] - gp["bytes"],
+                    "time_ratio": gp["ms_two"] / gp["ms"],
+                    "max_abs_diff": gp["max_abs_diff_vs_library"]},
+                "gpu_launches": 1, "device_status": gp["status"]}
         if sc:
             sgbs = sc["bytes"] / (sc["ms"] / 1e3) / 1e9
             line["slot_copy"] = {

@@ -12,7 +12,7 @@ from ._binding import (GDN_BF16, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_BAD_SLOT,  # no
                        GdnError, conv_dim, dims_from,
                        gdn_conv1d_update, gdn_decode_step, gdn_dims, gdn_gated_rmsnorm, gdn_params,
                        gdn_prefill_checkpointed, gdn_slot_copy, gdn_prefill_gated_norm,
-                       gdn_decode_step_gated_norm,
+                       gdn_decode_step_gated_norm, gdn_gate_projection,
                        gdn_prefill, gdn_prefill_noalloc, gdn_prefill_workspace_size,
                        GDN_NOALLOC_SCRATCH_BYTES, gdn_trace, load, make_dims,
                        make_trace, STAGES)

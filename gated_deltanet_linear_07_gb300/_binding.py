@@ -104,6 +104,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_prefill_gated_norm.restype = ctypes.c_int
     lib.gdn_decode_step_gated_norm.argtypes = [D, PR, P, P, P, P, I32, P, P, I64, P, P, F, P, P, P]
     lib.gdn_decode_step_gated_norm.restype = ctypes.c_int
+    lib.gdn_gate_projection.argtypes = [D, P, P, I32, I64, P, P, P, P]
+    lib.gdn_gate_projection.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -408,3 +410,28 @@ def gdn_gated_rmsnorm(dims, weight, o, z, y=None, eps=1e-6, stream=None):
                                   _ptr(y), _stream(stream))
     _check("gdn_gated_rmsnorm", rc)
     return y
+
+
+def gdn_gate_projection(dims, hidden, w_ba, a=None, b=None, d_status=None, stream=None):
+    """The decay and beta input projections as one matmul (see
+    gdn_gate_projection in include/gdn.h): hidden [n, d_model] bf16, w_ba
+    [2 h_v, d_model] bf16 (decay rows, then beta rows) -> a, b [n, h_v] bf16
+    (allocated when not given).  Returns (a, b)."""
+    import torch
+    d = dims_from(dims)
+    if hidden.dim() != 2:
+        raise ValueError("hidden must be [n, d_model]")
+    n, d_model = int(hidden.shape[0]), int(hidden.shape[1])
+    if a is None:
+        a = torch.empty((n, d.h_v), dtype=torch.bfloat16, device=hidden.device)
+    if b is None:
+        b = torch.empty((n, d.h_v), dtype=torch.bfloat16, device=hidden.device)
+    _expect(hidden, "hidden", torch.bfloat16)
+    _expect(w_ba, "w_ba", torch.bfloat16, 2 * d.h_v * d_model)
+    _expect(a, "a", torch.bfloat16, n * d.h_v)
+    _expect(b, "b", torch.bfloat16, n * d.h_v)
+    _expect(d_status, "d_status", torch.int32, 1)
+    rc = load().gdn_gate_projection(ctypes.byref(d), _ptr(hidden), _ptr(w_ba), d_model, n,
+                                    _ptr(a), _ptr(b), _ptr(d_status), _stream(stream))
+    _check("gdn_gate_projection", rc)
+    return a, b

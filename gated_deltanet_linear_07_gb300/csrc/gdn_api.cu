@@ -146,6 +146,19 @@ GDN_EXPORT int gdn_gated_rmsnorm(const gdn_dims* dims, const float* weight, floa
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+GDN_EXPORT int gdn_gate_projection(const gdn_dims* dims, const void* hidden, const void* w_ba,
+                                   int32_t d_model, int64_t n, void* a, void* b,
+                                   int32_t* d_status, gdn_stream_t stream) {
+  if (!dims || n < 0 || d_model <= 0) return GDN_EINVAL;
+  if (dims->h_v <= 0) return GDN_EINVAL;
+  if (dims->h_v % 16 != 0 || 2 * dims->h_v > 256 || d_model % 64 != 0) return GDN_EUNSUPPORTED;
+  if (n == 0) return GDN_OK;
+  if (!hidden || !w_ba || !a || !b) return GDN_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_ba) || !aligned16(a) || !aligned16(b)) return GDN_EALIGN;
+  return cuda_rc(gdn_launch_gate_projection(hidden, w_ba, d_model, n, dims->h_v, a, b, d_status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 GDN_EXPORT size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                              int32_t num_seqs) {
   if (check_prefill_dims(dims) != GDN_OK || total_tokens < 0 || num_seqs < 0) return 0;

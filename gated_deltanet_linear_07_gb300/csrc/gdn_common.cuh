@@ -184,6 +184,12 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a, cudaStream_t s, gdn_t
 cudaError_t gdn_launch_check(const GdnPrefillArgs& a, cudaStream_t s, gdn_trace* trace);
 cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, gdn_trace* trace);
 bool gdn_tc_prefill_supported(int h_k, int h_v, int d_k, int d_v, int chunk, int io);
+// cuTensorMapEncodeTiled (the driver's, as a PFN_cuTensorMapEncodeTiled_v12000)
+// looked up once through the runtime's entry-point query; null if unavailable.
+void* gdn_tensor_map_encoder();
+cudaError_t gdn_launch_gate_projection(const void* hidden, const void* w_ba, int d_model,
+                                       int64_t n, int h_v, void* a, void* b, int32_t* d_status,
+                                       cudaStream_t s);
 size_t gdn_tc_kq_bytes();
 size_t gdn_tc_vh_bytes();
 

@@ -139,16 +139,6 @@ __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   return v;
 }
 
-// 2-D tiled TMA load (tensor map in kernel-parameter space) of the box at
-// (x = c0 elements, y = c1 rows) into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                           uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;
@@ -181,11 +171,6 @@ __device__ __forceinline__ bool warpset_sync(WarpSet& w, int lane, uint64_t budg
 
 // Bulk async copies (no tensor map): global -> shared with mbarrier
 // completion, shared -> global with bulk-group completion.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
   asm volatile(
@@ -1556,15 +1541,15 @@ cudaError_t gdn_check_tc_records(const GdnPrefillArgs& a, cudaStream_t s) {
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on the driver library).
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+void* gdn_tensor_map_encoder() {
+  static void* const fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
-      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      return static_cast<void*>(nullptr);
+    return p;
   }();
   return fn;
 }
@@ -1572,7 +1557,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // Tensor map of x [total_tokens][conv_dim] bf16 for the prep's tiles: boxes of
 // 128 channels x 67 rows, dense (no swizzle), zero fill outside the input.
 static cudaError_t make_x_map(const GdnPrefillArgs& a, CUtensorMap* map) {
-  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  const auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(gdn_tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)a.conv_dim,
                               (cuuint64_t)(a.total_tokens > 0 ? a.total_tokens : 1)};

@@ -16,6 +16,7 @@
 // index mod 8 (tile bases are 1024-byte aligned).
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace gdn {
@@ -155,6 +156,23 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64
     if (mbar_test_wait(bar, parity)) return true;
     if ((i & 255u) == 0 && globaltimer_ns() - t0 > budget_ns) return false;
   }
+}
+
+// Expect `bytes` of asynchronous copies on `bar` (and arrive once).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// 2-D tiled TMA load (tensor map in kernel-parameter space) of the box at
+// (x = c0 elements, y = c1 rows) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Descriptor of the same tile `bytes` further on (the start-address field is

@@ -19,6 +19,9 @@ Workloads (numpy PCG64, workload i uses seed 1000 + i):
                  near 1.  Sub-case "b" also pins a = -12 (decay near 1).
   5 varlen       16 seqs, lengths ~ U{1..8192}, 4B shape, bf16, shuffled slots,
                  then 256 decode tokens per sequence.
+  6 gate_projection_inputs  hidden states [n][2560] ~ N(0,1) and the decay/beta
+                 projection weights [2 H_v][2560] ~ N(0, 1/2560), both bf16, so
+                 that the projected a and b are ~ N(0,1) like the layer's.
 Distributions: x, a, b ~ N(0,1) unless stated; conv weight ~ N(0, 0.5^2);
 A_log ~ U(0, 2.7); dt_bias ~ N(0, 0.1^2).
 """
@@ -219,3 +222,19 @@ def varlen(seed: int = SEED_BASE + 5, B: int = 16, max_len: int = 8192,
     inp["decode_a"] = _io(_normal(rng, (decode_steps, B, dims.h_v)), dims)
     inp["decode_b"] = _io(_normal(rng, (decode_steps, B, dims.h_v)), dims)
     return inp
+
+
+# The model width the decay/beta projection reads at the 4B shape (the
+# Qwen3-4B family's hidden size).
+D_MODEL_4B = 2560
+
+
+def gate_projection_inputs(n: int, d_model: int = D_MODEL_4B, h_v: int = 32,
+                           seed: int = SEED_BASE + 6) -> dict:
+    """Inputs of the decay/beta projection: hidden [n][d_model] ~ N(0,1) and
+    w_ba [2 h_v][d_model] ~ N(0, 1/d_model) (decay rows, then beta rows), both
+    rounded to bf16 and kept as float32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return {"hidden": round_bf16(_normal(rng, (n, d_model))),
+            "w_ba": round_bf16(_normal(rng, (2 * h_v, d_model), std=float(d_model) ** -0.5)),
+            "h_v": h_v, "d_model": d_model}

@@ -174,6 +174,32 @@ int gdn_conv1d_update(const gdn_dims* dims, const float* conv_weight,
 int gdn_gated_rmsnorm(const gdn_dims* dims, const float* weight, float eps, const void* o,
                       const void* z, int64_t n, void* y, gdn_stream_t stream);
 
+/*
+ * gdn_gate_projection -- the decay and beta input projections of the layer
+ * as one matmul over the whole token batch (oxydllm 0.0.0-alpha.12.2 release
+ * notes, Performance, "Gated DeltaNet fast paths": the small beta/decay
+ * projections fuse into one matmul when dense).  With W = w_ba, its rows
+ * 0 .. h_v - 1 the decay projection and rows h_v .. 2 h_v - 1 the beta
+ * projection:
+ *   a[t][h] = sum_i hidden[t][i] W[h][i],   b[t][h] = sum_i hidden[t][i] W[h_v + h][i]
+ * for t < n and h < h_v: the gate inputs a and b that gdn_prefill and
+ * gdn_decode_step take.  fp32 accumulation on the tensor cores, rounded once
+ * to bf16.
+ *   hidden     [n][d_model] bf16 (device), the layer's input hidden states
+ *   w_ba       [2 h_v][d_model] bf16 (device)
+ *   a, b       [n][h_v] bf16 (device), written
+ *   d_status   optional device int32: GDN_DEV_WAIT_TIMEOUT if an internal
+ *              wait ran out (the outputs are then not valid)
+ * Uses dims->h_v only (the inputs and outputs are bf16 whatever dims->io).
+ * Returns GDN_EINVAL (null dims or pointer, n < 0, d_model <= 0, h_v <= 0),
+ * GDN_EUNSUPPORTED (h_v not a multiple of 16 or above 128, d_model not a
+ * multiple of 64) or GDN_EALIGN (a pointer not 16-byte aligned) without
+ * launching anything; n = 0 does nothing.  The caller owns every buffer.
+ */
+int gdn_gate_projection(const gdn_dims* dims, const void* hidden, const void* w_ba,
+                        int32_t d_model, int64_t n, void* a, void* b, int32_t* d_status,
+                        gdn_stream_t stream);
+
 /* Bytes of device workspace gdn_prefill needs for this shape (0 on bad dims). */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                   int32_t num_seqs);

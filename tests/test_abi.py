@@ -149,6 +149,25 @@ def test_gated_rmsnorm_rejects_bad_calls_before_launch(lib):
     assert call(y=FAKE + 8) == -5
 
 
+def test_gate_projection_rejects_bad_calls_before_launch(lib):
+    d = gdn.make_dims(**D4B)
+    call = lambda **kw: lib.gdn_gate_projection(  # noqa: E731
+        ctypes.byref(kw.get("dims", d)) if kw.get("dims", d) is not None else None,
+        kw.get("hidden", FAKE), kw.get("w", FAKE), kw.get("d_model", 2560), kw.get("n", 4),
+        kw.get("a", FAKE), kw.get("b", FAKE), None, None)
+    assert call(dims=None) == -1
+    assert call(n=-1) == -1
+    assert call(d_model=0) == -1
+    assert call(hidden=None) == -1
+    assert call(b=None) == -1
+    assert call(dims=gdn.make_dims(**dict(D4B, h_k=1, h_v=8))) == -2    # h_v not a multiple of 16
+    assert call(dims=gdn.make_dims(**dict(D4B, h_k=16, h_v=144))) == -2  # 2 h_v above 256
+    assert call(d_model=2500) == -2                                      # not a multiple of 64
+    assert call(n=0) == 0
+    assert call(hidden=FAKE + 2) == -5
+    assert call(a=FAKE + 8) == -5
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
