@@ -20,8 +20,8 @@
 //       plus P = tril(Q K^T * e^{gamma_r-gamma_s}).  Results go to the
 //       workspace as ready-made shared-memory tile images.
 // scan  one CTA per (sequence, value head), sequential over the chunks, with
-//       the fp32 state S^T held in registers of the epilogue warps and a bf16
-//       copy in shared memory as the MMA operand.  Per chunk (H = S^T):
+//       the fp32 state S^T held in registers of sixteen chain warps and an
+//       fp16 copy in tensor memory as the MMA operand.  Per chunk (H = S^T):
 //         X    = H^T Wk^T                 W^T  = U^T - X
 //         O1   = H^T Q^T                  O2   = W^T P^T
 //         dH   = (W^T diag(e^{gamma_C - gamma})) K
@@ -317,7 +317,7 @@ struct PrepSmem {
   static constexpr uint32_t KQ = 0;          // 32768  [K;Q] K-major, 128 rows x 128
   static constexpr uint32_t V = 32768;       // 2 x 16384, MN-major (64 rows s x 128 j)
   static constexpr uint32_t AT = 65536;      // 2 x fp32 [64][68]: A, then T in place; finally
-                                             // BU_0 | BU_1 | [BW_0; BW_1] bf16 tiles
+                                             // BU_0 | BU_1 | [BW_0; BW_1] fp16 tiles
   static constexpr uint32_t AH = 17408;      // bytes per head of A / T
   static constexpr uint32_t R = 100352;      // 2 x fp32 [4][16][RST]: inverse products
   static constexpr int RST = 24;             // fp32 row stride of those blocks
@@ -338,7 +338,7 @@ struct PrepSmem {
   static constexpr uint32_t XT_SEG = 17408;                   // 67 x 256 bytes, rounded to 1 KiB
   static constexpr uint32_t XT_BYTES = 4 * XT_ROWS * 256;     // transaction bytes per item
   static constexpr uint32_t SIZE_X0 = XT + 4 * XT_SEG;
-  // B operands of the second MMAs: BU_0 | BU_1 | [BW_0; BW_1], bf16 tiles
+  // B operands of the second MMAs: BU_0 | BU_1 | [BW_0; BW_1], fp16 tiles
   // (K-major; the blocks above the diagonal are zeroed once per kernel)
   static constexpr uint32_t BT = SIZE_X0;
   // the CTA's item schedule (SCHED entries of 24 bytes) and 16 warp counts
@@ -664,9 +664,9 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   if (tid == 32 && next) issue_x_tile(a, xmap, *next, s_base + PrepSmem::XT, xbar);
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] [K;Q]^T -> TMEM columns [0, 128)
-      mma_bf16(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
-               sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, false),
-               ks > 0);
+      mma_ss(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
+             sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, false),
+             ks > 0);
     mma_commit(&bar[0]);
   }
   // ---- L2 norms from the diagonal of D1 (warps 0..3: lane m holds row m) ----
@@ -773,9 +773,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   // With 16 x 16 blocks: D_i = (I + A_ii)^-1 by forward substitution (fp32),
   // then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then the lower-left
   // 32 x 32 block -T_[23][23] R with R = A_[23][01] T_[01][01] (products on the
-  // tensor cores in TF32).  Only products of exact blocks, no matrix powers:
-  // finite for fully correlated keys.  T overwrites A block by block; each
-  // block's producer also writes its entries of the second MMAs' bf16 B
+  // tensor cores as fp16 m16n8k16 steps, fp32 accumulation).  Only products of
+  // exact blocks, no matrix powers: finite for fully correlated keys.  T
+  // overwrites A block by block; each block's producer also writes its entries
+  // of the second MMAs' fp16 B
   // operands BU_g = T diag(beta) and BW_g = T diag(beta e^gamma) (the blocks
   // above the diagonal stay zero from the kernel's start).  The stages of a
   // head meet at its own named barrier.
@@ -873,13 +874,13 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
     for (int g = 0; g < 2; ++g)
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
-        mma_bf16(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
-                 sdesc_kmaj(s_base + PrepSmem::BT + 8192 * g, 64, ks),
-                 idesc_f16(128, 64, true, false), ks > 0);
+        mma_ss(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
+               sdesc_kmaj(s_base + PrepSmem::BT + 8192 * g, 64, ks),
+               idesc_f16(128, 64, true, false), ks > 0);
     for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
-      mma_bf16(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BT + 16384, 128, ks),
-               sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, true),
-               ks > 0);
+      mma_ss(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BT + 16384, 128, ks),
+             sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, true),
+             ks > 0);
     mma_commit(&bar[1]);
   }
   if (tid == CP_TID) {  // Q rows then K rows of the [K;Q] tile (tile images) to the workspace
@@ -1036,7 +1037,7 @@ __global__ void __launch_bounds__(512, 1)
 // scan: one CTA (704 threads) per (sequence, value head).
 //   warp 0: bulk loads of chunk inputs (two buffers)
 //   warp 1: MMA issue, four groups per chunk, every A operand in tensor memory
-//           (bf16, written by the chain warps), every B operand in shared memory:
+//           (fp16, written by the chain warps), every B operand in shared memory:
 //             X  = H^T Wk^T                  (N = 64)
 //             O1 = H^T Q^T                   (N = 64, double-buffered)
 //             dH = Wt^T K                    (N = 128; Wt = diag(e^{gamma_C-gamma}) W)
@@ -1067,7 +1068,7 @@ struct ScanSmem {
   static constexpr uint32_t WIN = SIZE;
   static constexpr uint32_t SIZE_WIN = WIN + 3 * 3 * D * 2;
 };
-// TMEM columns (fp32 accumulators, then the bf16 A operands, two per column):
+// TMEM columns (fp32 accumulators, then the fp16 A operands, two per column):
 //   X [64] | O1 x 2 [64] | dH [128] | O2 [64] | H^T [64] | Wt^T [32] | W^T [32]
 constexpr uint32_t TX = 0, TO1 = 64, TDH = 192, TO2 = 320, THT = 384, TWT = 448, TW = 480;
 constexpr int SCAN_THREADS = 704;
@@ -1256,19 +1257,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         // 128B-swizzled K-major tiles of 64-element K blocks.
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // X = H^T Wk^T first: it is on the chain
-          mma_bf16_ts(tmem + TX, tmem + THT + 8 * ks,
-                      sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
+          mma_ts(tmem + TX, tmem + THT + 8 * ks,
+                 sdesc_add(d_b1, (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(bar_x);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // O1 = H^T Q^T
-          mma_bf16_ts(tmem + TO1 + 64 * s, tmem + THT + 8 * ks,
-                      sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
+          mma_ts(tmem + TO1 + 64 * s, tmem + THT + 8 * ks,
+                 sdesc_add(d_b1, 8192 + (ks >> 2) * 16384 + (ks & 3) * 32), ID_XO, ks > 0);
         mma_commit(&empty_b1[s]);
         if (!mbar_spin(wready, c & 1, a.wait_ns)) { fail(); break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dH = Wt^T K
-          mma_bf16_ts(tmem + TDH, tmem + TWT + 8 * ks, sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
+          mma_ts(tmem + TDH, tmem + TWT + 8 * ks, sdesc_add(d_k, ks * 2048), ID_DH, ks > 0);
         // the chain warps stage the next checkpoint (after this chunk, if there is
         // one) only after bar_dh: the copy has read the staging area by then
         if (ck_reading && c == ck_next && c + 1 < nch) {
@@ -1281,7 +1282,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O2 = W^T P^T
-          mma_bf16_ts(tmem + TO2, tmem + TW + 8 * ks, sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
+          mma_ts(tmem + TO2, tmem + TW + 8 * ks, sdesc_add(d_p, ks * 32), ID_O2, ks > 0);
         mma_commit(&bar_o[s]);
         mma_commit(&empty[s]);
       }
@@ -1300,7 +1301,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     // In a 128B-swizzled row the consecutive 16-byte pieces q of one 64-column block
     // sit at (first piece) ^ 16 q, so only the first address is kept.
     const uint32_t a_ut0 = ScanSmem::B_UT + kmaj_off(128, j, 16 * grp);   // + buffer base
-    // this thread's bf16 A-operand columns: H^T[j][32 grp ..], W^T[j][16 grp ..]
+    // this thread's fp16 A-operand columns: H^T[j][32 grp ..], W^T[j][16 grp ..]
     const uint32_t t_ht = tmem + lbase + THT + 16 * grp;
     const uint32_t t_wt = tmem + lbase + TWT + 8 * grp;
     const uint32_t t_w = tmem + lbase + TW + 8 * grp;
@@ -1372,7 +1373,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 
       if (!mbar_wait(bar_dh, c & 1, a.wait_ns)) { fail(); break; }
       tc_fence_after();
-      // H^T <- e^{gamma_C} H^T + dH; bf16 copy for the next chunk's MMAs
+      // H^T <- e^{gamma_C} H^T + dH; fp16 copy for the next chunk's MMAs
       {
         float dH[32];
         tmem_ld32(tmem + lbase + TDH + 32 * grp, dH);

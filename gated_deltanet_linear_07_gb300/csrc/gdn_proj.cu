@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(THREADS)
       const uint32_t st = base + (uint32_t)s * stage_bytes;
 #pragma unroll
       for (int ks = 0; ks < KB / 16; ++ks)
-        mma_bf16(tmem, sdesc_kmaj(st, TM, ks), sdesc_kmaj(st + A_BYTES, N, ks), idesc,
-                 (i > 0 || ks > 0) ? 1u : 0u);
+        mma_ss(tmem, sdesc_kmaj(st, TM, ks), sdesc_kmaj(st + A_BYTES, N, ks), idesc,
+               (i > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&empty[s]);
     }
     // arrives once everything issued above has completed (also after a failed wait)
