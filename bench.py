@@ -506,7 +506,23 @@ def bench_e2e(torch, gdn, run, steps, warmup):
     # the last step's output arrived intact
     np.testing.assert_array_equal(host_out[(steps - 1) % nbuf].float().numpy(),
                                   dev_out[(steps - 1) % nbuf].float().cpu().numpy())
-    return {"ms": ms, "h2d": h2d, "d2h": d2h, "pipeline": f"{nbuf} buffer sets, 3 streams"}
+    # What the host link gives one plain copy of the same size, each direction alone
+    # (pinned memory, one cudaMemcpyAsync): the ceiling the pipeline is held to.
+    def link(dst, src):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(5):
+            t0.record()
+            dst.copy_(src, non_blocking=True)
+            t1.record()
+            torch.cuda.synchronize()
+            ts.append(t0.elapsed_time(t1))
+        return dst.numel() * dst.element_size() / (statistics.median(ts) / 1e3) / 1e9
+    h2d_gbs = link(dev_in[0][0], host_in[0])
+    d2h_gbs = link(host_out[0], dev_out[0])
+    return {"ms": ms, "h2d": h2d, "d2h": d2h, "pipeline": f"{nbuf} buffer sets, 3 streams",
+            "link": {"h2d_gbs_plain_copy": h2d_gbs, "d2h_gbs_plain_copy": d2h_gbs,
+                     "what": "one pinned copy of x (H2D) and of o (D2H), each alone"}}
 
 
 def bench_gated_norm(torch, gdn, dims, T, device, steps, warmup):
@@ -970,7 +986,8 @@ def run_gdn(args):
             line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],
                            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                           "pipeline": e2e["pipeline"]}
+                           "pipeline": e2e["pipeline"], "link": e2e["link"],
+                           "h2d_gbs_achieved": e2e["h2d"] / (e2e["ms"] / 1e3) / 1e9}
         if gn:
             ggbs = gn["bytes"] / (gn["ms"] / 1e3) / 1e9
             line["gated_norm"] = {
