@@ -152,6 +152,7 @@ GDN_EXPORT int gdn_gate_projection(const gdn_dims* dims, const void* hidden, con
   if (!dims || n < 0 || d_model <= 0) return GDN_EINVAL;
   if (dims->h_v <= 0) return GDN_EINVAL;
   if (dims->h_v % 16 != 0 || 2 * dims->h_v > 256 || d_model % 64 != 0) return GDN_EUNSUPPORTED;
+  if (n > (int64_t)INT32_MAX) return GDN_EUNSUPPORTED;   // 128-token tiles index the grid
   if (n == 0) return GDN_OK;
   if (!hidden || !w_ba || !a || !b) return GDN_EINVAL;
   if (!aligned16(hidden) || !aligned16(w_ba) || !aligned16(a) || !aligned16(b)) return GDN_EALIGN;

@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(THREADS)
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
-    // every thread of every other rank pushes once
-    mbar_init(landed, (uint32_t)(p.split - 1) * THREADS);
+    // every thread of every other rank pushes once (unused without a split)
+    mbar_init(landed, p.split > 1 ? (uint32_t)(p.split - 1) * THREADS : 1u);
     fence_mbar_init();
   }
   if (warp == 1) {

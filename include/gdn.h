@@ -193,7 +193,7 @@ int gdn_gated_rmsnorm(const gdn_dims* dims, const float* weight, float eps, cons
  * Uses dims->h_v only (the inputs and outputs are bf16 whatever dims->io).
  * Returns GDN_EINVAL (null dims or pointer, n < 0, d_model <= 0, h_v <= 0),
  * GDN_EUNSUPPORTED (h_v not a multiple of 16 or above 128, d_model not a
- * multiple of 64) or GDN_EALIGN (a pointer not 16-byte aligned) without
+ * multiple of 64, n above 2^31 - 1) or GDN_EALIGN (a pointer not 16-byte aligned) without
  * launching anything; n = 0 does nothing.  The caller owns every buffer.
  */
 int gdn_gate_projection(const gdn_dims* dims, const void* hidden, const void* w_ba,

@@ -163,6 +163,7 @@ def test_gate_projection_rejects_bad_calls_before_launch(lib):
     assert call(dims=gdn.make_dims(**dict(D4B, h_k=1, h_v=8))) == -2    # h_v not a multiple of 16
     assert call(dims=gdn.make_dims(**dict(D4B, h_k=16, h_v=144))) == -2  # 2 h_v above 256
     assert call(d_model=2500) == -2                                      # not a multiple of 64
+    assert call(n=1 << 31) == -2                                         # above 2^31 - 1 tokens
     assert call(n=0) == 0
     assert call(hidden=FAKE + 2) == -5
     assert call(a=FAKE + 8) == -5
