@@ -7,9 +7,10 @@ once to bf16, so |err| <= 2^-8 |ref| (the final rounding, 2^-9, with margin)
 that).  A wrong weight row, a swapped a / b, a transposed operand or a lost K
 block moves outputs by O(max|ref|) and fails it.
 
-Shapes cover one and several K blocks per cluster rank (K split 1, 2 and 4),
-N = 2 h_v from 32 to 256 (16-column groups on both sides of the a / b
-boundary), ragged token tails and a single token, and the full 4B size
+Shapes cover one and several K blocks per cluster rank (K split 1, 2 and 4,
+even and uneven block counts), N = 2 h_v from 32 to 256 (16-column groups
+on both sides of the a / b boundary), ragged token tails and a single token,
+and the full 4B size
 (T = 4096 tokens of width 2560).  The last test feeds the projected gates to
 gdn_prefill and compares the layer with the oracle's projection and layer.
 """
@@ -52,6 +53,8 @@ def _check(got, ref, what):
     (128, 64, 16),      # one K block: no split; N = 32
     (200, 192, 48),     # three K blocks: split 2 (two and one); N = 96
     (1, 640, 128),      # one token, N = 256, ten blocks over four ranks
+    (130, 320, 32),     # five blocks over four ranks (two, one, one, one)
+    (257, 576, 16),     # nine blocks over four ranks (three, two, two, two)
     (4096, 2560, 32),   # the 4B size: 32 tiles x 40 K blocks
 ])
 def test_gate_projection_matches_oracle(gpu_lib, n, d_model, h_v):
