@@ -7,7 +7,7 @@ fallback for any step of the layer.
 """
 from ._binding import (GDN_BF16, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_BAD_SLOT,  # noqa: F401
                        GDN_DEV_WAIT_TIMEOUT, GDN_FP32, GDN_FP32_STATE, GDN_CHECK_FINITE,
-                       GDN_TEST_WAIT_TIMEOUT,
+                       GDN_TEST_WAIT_TIMEOUT, GDN_BF16_OPERANDS,
                        GDN_DEV_NONFINITE_FRONTEND, GDN_DEV_NONFINITE_CHUNK, GDN_DEV_NONFINITE_OUT,
                        GdnError, conv_dim, dims_from,
                        gdn_conv1d_update, gdn_decode_step, gdn_dims, gdn_gated_rmsnorm, gdn_params,

@@ -16,6 +16,7 @@ GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 GDN_FP32_STATE = 0x1   # gdn_dims.flags: fp32 state products in prefill
 GDN_CHECK_FINITE = 0x2  # gdn_dims.flags: per-stage NaN/Inf probe of prefill
 GDN_TEST_WAIT_TIMEOUT = 0x4  # gdn_dims.flags (tests only): 2 ms waits, one chunk withheld
+GDN_BF16_OPERANDS = 0x8      # gdn_dims.flags: bf16 instead of fp16 tensor-core operands
 GDN_DEV_NONFINITE_FRONTEND, GDN_DEV_NONFINITE_CHUNK, GDN_DEV_NONFINITE_OUT = 0x8, 0x10, 0x20
 STATUS = {0: "GDN_OK", -1: "GDN_EINVAL", -2: "GDN_EUNSUPPORTED", -3: "GDN_ECUDA",
           -4: "GDN_EWORKSPACE", -5: "GDN_EALIGN"}

@@ -30,7 +30,8 @@ int check_dims(const gdn_dims* d) {
   if (!d) return GDN_EINVAL;
   if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0) return GDN_EINVAL;
   if (!(d->l2_eps >= 0.0f)) return GDN_EINVAL;
-  if (d->flags & ~(GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT)) return GDN_EINVAL;
+  if (d->flags & ~(GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT | GDN_BF16_OPERANDS))
+    return GDN_EINVAL;
   if (!pow2_dim(d->d_k) || !pow2_dim(d->d_v)) return GDN_EUNSUPPORTED;
   if (d->conv_w != 4) return GDN_EUNSUPPORTED;
   if (d->io != GDN_FP32 && d->io != GDN_BF16) return GDN_EUNSUPPORTED;
@@ -240,6 +241,7 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   const bool test_timeout = (dims->flags & GDN_TEST_WAIT_TIMEOUT) != 0;
   p.wait_ns = test_timeout ? 2000000ull : 4000000000ull;
   p.withhold_last_chunk = test_timeout ? 1 : 0;
+  p.bf16_ops = (dims->flags & GDN_BF16_OPERANDS) != 0 ? 1 : 0;
   char* ws = reinterpret_cast<char*>(workspace);
   p.ws_flag = reinterpret_cast<int32_t*>(ws + L.flag);
   p.ws_q = reinterpret_cast<float*>(ws + L.q);

@@ -144,6 +144,8 @@ struct GdnPrefillArgs {
   // GDN_TEST_WAIT_TIMEOUT: the prep does not publish the last chunk of
   // sequence 0, key head 0 (the scan's wait for it runs out)
   int32_t withhold_last_chunk;
+  // GDN_BF16_OPERANDS: bf16 instead of fp16 tensor-core operands
+  int32_t bf16_ops;
   // interval checkpoints (0 / null: none): every ckpt_every_chunks chunks strictly
   // inside sequence b, the state and window go to slot ckpt_slot[b] + k - 1
   int32_t ckpt_every_chunks;

@@ -86,22 +86,76 @@ __device__ __forceinline__ float sigmoid_fast(float b) {
   return __fdividef(1.0f, 1.0f + fast_exp2(-1.4426950408889634f * b));
 }
 
-// The tensor-core operands of both kernels are fp16 (10-bit mantissa, range
-// +-65504): the state is multiplied by rounded factors every chunk, and
-// fp16 keeps that rounding 8x below bf16's.
-__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
-  __half2 v = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ void f16x8_to_float(const uint4& u, float (&f)[8]) {
-  const __half2* p = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __half22float2(p[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
+// The tensor-core operands of both kernels are fp16 by default (10-bit
+// mantissa, range +-65504): the state is multiplied by rounded factors every
+// chunk, and fp16 keeps that rounding 8x below bf16's.  GDN_BF16_OPERANDS
+// selects bf16 operands instead (the kernels are instantiated for both).
+template <bool BF>
+struct Op;
+template <>
+struct Op<false> {   // fp16
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
   }
-}
+  static __device__ __forceinline__ uint16_t one(float a) {
+    __half v = __float2half_rn(a);
+    return *reinterpret_cast<uint16_t*>(&v);
+  }
+  static __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const __half2* p = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(p[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  static constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_f16(M, N, a_mn, b_mn);
+  }
+  // warp-level m16n8k16 product, fp32 accumulate
+  static __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                                  const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+  static constexpr uint16_t EXP_MASK = 0x7c00u;   // all-ones exponent: Inf / NaN
+};
+template <>
+struct Op<true> {   // bf16
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ uint16_t one(float a) {
+    __nv_bfloat16 v = __float2bfloat16_rn(a);
+    return *reinterpret_cast<uint16_t*>(&v);
+  }
+  static __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  static constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_bf16(M, N, a_mn, b_mn);
+  }
+  static __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                                  const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+  static constexpr uint16_t EXP_MASK = 0x7f80u;
+};
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -123,9 +177,8 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void st_shared_b16(uint32_t addr, __half v) {
-  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<uint16_t*>(&v))
-               : "memory");
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 // Named barrier among `n` threads (whole, converged warps).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
@@ -271,23 +324,16 @@ __global__ void __launch_bounds__(1024) setup_kernel(const GdnPrefillArgs a) {
 // ---------------------------------------------------------------------------
 // prep: persistent CTAs (512 threads), one (chunk, key head) item at a time.
 
-// Warp-level tensor-core product for the 16 x 16 blocks of the chunk inverse:
-// fp16 operands (the same 10-bit mantissa as TF32, half the instructions:
-// one m16n8k16 step covers K = 16), fp32 accumulate.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                              const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 // d (16 x 16, as two 16 x 8 accumulator fragments) += P Q for 16 x 16 fp32
-// blocks P (row stride sp, even) and Q (row stride sq) in shared memory.
+// blocks P (row stride sp, even) and Q (row stride sq) in shared memory: the
+// blocks of the chunk inverse, on the tensor cores as m16n8k16 steps with the
+// operand type of the call (fp16 carries TF32's 10-bit mantissa at half the
+// instructions: one step covers K = 16), fp32 accumulate.
+template <bool BF>
 __device__ __forceinline__ void mma16x16(float (&d)[2][4], const float* P, int sp, const float* Q,
                                          int sq, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
-  auto pk = [](float2 v) { return pack_f16(v.x, v.y); };
+  auto pk = [](float2 v) { return Op<BF>::pack(v.x, v.y); };
   const uint32_t a[4] = {pk(*reinterpret_cast<const float2*>(P + gid * sp + 2 * tig)),
                          pk(*reinterpret_cast<const float2*>(P + (gid + 8) * sp + 2 * tig)),
                          pk(*reinterpret_cast<const float2*>(P + gid * sp + 2 * tig + 8)),
@@ -295,9 +341,9 @@ __device__ __forceinline__ void mma16x16(float (&d)[2][4], const float* P, int s
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const float* q = Q + 8 * nt + gid;
-    const uint32_t b[2] = {pack_f16(q[(2 * tig) * sq], q[(2 * tig + 1) * sq]),
-                           pack_f16(q[(2 * tig + 8) * sq], q[(2 * tig + 9) * sq])};
-    mma_f16_16816(d[nt], a, b);
+    const uint32_t b[2] = {Op<BF>::pack(q[(2 * tig) * sq], q[(2 * tig + 1) * sq]),
+                           Op<BF>::pack(q[(2 * tig + 8) * sq], q[(2 * tig + 9) * sq])};
+    Op<BF>::mma16816(d[nt], a, b);
   }
 }
 // Store sign * d into a 16 x 16 fp32 block (row stride st).
@@ -460,6 +506,7 @@ constexpr int WPS = NW / 4;             // warps per front-end segment
 // read shared memory before anyone writes tiles there again.
 constexpr int CP_TID = 2 * WPS * 32;
 constexpr int TPW = C / WPS;            // tokens per front-end warp
+template <bool BF>
 __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtensorMap* xmap,
                                           const ItemInfo& it, const ItemInfo* next, unsigned char* sm,
                                           int tid, WarpSet& grp, WarpSet& head4, uint64_t* bar,
@@ -603,11 +650,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
           asm("tanh.approx.f32 %0, %1;" : "=f"(t.y) : "f"(h2.y));
           y[p2] = __ffma2_rn(h2, t, h2);
         }
-        const __half2 v0 = __float22half2_rn(y[0]);
-        const __half2 v1 = __float22half2_rn(y[1]);
         const uint2 val = interior || rb + i < L
-                              ? make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
-                                           *reinterpret_cast<const uint32_t*>(&v1))
+                              ? make_uint2(Op<BF>::pack(y[0].x, y[0].y), Op<BF>::pack(y[1].x, y[1].y))
                               : make_uint2(0, 0);
         st_shared_v2(out_addr(4 * hh + i), val);
       }
@@ -665,7 +709,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks)  // D1 = [K;Q] [K;Q]^T -> TMEM columns [0, 128)
       mma_ss(tmem, sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks),
-             sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, false),
+             sdesc_kmaj(s_base + PrepSmem::KQ, 128, ks), Op<BF>::idesc(128, 128, false, false),
              ks > 0);
     mma_commit(&bar[0]);
   }
@@ -761,8 +805,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
                             : 0.f;
           }
           *reinterpret_cast<uint4*>(ptile + kmaj_off(64, r, 32 * hf + 8 * ck)) =
-              make_uint4(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]), pack_f16(pv[4], pv[5]),
-                         pack_f16(pv[6], pv[7]));
+              make_uint4(Op<BF>::pack(pv[0], pv[1]), Op<BF>::pack(pv[2], pv[3]), Op<BF>::pack(pv[4], pv[5]),
+                         Op<BF>::pack(pv[6], pv[7]));
         }
       }
     }
@@ -802,8 +846,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
         for (int hh = 0; hh < 2; ++hh) {
           const int r = 16 * bi + gid + 8 * hh;
           const float t0 = -d[nt][2 * hh], t1 = -d[nt][2 * hh + 1];
-          st_shared_b32(bu + kmaj_off(64, r, c), pack_f16(t0 * b0, t1 * b1));
-          st_shared_b32(bw + kmaj_off(128, 64 * g + r, c), pack_f16(t0 * w0, t1 * w1));
+          st_shared_b32(bu + kmaj_off(64, r, c), Op<BF>::pack(t0 * b0, t1 * b1));
+          st_shared_b32(bw + kmaj_off(128, 64 * g + r, c), Op<BF>::pack(t0 * w0, t1 * w1));
         }
       }
     };
@@ -832,8 +876,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           AT[(o + r) * S + o + j] = x[r];
-          st_shared_b16(bu + kmaj_off(64, o + r, o + j), __float2half_rn(x[r] * b0));
-          st_shared_b16(bw + kmaj_off(128, 64 * g + o + r, o + j), __float2half_rn(x[r] * w0));
+          st_shared_b16(bu + kmaj_off(64, o + r, o + j), Op<BF>::one(x[r] * b0));
+          st_shared_b16(bw + kmaj_off(128, 64 * g + o + r, o + j), Op<BF>::one(x[r] * w0));
         }
       }
     }
@@ -842,11 +886,11 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       const int i = 1 + 2 * wl;   // block row; column block i - 1
       float* Rw = Rt + wl * 16 * RS;
       float d[2][4] = {};
-      mma16x16(d, AT + 16 * i * S + 16 * (i - 1), S, AT + 16 * (i - 1) * S + 16 * (i - 1), S, lane);
+      mma16x16<BF>(d, AT + 16 * i * S + 16 * (i - 1), S, AT + 16 * (i - 1) * S + 16 * (i - 1), S, lane);
       store16x16(Rw, RS, d, 1.f, lane);
       __syncwarp();
       float e[2][4] = {};
-      mma16x16(e, AT + 16 * i * S + 16 * i, S, Rw, RS, lane);
+      mma16x16<BF>(e, AT + 16 * i * S + 16 * i, S, Rw, RS, lane);
       store16x16(AT + 16 * i * S + 16 * (i - 1), S, e, -1.f, lane);
       put_frag(i, i - 1, e);
     }
@@ -854,15 +898,15 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
     const int bi = 2 + (wl >> 1), bj = wl & 1;   // this warp's block of the lower-left 32 x 32
     if (wl < 4) {  // R_ij = A_i0 T_0j + A_i1 T_1j  (T_01 = 0)
       float d[2][4] = {};
-      if (bj == 0) mma16x16(d, AT + 16 * bi * S, S, AT, S, lane);
-      mma16x16(d, AT + 16 * bi * S + 16, S, AT + 16 * S + 16 * bj, S, lane);
+      if (bj == 0) mma16x16<BF>(d, AT + 16 * bi * S, S, AT, S, lane);
+      mma16x16<BF>(d, AT + 16 * bi * S + 16, S, AT + 16 * S + 16 * bj, S, lane);
       store16x16(Rt + wl * 16 * RS, RS, d, 1.f, lane);
     }
     named_bar_sync(hbar, 256);
     if (wl < 4) {  // T_ij = -(sum_{k = 2..i} T_ik R_kj): only its B entries are needed
       float d[2][4] = {};
-      if (bi == 3) mma16x16(d, AT + 48 * S + 32, S, Rt + bj * 16 * RS, RS, lane);
-      mma16x16(d, AT + 16 * bi * S + 16 * bi, S, Rt + ((bi - 2) * 2 + bj) * 16 * RS, RS, lane);
+      if (bi == 3) mma16x16<BF>(d, AT + 48 * S + 32, S, Rt + bj * 16 * RS, RS, lane);
+      mma16x16<BF>(d, AT + 16 * bi * S + 16 * bi, S, Rt + ((bi - 2) * 2 + bj) * 16 * RS, RS, lane);
       put_frag(bi, bj, d);
     }
   }
@@ -876,10 +920,10 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
       for (int ks = 0; ks < 4; ++ks)  // U^T_g -> TMEM columns [64g, 64g+64)
         mma_ss(tmem + 64 * g, sdesc_mnmaj(s_base + PrepSmem::V + 16384 * g, 64, ks),
                sdesc_kmaj(s_base + PrepSmem::BT + 8192 * g, 64, ks),
-               idesc_f16(128, 64, true, false), ks > 0);
+               Op<BF>::idesc(128, 64, true, false), ks > 0);
     for (int ks = 0; ks < 4; ++ks)  // [Wk_0; Wk_1] = [BW_0; BW_1] K -> columns [128, 256)
       mma_ss(tmem + 128, sdesc_kmaj(s_base + PrepSmem::BT + 16384, 128, ks),
-             sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), idesc_f16(128, 128, false, true),
+             sdesc_mnmaj(s_base + PrepSmem::KQ, 128, ks), Op<BF>::idesc(128, 128, false, true),
              ks > 0);
     mma_commit(&bar[1]);
   }
@@ -922,8 +966,8 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
         for (int ck = 0; ck < 4; ++ck) {
           const float* f = &v[8 * ck];
           st_shared_v4(s_base + tile + kmaj_off(R, row, c0 + 32 * h2 + 8 * ck),
-                       make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
-                                  pack_f16(f[6], f[7])));
+                       make_uint4(Op<BF>::pack(f[0], f[1]), Op<BF>::pack(f[2], f[3]), Op<BF>::pack(f[4], f[5]),
+                                  Op<BF>::pack(f[6], f[7])));
         }
       }
     }
@@ -964,6 +1008,7 @@ __device__ __forceinline__ void prep_item(const GdnPrefillArgs& a, const CUtenso
 // at a time.  It lets dependent grids (the scan) launch at once.
 constexpr uint32_t PREP_SMEM = (PrepSmem::SIZE_X + 1023) / 1024 * 1024;
 
+template <bool BF>
 __global__ void __launch_bounds__(512, 1)
     prep_persistent_kernel(const GdnPrefillArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1020,7 +1065,7 @@ __global__ void __launch_bounds__(512, 1)
     if (cnt > 0 && tid == 32) issue_x_tile(a, &xmap, sched[0], smem_u32(sm) + PrepSmem::XT, &s_bar[5]);
     for (int i = 0; i < cnt; ++i) {
       const ItemInfo it = sched[i];
-      prep_item(a, &xmap, it, i + 1 < cnt ? &sched[i + 1] : nullptr, sm, tid, grp16, head4, s_bar,
+      prep_item<BF>(a, &xmap, it, i + 1 < cnt ? &sched[i + 1] : nullptr, sm, tid, grp16, head4, s_bar,
                 ph, &s_bar[5], xph, s_tmem, &s_bar[6]);
       ph ^= 1u;
       xph ^= 1u;
@@ -1075,6 +1120,7 @@ constexpr int SCAN_THREADS = 704;
 constexpr uint32_t EPI_THREADS = 512;   // the chain warps
 constexpr uint32_t OUT_WARPS = 4;
 
+template <bool BF>
 __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -1223,9 +1269,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t ID_XO = idesc_f16(128, 64, false, false);
-      constexpr uint32_t ID_DH = idesc_f16(128, 128, false, true);
-      constexpr uint32_t ID_O2 = idesc_f16(128, 64, false, false);
+      constexpr uint32_t ID_XO = Op<BF>::idesc(128, 64, false, false);
+      constexpr uint32_t ID_DH = Op<BF>::idesc(128, 128, false, true);
+      constexpr uint32_t ID_O2 = Op<BF>::idesc(128, 64, false, false);
       bool ck_reading = false;   // a checkpoint copy may still be reading the staging area
       int ck_next = ck_every - 1;           // chunk after which the next checkpoint falls
       int64_t ck_slot = ck_base;            // and its slot
@@ -1308,7 +1354,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
     {
       uint32_t hp[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) hp[e] = pack_f16(H[2 * e], H[2 * e + 1]);
+      for (int e = 0; e < 16; ++e) hp[e] = Op<BF>::pack(H[2 * e], H[2 * e + 1]);
       tmem_st16(t_ht, hp);
     }
     // warp 2 certifies, through its hready arrivals, what the MMA issuer would
@@ -1344,12 +1390,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           float u[8];
-          f16x8_to_float(q == 0 ? ut0 : ut1, u);
+          Op<BF>::unpack8(q == 0 ? ut0 : ut1, u);
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const float w0 = u[e] - X[8 * q + e], w1 = u[e + 1] - X[8 * q + e + 1];
-            wp[4 * q + e / 2] = pack_f16(w0, w1);
-            wtp[4 * q + e / 2] = pack_f16(w0 * edv[8 * q + e], w1 * edv[8 * q + e + 1]);
+            wp[4 * q + e / 2] = Op<BF>::pack(w0, w1);
+            wtp[4 * q + e / 2] = Op<BF>::pack(w0 * edv[8 * q + e], w1 * edv[8 * q + e + 1]);
           }
         }
         tmem_st8(t_wt, wtp);
@@ -1389,7 +1435,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) scan_kernel(const GdnPrefillA
       {
         uint32_t hp[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) hp[e] = pack_f16(H[2 * e], H[2 * e + 1]);
+        for (int e = 0; e < 16; ++e) hp[e] = Op<BF>::pack(H[2 * e], H[2 * e + 1]);
         tmem_st16(t_ht, hp);
       }
       if (ckpt_on && (c + 1) % ck_every == 0 && c + 1 < nch) {   // stage it, [i][j] as in the pool
@@ -1497,6 +1543,7 @@ namespace tcp {
 // takes chunk gc's [Q; K] record of key head y (y < h_k, the front end's
 // output) or the record of value head y - h_k (the chunk stage's output: P,
 // U^T, the 129 decay factors, Wk).
+template <bool BF>
 __global__ void __launch_bounds__(256) check_records_kernel(const GdnPrefillArgs a) {
   if (!a.ws_flag[0]) return;
   const int gc = blockIdx.x, y = blockIdx.y;
@@ -1509,10 +1556,10 @@ __global__ void __launch_bounds__(256) check_records_kernel(const GdnPrefillArgs
   }
   const int slot = a.slot_idx[lo];
   if (slot < 0 || slot >= a.num_slots) return;
-  auto f16_bad = [](const unsigned char* p, int n, int tid, int nt) {   // fp16 Inf / NaN
+  auto f16_bad = [](const unsigned char* p, int n, int tid, int nt) {   // operand Inf / NaN
     const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
     bool bad = false;
-    for (int e = tid; e < n; e += nt) bad |= (q[e] & 0x7c00u) == 0x7c00u;
+    for (int e = tid; e < n; e += nt) bad |= (q[e] & Op<BF>::EXP_MASK) == Op<BF>::EXP_MASK;
     return bad;
   };
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -1536,7 +1583,11 @@ __global__ void __launch_bounds__(256) check_records_kernel(const GdnPrefillArgs
 
 cudaError_t gdn_check_tc_records(const GdnPrefillArgs& a, cudaStream_t s) {
   if (a.total_tokens == 0) return cudaSuccess;
-  gdn::tcp::check_records_kernel<<<dim3((unsigned)a.max_chunks, a.h_k + a.h_v), 256, 0, s>>>(a);
+  const dim3 grid((unsigned)a.max_chunks, a.h_k + a.h_v);
+  if (a.bf16_ops)
+    gdn::tcp::check_records_kernel<true><<<grid, 256, 0, s>>>(a);
+  else
+    gdn::tcp::check_records_kernel<false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1594,11 +1645,14 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a_in, cudaStream_t s, gd
   const int psmem = (int)PREP_SMEM + 1024;
   const int ssmem =
       (int)(a.ckpt_every_chunks > 0 ? ScanSmem::SIZE_CK : ScanSmem::SIZE_WIN) + 1024;
-  if ((e = cudaFuncSetAttribute(prep_persistent_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) != cudaSuccess)
+  // the fp16 or the bf16 instantiation (GDN_BF16_OPERANDS)
+  auto prep_fn = a.bf16_ops ? prep_persistent_kernel<true> : prep_persistent_kernel<false>;
+  auto scan_fn = a.bf16_ops ? scan_kernel<true> : scan_kernel<false>;
+  if ((e = cudaFuncSetAttribute(prep_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem)) !=
+      cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                ssmem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(scan_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem)) !=
+      cudaSuccess)
     return e;
 
   if ((e = gdn_trace_mark(tr, 0, true, s)) != cudaSuccess) return e;
@@ -1621,17 +1675,17 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a_in, cudaStream_t s, gd
 
   if (!overlap) {
     if ((e = gdn_trace_mark(tr, 1, true, s)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a, xmap)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_fn, a, xmap)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
     if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
-    scan_kernel<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, ssmem, s>>>(a);
+    scan_fn<<<dim3(a.num_seqs, a.h_v), SCAN_THREADS, ssmem, s>>>(a);
     gdn_trace_count(tr, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else {
     // stage 2 covers prep and scan together: no event may sit between them
     if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernelEx(&pcfg, prep_persistent_kernel, a, xmap)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&pcfg, prep_fn, a, xmap)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_seqs, a.h_v);
@@ -1640,7 +1694,7 @@ cudaError_t gdn_launch_prefill_tc(const GdnPrefillArgs& a_in, cudaStream_t s, gd
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, scan_kernel, a)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, scan_fn, a)) != cudaSuccess) return e;
     gdn_trace_count(tr, 1);
   }
   // With checkpoints the window kernel writes the sequences' windows and the

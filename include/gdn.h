@@ -117,6 +117,15 @@ typedef enum { GDN_FP32 = 0, GDN_BF16 = 1 } gdn_dtype;
  *   scan runs beside the prep (at most half as many (sequence, value head)
  *   chains as SMs); elsewhere it is ignored, as it is by the SIMT path. */
 #define GDN_TEST_WAIT_TIMEOUT 0x4
+/* GDN_BF16_OPERANDS: the tensor-core prefill feeds its MMAs bf16 operands
+ *   (8-bit mantissa, the range of fp32) instead of fp16: the bf16 state option
+ *   for precision comparisons, at the same speed.  On ordinary inputs it meets
+ *   the bf16 I/O tolerance; on long runs of fully correlated keys with beta
+ *   near 1 and no decay its rounding leaves several times the fp16 operands'
+ *   error in the state and can take the outputs past that tolerance (the
+ *   precision tests measure it).  Ignored where the SIMT path runs
+ *   (GDN_FP32_STATE or other shapes). */
+#define GDN_BF16_OPERANDS 0x8
 
 typedef struct {
   int32_t h_k;     /* key/query heads */
@@ -127,8 +136,8 @@ typedef struct {
   int32_t chunk;   /* prefill chunk length: 16, 32 or 64 */
   int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
   float l2_eps;    /* added to the sum of squares inside the L2-norm root */
-  int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT, or 0;
-                      other bits: GDN_EINVAL */
+  int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT |
+                      GDN_BF16_OPERANDS, or 0; other bits: GDN_EINVAL */
 } gdn_dims;
 
 typedef struct {

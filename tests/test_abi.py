@@ -73,7 +73,7 @@ def test_workspace_size_rules(lib):
     dfp = gdn.make_dims(**D4B, flags=gdn.GDN_FP32_STATE)
     assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
     assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) != w1
-    for bad_flags in (8, 16, -1):                  # unknown flag bits
+    for bad_flags in (16, 32, -1):                 # unknown flag bits
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**D4B, flags=bad_flags), 4096, 1) == 0
         assert _prefill(lib, gdn.make_dims(**D4B, flags=bad_flags)) == -1
     both = gdn.GDN_FP32_STATE | gdn.GDN_CHECK_FINITE

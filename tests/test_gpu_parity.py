@@ -60,6 +60,8 @@ SHAPES = {
     "asym2_bf16": Dims(h_k=1, h_v=2, d_k=16, d_v=32, chunk=32, io="bf16"),
     "tall_fp32": Dims(h_k=1, h_v=1, d_k=128, d_v=16, chunk=64, io="fp32"),
     "qwen35_4b": QWEN35_4B,
+    # the tensor-core path with bf16 instead of fp16 MMA operands
+    "qwen35_4b_bf16_ops": dataclasses.replace(QWEN35_4B, flags=gdn.GDN_BF16_OPERANDS),
 }
 
 

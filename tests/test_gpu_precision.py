@@ -1,14 +1,18 @@
 """State-operand precision: the prefill with GDN_FP32_STATE (every product with
 the fp32 state in fp32, the SIMT path) against the float64 oracle, and the
-ablation of that option against the tensor-core path (the state and the
-other MMA operands fed to the tensor cores as fp16) on the adversarial
+ablation of that option against the tensor-core path, with the state and the
+other MMA operands fed to the tensor cores as fp16 (the default: TF32's 10-bit
+mantissa) or as bf16 (GDN_BF16_OPERANDS: 7 bits), on the adversarial
 long-sequence workload.
 
 The fp32-state prefill is held to the fp32 tolerance of tests/_gpu.py on its
 final states (|err| <= 1e-3 max|ref| + 1e-5) even with bf16 I/O; its outputs,
-written in bf16, to the bf16 one.  In the ablation both variants meet their
-tolerances on every sampled (sequence, head), and the fp32-state final states
-are the closer ones.
+written in bf16, to the bf16 one.  In the ablation the fp32-state and the
+fp16-operand variants meet their tolerances on every sampled (sequence, head);
+the bf16-operand variant is the ablation's point of comparison and is not held
+to one (on sub-case b its outputs miss the bf16 bound: that is why the
+product's operands are fp16).  The final states are ordered as the operands'
+precision: fp32 closer than fp16, fp16 closer than bf16.
 """
 import dataclasses
 import os
@@ -26,6 +30,7 @@ pytestmark = pytest.mark.gpu
 NCPU = os.cpu_count() or 1
 FP32_STATE = dataclasses.replace(QWEN35_4B, flags=gdn.GDN_FP32_STATE)
 FP32 = dataclasses.replace(QWEN35_4B, io="fp32")    # the fp32 tolerance, for states
+BF16_OPS = dataclasses.replace(QWEN35_4B, flags=gdn.GDN_BF16_OPERANDS)
 
 
 def _with_dims(inp, d):
@@ -78,6 +83,7 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
                        n_threads=NCPU)
     errs = {}
     for name, d in (("tensor-core, fp16 operands", QWEN35_4B),
+                    ("tensor-core, bf16 operands", BF16_OPS),
                     ("fp32 state, chunk 64", FP32_STATE),
                     ("fp32 state, chunk 32", dataclasses.replace(FP32_STATE, chunk=32))):
         inp = _with_dims(base, d)
@@ -86,12 +92,14 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
         got = run.results()
         assert got["status"] == 0
         errs[name] = _errors(got, ref, inp, mask)
-        tol_state = 2e-2 if name.startswith("tensor") else 1e-3 + 1e-5
-        assert errs[name][0] <= 2e-2, (name, errs[name])
-        assert errs[name][1] <= tol_state, (name, errs[name])
+        if "bf16" not in name:
+            tol_state = 2e-2 if name.startswith("tensor") else 1e-3 + 1e-5
+            assert errs[name][0] <= 2e-2, (name, errs[name])
+            assert errs[name][1] <= tol_state, (name, errs[name])
         del run
     for name, (eo, es) in errs.items():
         print(f"adversarial {sub}: {name:34s} worst normalised error o {eo:.2e} state {es:.2e}")
     tc = errs["tensor-core, fp16 operands"][1]
     assert errs["fp32 state, chunk 64"][1] < tc
     assert errs["fp32 state, chunk 32"][1] < tc
+    assert tc < errs["tensor-core, bf16 operands"][1]
