@@ -9,19 +9,22 @@
 //
 // prep  persistent, one CTA per SM; its 16 warps take one (chunk, key head)
 //       item at a time, all chunks of all sequences.  Causal conv + SiLU of
-//       the chunk's q, k and both value
-//       heads' v (3-token halo from x or from the slot's window), L2 norms,
-//       gates and the in-chunk cumulative log-decay gamma; then on the tensor
-//       cores  [K;Q] K^T  (one M=128 MMA gives K K^T and Q K^T), the exact
+//       the chunk's q, k and both value heads' v (the x rows by TMA, one item
+//       ahead; the 3-token halo from x or from the slot's window), gates and
+//       the in-chunk cumulative log-decay gamma; then on the tensor cores the
+//       [K;Q] Gram matrix (one M=128, N=128 MMA: K K^T, Q K^T and, on its
+//       diagonal, the L2 norms, folded into the factors below), the exact
 //       inverse T = (I + strict_tril(diag(beta) K K^T * e^{gamma_r-gamma_s}))^-1
-//       by blockwise forward substitution in fp32 (finite on fully correlated
-//       keys: no matrix powers are formed), and
+//       blockwise (16 x 16 diagonal blocks by fp32 forward substitution, block
+//       products on the tensor cores; finite on fully correlated keys: no
+//       matrix powers are formed), and
 //         U^T  = V^T  (T diag(beta))^T,      Wk^T = K^T (T diag(beta e^gamma))^T,
 //       plus P = tril(Q K^T * e^{gamma_r-gamma_s}).  Results go to the
 //       workspace as ready-made shared-memory tile images.
 // scan  one CTA per (sequence, value head), sequential over the chunks, with
 //       the fp32 state S^T held in registers of sixteen chain warps and an
-//       fp16 copy in tensor memory as the MMA operand.  Per chunk (H = S^T):
+//       fp16 (or bf16) copy in tensor memory as the MMA operand.  Per chunk
+//       (H = S^T):
 //         X    = H^T Wk^T                 W^T  = U^T - X
 //         O1   = H^T Q^T                  O2   = W^T P^T
 //         dH   = (W^T diag(e^{gamma_C - gamma})) K
@@ -30,8 +33,10 @@
 //       thread issues the MMAs; sixteen chain warps own TMEM lanes and keep
 //       the fp32 state in registers; four output warps write o off the chain.
 //
-// Every mbarrier wait is bounded; on timeout the kernel sets
+// Every wait is bounded in global time; on timeout the kernel sets
 // GDN_DEV_WAIT_TIMEOUT, skips the dependent work and still frees its TMEM.
+// Both kernels are instantiated for fp16 (the default) and bf16 MMA operands
+// (GDN_BF16_OPERANDS).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -47,7 +52,6 @@ using namespace gdn::tc;
 
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // d_k = d_v
-constexpr uint32_t KQ_BYTES = 128 * 128 * 2;  // [K;Q] tile in the prep, K-major, 128 rows
 constexpr uint32_t Q_REC = 2 * 64 * 128 * 2;  // per (chunk, key head): Q tile | K tile, K-major, 64 rows each
 constexpr uint32_t K_IN_QREC = 64 * 128 * 2;
 // Record of one (chunk, value head), every tile a ready shared-memory image:
