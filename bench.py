@@ -8,8 +8,12 @@ flushed before every timed step (a 256 MiB write, then a 256 MiB read so the
 write-backs land outside the timed region).  The same JSON line also
 carries the decode step (24 layers x 64 slots, one bf16 token per slot,
 shuffled slots, random fp32 states) as a second measured quantity, the
-end-to-end figure through the C ABI with host buffers, the roofline of the
-dominant kernel and the float64 CPU oracle timed on the host cores.
+large prefill workloads (4 x 32768 adversarial, a 16-sequence varlen batch)
+with their rooflines, the end-to-end figure through the C ABI with host
+buffers (and the host link's plain-copy ceiling), the side operations (gated
+norm, decay/beta projection, slot copy, checkpointed and fp32-state
+prefills), the roofline of the dominant kernel and the float64 CPU oracle
+timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
 
