@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs
   // its part of each row's series and the group adds the parts with shuffles.
   // Each T[s][j] is written and read only by its owner.
   {
-    const int TPC = NT / C;   // 4, 8 or 16 (NT = 256, C = 64, 32, 16)
+    const int TPC = NT / C;   // 2, 4, 8 or 16 (NT = 256, C = 128, 64, 32, 16)
     const int j = tid / TPC, q = tid % TPC;
     for (int r = 0; r < C; ++r) {
       float part = 0.f;

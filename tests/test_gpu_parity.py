@@ -59,6 +59,9 @@ SHAPES = {
     "asym_fp32": Dims(h_k=2, h_v=4, d_k=32, d_v=64, chunk=16, io="fp32"),
     "asym2_bf16": Dims(h_k=1, h_v=2, d_k=16, d_v=32, chunk=32, io="bf16"),
     "tall_fp32": Dims(h_k=1, h_v=1, d_k=128, d_v=16, chunk=64, io="fp32"),
+    # chunk 128 (the SIMT path; head dims up to 64 fit its shared memory)
+    "c128_bf16": Dims(h_k=2, h_v=4, d_k=64, d_v=64, chunk=128, io="bf16"),
+    "c128_fp32": Dims(h_k=1, h_v=2, d_k=32, d_v=16, chunk=128, io="fp32"),
     "qwen35_4b": QWEN35_4B,
     # the tensor-core path with bf16 instead of fp16 MMA operands
     "qwen35_4b_bf16_ops": dataclasses.replace(QWEN35_4B, flags=gdn.GDN_BF16_OPERANDS),
@@ -71,6 +74,17 @@ def test_prefill_varlen_matches_oracle(gpu_lib, name, init):
     d = SHAPES[name]
     inp = workloads.layer_inputs(d, LENGTHS, seed=zlib.crc32(f"{name}-{init}".encode()) % 10000, init=init,
                                  num_slots=len(LENGTHS) + 3)
+    run = PrefillRun(inp)
+    run()
+    check_prefill(inp, run.results(), oracle_prefill(inp, n_threads=NCPU))
+
+
+def test_prefill_chunk128_spans_several_chunks(gpu_lib):
+    """Chunk 128 over sequences of three, two and one chunks (ragged tails),
+    with random initial states: the chunk-local factors and the cross-chunk
+    scan at the largest chunk length."""
+    d = SHAPES["c128_bf16"]
+    inp = workloads.layer_inputs(d, [300, 256, 129, 1, 0], seed=128, init="random")
     run = PrefillRun(inp)
     run()
     check_prefill(inp, run.results(), oracle_prefill(inp, n_threads=NCPU))

@@ -21,6 +21,8 @@ SHAPES = {
     "qwen35_4b_every128": (QWEN35_4B, [257, 128], 128),
     "tiny_fp32": (TINY, [64, 9, 33], 16),                 # SIMT path, chunk 16
     "asym_bf16": (Dims(h_k=1, h_v=2, d_k=16, d_v=32, chunk=32, io="bf16"), [100, 31], 32),
+    # SIMT path, chunk 128: checkpoints land after every 128-token chunk
+    "c128_bf16": (Dims(h_k=1, h_v=2, d_k=32, d_v=32, chunk=128, io="bf16"), [300, 129, 1], 128),
 }
 
 
