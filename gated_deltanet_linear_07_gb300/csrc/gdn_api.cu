@@ -45,8 +45,8 @@ int check_prefill_dims(const gdn_dims* d) {
   int rc = check_dims(d);
   if (rc != GDN_OK) return rc;
   if (d->chunk != 16 && d->chunk != 32 && d->chunk != 64 && d->chunk != 128) return GDN_EUNSUPPORTED;
-  // the SIMT path keeps a chunk's factors in shared memory: chunk 128 fits for
-  // head dims up to 64
+  // the SIMT path keeps a chunk's factors in shared memory (it streams the scan's
+  // inputs and narrows its d_v tile where they would not fit)
   if (gdn_simt_scan_smem_bytes(d->chunk, d->d_k, d->d_v) > kMaxSmem) return GDN_EUNSUPPORTED;
   return GDN_OK;
 }

@@ -292,6 +292,35 @@ __device__ __forceinline__ void tile_cols_cols(float (&acc)[RM][RN], const float
   }
 }
 
+// a(m, k) = T[r0 + m][k] for the unit lower-triangular T stored transposed in
+// the upper triangle (and diagonal) of AT: T[r][k] = AT[k * lda + r] for k <= r,
+// 0 for k > r (AT holds A there); b(k, n) = sc[k] B[k * ldb + c0 + n].  Four
+// rows r0 .. r0 + 3 (r0 a multiple of 4), k over 0 .. r0 + 3.
+template <int RN>
+__device__ __forceinline__ void tile_tt_cols(float (&acc)[4][RN], const float* AT, int lda, int r0,
+                                             const float* B, int ldb, int c0, const float* sc) {
+  static_assert(RN % 4 == 0, "four columns per load");
+  for (int k = 0; k < r0 + 4; ++k) {
+    const float4 v = *reinterpret_cast<const float4*>(AT + k * lda + r0);
+    float a[4] = {v.x, v.y, v.z, v.w};
+    if (k > r0) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) a[m] = m < k - r0 ? 0.f : a[m];
+    }
+    const float s = sc[k];
+    float b[RN];
+#pragma unroll
+    for (int n = 0; n < RN; n += 4) {
+      const float4 w = *reinterpret_cast<const float4*>(B + k * ldb + c0 + n);
+      b[n] = w.x * s; b[n + 1] = w.y * s; b[n + 2] = w.z * s; b[n + 3] = w.w * s;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int n = 0; n < RN; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+  }
+}
+
 // Rows r < L of a [C][cols] block from a token-major workspace array (row r is
 // token tok0 + r, `stride` floats apart) into shared rows `ld` floats apart;
 // rows L..C-1 zero.  cols is a multiple of 4.  Issued as 16-byte cp.async
@@ -316,16 +345,18 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // ---- the chunk-local WY factors: one CTA per (chunk, value head) ---------------
 // Shared-memory layout (floats): K [C][DK+4] | Q, then V [C][max(DK+4, DV)] |
-// A [C][C+4] | T [C][C+4] | gamma [C] | beta [C] | beta e^gamma [C].
+// AT [C][C+4] | gamma [C] | beta [C] | beta e^gamma [C].  AT holds A in its
+// strict lower triangle and, once inverted, T transposed in its upper triangle
+// and diagonal (T[r][j] at AT[j][r], j <= r): one C x C array instead of two,
+// so that chunk 128 fits at head dim 128.
 struct ChunkSmem {
-  int K, QV, A, T, gam, beta, be, n;
+  int K, QV, A, gam, beta, be, n;
   __host__ __device__ ChunkSmem(int C, int DK, int DV) {
     const int qv = (DK + 4) > DV ? DK + 4 : DV;
     int o = 0;
     K = o; o += C * (DK + 4);
     QV = o; o += C * qv;
     A = o; o += C * (C + 4);
-    T = o; o += C * (C + 4);
     gam = o; o += C;
     beta = o; o += C;
     be = o; o += C;
@@ -366,8 +397,7 @@ __global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs
   const int KS = DK + 4, CS = C + 4, QS = (DK + 4) > DV ? DK + 4 : DV;
   float* sK = sm + S.K;
   float* sQV = sm + S.QV;
-  float* sA = sm + S.A;
-  float* sT = sm + S.T;
+  float* sA = sm + S.A;   // A, then A below the diagonal and T^T on and above it
   float* sG = sm + S.gam;
   float* sB = sm + S.beta;
   float* sBe = sm + S.be;
@@ -421,18 +451,21 @@ __global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs
   // V over Q (Q is no longer read), in flight during the inverse
   load_rows(sQV, QS, args.ws_v + ((size_t)tok0 * args.h_v + h) * DV, (size_t)args.h_v * DV, C, L, DV);
   // T = (I + A)^-1 by forward substitution down each column j: T[r][j] =
-  // delta_rj - sum_{s<r} A[r][s] T[s][j].  TPC = NT / C threads share a column
-  // (adjacent lanes); thread q of the group owns the rows s = q mod TPC, sums
-  // its part of each row's series and the group adds the parts with shuffles.
-  // Each T[s][j] is written and read only by its owner.
+  // delta_rj - sum_{j<=s<r} A[r][s] T[s][j] (T[s][j] = 0 for s < j).  TPC = NT / C
+  // threads share a column (adjacent lanes); thread q of the group owns the
+  // rows s = q mod TPC, sums its part of each row's series and the group adds
+  // the parts with shuffles.  T[s][j] goes to AT[j][s] (on or above the
+  // diagonal, where A is zero and never read); each is written and read only
+  // by its owner.  Every lane runs every row (the shuffles are warp-wide).
   {
     const int TPC = NT / C;   // 2, 4, 8 or 16 (NT = 256, C = 128, 64, 32, 16)
     const int j = tid / TPC, q = tid % TPC;
     for (int r = 0; r < C; ++r) {
       float part = 0.f;
-      for (int s2 = q; s2 < r; s2 += TPC) part = fmaf(sA[r * CS + s2], sT[s2 * CS + j], part);
+      for (int s2 = q; s2 < r; s2 += TPC)
+        if (s2 >= j) part = fmaf(sA[r * CS + s2], sA[j * CS + s2], part);
       for (int m = TPC >> 1; m >= 1; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-      if (r % TPC == q) sT[r * CS + j] = r < j ? 0.f : (r == j ? 1.f : -part);
+      if (r % TPC == q && r >= j) sA[j * CS + r] = r == j ? 1.f : -part;
     }
   }
   cp_async_wait_all();
@@ -449,8 +482,8 @@ __global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs
     const int r0 = (t2 / ncb) * 4;
     const int c0c = (t2 % ncb) * 8;
     float acc[4][8] = {};
-    if (is_u) tile_rows_cols<4, 8>(acc, sT, CS, r0, sQV, QS, c0c, 0, r0 + 4, sB);
-    else tile_rows_cols<4, 8>(acc, sT, CS, r0, sK, KS, c0c, 0, r0 + 4, sBe);
+    if (is_u) tile_tt_cols<8>(acc, sA, CS, r0, sQV, QS, c0c, sB);
+    else tile_tt_cols<8>(acc, sA, CS, r0, sK, KS, c0c, sBe);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int r = r0 + m;
@@ -624,12 +657,197 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const GdnPrefillArgs arg
   }
 }
 
+// ---- the scan with its chunk inputs streamed through two buffers ------------
+// For chunks whose Wk, Q and K rows do not fit in shared memory side by side
+// (chunk 128 at head dim 128): the three [C][DK+4] blocks of a chunk pass
+// through two buffers in the order they are used (Wk, Q, K, next Wk, ...), each
+// fetched while the previous one is in use.  Shared-memory layout (floats):
+// S^T [DK][DVT] | X0, X1 [C][DK+4] | P [C][C+4] | U, then W [C][DVT] |
+// e^gamma [C] | e^{gamma_last - gamma} [C].  Same arithmetic as scan_simt_kernel.
+struct ScanStreamSmem {
+  int H, X0, X1, P, W, eg, dl, n;
+  __host__ __device__ ScanStreamSmem(int C, int DK, int DVT) {
+    int o = 0;
+    H = o; o += DK * DVT;
+    X0 = o; o += C * (DK + 4);
+    X1 = o; o += C * (DK + 4);
+    P = o; o += C * (C + 4);
+    W = o; o += C * DVT;
+    eg = o; o += C;
+    dl = o; o += C;
+    n = o;
+  }
+};
+
+template <typename IO, int RMW, int RMS>
+__global__ void __launch_bounds__(256) scan_simt_stream_kernel(const GdnPrefillArgs args, int DVT) {
+  extern __shared__ __align__(16) float sm[];
+  if (!args.ws_flag[0]) return;
+  const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * DVT;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int C = args.chunk, DK = args.d_k, DV = args.d_v;
+  const int slot = args.slot_idx[b];
+  if (slot < 0 || slot >= args.num_slots) {
+    if (h == 0 && blockIdx.z == 0 && tid == 0) set_status(args.d_status, GDN_DEV_BAD_SLOT);
+    return;
+  }
+  const ScanStreamSmem S(C, DK, DVT);
+  const int KS = DK + 4, CS = C + 4;
+  float* sH = sm + S.H;
+  float* const sX0 = sm + S.X0;
+  float* const sX1 = sm + S.X1;
+  float* sP = sm + S.P;
+  float* sW = sm + S.W;
+  float* sEg = sm + S.eg;
+  float* sDl = sm + S.dl;
+
+  const int hk = h / (args.h_v / args.h_k);
+  const int64_t start = args.cu_seqlens[b];
+  const int64_t Tlen = args.cu_seqlens[b + 1] - start;
+  const bool init = args.has_init ? args.has_init[b] != 0 : false;
+  float* gstate = args.state_pool + ((size_t)slot * args.h_v + h) * (size_t)DK * DV;
+  for (int e = tid; e < DK * DVT; e += NT) {
+    const int i = e / DVT, j = e % DVT;
+    sH[e] = init ? gstate[(size_t)i * DV + j0 + j] : 0.f;
+  }
+  IO* out = reinterpret_cast<IO*>(args.o);
+  const int nr = C / RMW, nc = DVT / 4;
+  const int ni = DK / RMS;
+  auto len_at = [&](int64_t cc) { return (Tlen - cc) < (int64_t)C ? (int)(Tlen - cc) : C; };
+  // block i of the stream (3 per chunk: Wk, Q, K) goes to buffer i % 2
+  auto fetch = [&](int64_t cc, int which, float* dst) {
+    const int L = len_at(cc);
+    if (which == 0)
+      load_rows(dst, KS, args.ws_wk + ((size_t)(start + cc) * args.h_v + h) * DK,
+                (size_t)args.h_v * DK, C, L, DK);
+    else
+      load_rows(dst, KS, (which == 1 ? args.ws_q : args.ws_k) + ((size_t)(start + cc) * args.h_k + hk) * DK,
+                (size_t)args.h_k * DK, C, L, DK);
+  };
+  auto fetch_p = [&](int64_t cc) {
+    load_rows(sP, CS, args.ws_p + ((size_t)(start + cc) * args.h_v + h) * C, (size_t)args.h_v * C, C,
+              len_at(cc), C);
+  };
+  int64_t blk = 0;   // stream index of the chunk's Wk block
+  if (Tlen > 0) {
+    fetch(0, 0, sX0);
+    fetch_p(0);
+  }
+  for (int64_t c0 = 0; c0 < Tlen; c0 += C, blk += 3) {
+    const int L = len_at(c0);
+    const int64_t tok0 = start + c0;
+    const bool more = c0 + C < Tlen;
+    float* const xWk = (blk & 1) ? sX1 : sX0;   // the K block reuses this buffer
+    float* const xQ = (blk & 1) ? sX0 : sX1;
+    __syncthreads();   // the previous chunk's reads of its K block, W and S^T are done
+    load_rows(sW, DVT, args.ws_u + ((size_t)tok0 * args.h_v + h) * DV + j0, (size_t)args.h_v * DV, C, L, DVT);
+    fetch(c0, 1, xQ);
+    const float glast = args.ws_gam[(size_t)(tok0 + L - 1) * args.h_v + h];
+    for (int r = tid; r < C; r += NT) {
+      const float g = r < L ? args.ws_gam[(size_t)(tok0 + r) * args.h_v + h] : 0.f;
+      sEg[r] = r < L ? expf(g) : 0.f;
+      sDl[r] = r < L ? expf(glast - g) : 0.f;   // exponent <= 0
+    }
+    asm volatile("cp.async.wait_group 1;" ::: "memory");   // Wk, P and U (Q may still fly)
+    __syncthreads();
+    // W = U - Wk S^T
+    for (int tile = tid; tile < nr * nc; tile += NT) {
+      const int r0 = (tile / nc) * RMW, cc = (tile % nc) * 4;
+      float acc[RMW][4] = {};
+      tile_rows_cols<RMW, 4>(acc, xWk, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+#pragma unroll
+      for (int m = 0; m < RMW; ++m) {
+        float4* w = reinterpret_cast<float4*>(sW + (r0 + m) * DVT + cc);
+        const float4 u = *w;
+        *w = make_float4(u.x - acc[m][0], u.y - acc[m][1], u.z - acc[m][2], u.w - acc[m][3]);
+      }
+    }
+    __syncthreads();
+    float* const xK = xWk;
+    fetch(c0, 2, xK);   // into the Wk block's buffer
+    asm volatile("cp.async.wait_group 1;" ::: "memory");   // Q (K may still fly)
+    __syncthreads();
+    // O = diag(e^gamma) Q S^T + P W
+    for (int tile = tid; tile < nr * nc; tile += NT) {
+      const int r0 = (tile / nc) * RMW, cc = (tile % nc) * 4;
+      float acc[RMW][4] = {};
+      tile_rows_cols<RMW, 4>(acc, xQ, KS, r0, sH, DVT, cc, 0, DK, nullptr);
+#pragma unroll
+      for (int m = 0; m < RMW; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] *= sEg[r0 + m];
+      tile_rows_cols<RMW, 4>(acc, sP, CS, r0, sW, DVT, cc, 0, r0 + RMW, nullptr);
+#pragma unroll
+      for (int m = 0; m < RMW; ++m) {
+        const int r = r0 + m;
+        if (r >= L) continue;
+        IO* orow = out + ((size_t)(tok0 + r) * args.h_v + h) * DV + j0 + cc;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) st_io(orow + n, acc[m][n]);
+      }
+    }
+    __syncthreads();
+    if (more) {   // the next chunk's Wk into the Q block's buffer, its P
+      fetch(c0 + C, 0, xQ);
+      fetch_p(c0 + C);
+      asm volatile("cp.async.wait_group 2;" ::: "memory");   // K
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    // S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
+    const float dlast = expf(glast);
+    const int64_t cs = args.ckpt_every_chunks > 0 ? ckpt_slot_of(args, b, c0 / C + 1, Tlen) : -1;
+    float* cst = cs >= 0 ? args.state_pool + ((size_t)cs * args.h_v + h) * (size_t)DK * DV : nullptr;
+    for (int tile = tid; tile < ni * nc; tile += NT) {
+      const int i0 = (tile / nc) * RMS, cc = (tile % nc) * 4;
+      float acc[RMS][4] = {};
+      tile_cols_cols<RMS, 4>(acc, xK, KS, i0, sW, DVT, cc, L, sDl);
+#pragma unroll
+      for (int m = 0; m < RMS; ++m) {
+        float4* hp = reinterpret_cast<float4*>(sH + (i0 + m) * DVT + cc);
+        const float4 o = *hp;
+        const float4 nv = make_float4(fmaf(dlast, o.x, acc[m][0]), fmaf(dlast, o.y, acc[m][1]),
+                                      fmaf(dlast, o.z, acc[m][2]), fmaf(dlast, o.w, acc[m][3]));
+        *hp = nv;
+        if (cst) *reinterpret_cast<float4*>(cst + (size_t)(i0 + m) * DV + j0 + cc) = nv;
+      }
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int e = tid; e < DK * DVT; e += NT) {
+    const int i = e / DVT, j = e % DVT;
+    gstate[(size_t)i * DV + j0 + j] = sH[e];
+  }
+}
+
 // d_v tile of the scan: 64 wide, or 32 when 64-wide tiles would leave SMs idle
 // (fewer (sequence, head, tile) CTAs than SMs); sms <= 0: the largest tile.
 static int scan_dv_tile(int d_v, int64_t seq_heads = 0, int sms = 0) {
   if (d_v < 64) return d_v;
   if (sms > 0 && seq_heads * (d_v / 64) < sms) return 32;
   return 64;
+}
+
+// The scan's plan: the d_v tile and whether the chunk inputs stream through two
+// buffers (when Wk, Q and K side by side do not fit in shared memory), with its
+// shared-memory bytes.  A plan above the limit is rejected by the caller.
+constexpr size_t kScanSmemLimit = 227 * 1024;
+struct ScanPlan {
+  int dvt;
+  bool stream;
+  size_t bytes;
+};
+static ScanPlan scan_plan(int C, int DK, int DV, int64_t seq_heads = 0, int sms = 0) {
+  const int dvt = scan_dv_tile(DV, seq_heads, sms);
+  const size_t std_bytes = (size_t)ScanSmem(C, DK, dvt).n * sizeof(float);
+  if (std_bytes <= kScanSmemLimit) return {dvt, false, std_bytes};
+  for (int t = dvt; t >= 8; t /= 2) {
+    const size_t b = (size_t)ScanStreamSmem(C, DK, t).n * sizeof(float);
+    if (b <= kScanSmemLimit) return {t, true, b};
+  }
+  return {dvt, false, std_bytes};
 }
 
 static int num_sms() {
@@ -680,11 +898,12 @@ static cudaError_t launch_simt(const GdnPrefillArgs& a, cudaStream_t s, gdn_trac
     if (e != cudaSuccess) return e;
     if ((e = gdn_trace_mark(tr, 1, false, s)) != cudaSuccess) return e;
   }
-  const int DVT = scan_dv_tile(a.d_v, (int64_t)a.num_seqs * a.h_v, num_sms());
-  const ScanSmem L(a.chunk, a.d_k, DVT);
-  const size_t smem = (size_t)L.n * sizeof(float);
-  // 32-wide tiles: 2 x 4 and 4 x 4 blocks, else 4 x 4 and 8 x 4
-  auto kern = DVT == 32 ? scan_simt_kernel<IO, 2, 4> : scan_simt_kernel<IO, 4, 8>;
+  const ScanPlan plan = scan_plan(a.chunk, a.d_k, a.d_v, (int64_t)a.num_seqs * a.h_v, num_sms());
+  const int DVT = plan.dvt;
+  const size_t smem = plan.bytes;
+  // 32-wide (or narrower) tiles: 2 x 4 and 4 x 4 blocks, else 4 x 4 and 8 x 4
+  auto kern = plan.stream ? (DVT <= 32 ? scan_simt_stream_kernel<IO, 2, 4> : scan_simt_stream_kernel<IO, 4, 8>)
+                          : (DVT == 32 ? scan_simt_kernel<IO, 2, 4> : scan_simt_kernel<IO, 4, 8>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if ((e = gdn_trace_mark(tr, 2, true, s)) != cudaSuccess) return e;
@@ -725,7 +944,7 @@ cudaError_t gdn_launch_window(const GdnPrefillArgs& a, int io, cudaStream_t s, g
 }
 
 size_t gdn_simt_scan_smem_bytes(int chunk, int d_k, int d_v) {
-  const size_t scan = (size_t)gdn::ScanSmem(chunk, d_k, gdn::scan_dv_tile(d_v)).n * sizeof(float);
+  const size_t scan = gdn::scan_plan(chunk, d_k, d_v).bytes;
   const size_t chk = (size_t)gdn::ChunkSmem(chunk, d_k, d_v).n * sizeof(float);
   return scan > chk ? scan : chk;
 }

@@ -133,9 +133,8 @@ typedef struct {
   int32_t d_k;     /* key head dim: 16, 32, 64 or 128 */
   int32_t d_v;     /* value head dim: 16, 32, 64 or 128 */
   int32_t conv_w;  /* conv width; must be 4 */
-  int32_t chunk;   /* prefill chunk length: 16, 32, 64 or 128 (128 where the
-                      SIMT path's per-chunk factors fit in shared memory: head
-                      dims up to 64; otherwise GDN_EUNSUPPORTED) */
+  int32_t chunk;   /* prefill chunk length: 16, 32, 64 or 128 (the tensor-core
+                      path runs chunk 64; other lengths take the SIMT path) */
   int32_t io;      /* gdn_dtype of x, a, b, o and the conv pool */
   float l2_eps;    /* added to the sum of squares inside the L2-norm root */
   int32_t flags;   /* GDN_FP32_STATE | GDN_CHECK_FINITE | GDN_TEST_WAIT_TIMEOUT |

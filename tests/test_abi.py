@@ -65,10 +65,11 @@ def test_workspace_size_rules(lib):
     d32 = gdn.make_dims(**dict(D4B, io="fp32"))
     per_token = (2 * 16 * 128 + 32 * 128 + 2 * 32) + (32 * 128 + 32 * 128 + 32 * 64 + 32)
     assert gdn.gdn_prefill_workspace_size(d32, 4096, 1) >= 4096 * per_token * 4
-    # chunk 128 where the SIMT path's shared memory holds it (head dims <= 64), not at d = 128
-    assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**dict(D4B, d_k=64, d_v=64, chunk=128)),
-                                          4096, 1) > 0
-    for bad in (dict(D4B, d_k=48), dict(D4B, chunk=128), dict(D4B, chunk=256), dict(D4B, h_v=33),
+    # chunk 128 on the SIMT path, at head dim 64 and at the 4B shape's 128 (streamed scan)
+    for dd in (64, 128):
+        assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**dict(D4B, d_k=dd, d_v=dd, chunk=128)),
+                                              4096, 1) > 0
+    for bad in (dict(D4B, d_k=48), dict(D4B, chunk=256), dict(D4B, chunk=48), dict(D4B, h_v=33),
                 dict(D4B, conv_w=3), dict(D4B, io=7), dict(D4B, h_k=1, h_v=65536, d_v=16)):
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**bad), 4096, 1) == 0
     assert gdn.gdn_prefill_workspace_size(d, -1, 1) == 0

@@ -59,9 +59,10 @@ SHAPES = {
     "asym_fp32": Dims(h_k=2, h_v=4, d_k=32, d_v=64, chunk=16, io="fp32"),
     "asym2_bf16": Dims(h_k=1, h_v=2, d_k=16, d_v=32, chunk=32, io="bf16"),
     "tall_fp32": Dims(h_k=1, h_v=1, d_k=128, d_v=16, chunk=64, io="fp32"),
-    # chunk 128 (the SIMT path; head dims up to 64 fit its shared memory)
+    # chunk 128 (the SIMT path; at head dim 128 its scan streams the chunk inputs)
     "c128_bf16": Dims(h_k=2, h_v=4, d_k=64, d_v=64, chunk=128, io="bf16"),
     "c128_fp32": Dims(h_k=1, h_v=2, d_k=32, d_v=16, chunk=128, io="fp32"),
+    "qwen35_4b_c128": dataclasses.replace(QWEN35_4B, chunk=128),
     "qwen35_4b": QWEN35_4B,
     # the tensor-core path with bf16 instead of fp16 MMA operands
     "qwen35_4b_bf16_ops": dataclasses.replace(QWEN35_4B, flags=gdn.GDN_BF16_OPERANDS),

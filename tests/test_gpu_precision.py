@@ -39,7 +39,7 @@ def _with_dims(inp, d):
     return out
 
 
-@pytest.mark.parametrize("chunk", [64, 32])
+@pytest.mark.parametrize("chunk", [128, 64, 32])
 def test_fp32_state_prefill_matches_oracle(gpu_lib, chunk):
     d = dataclasses.replace(FP32_STATE, chunk=chunk)
     inp = workloads.layer_inputs(d, [130, 64, 300, 1, 77], seed=70 + chunk, init="mixed")
