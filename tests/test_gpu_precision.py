@@ -69,7 +69,7 @@ def _errors(got, ref, inp, mask):
 @pytest.mark.parametrize("sub", ["a", "b"])
 def test_state_precision_ablation_adversarial(gpu_lib, sub):
     """4 x 32768 tokens of correlated keys (512 chunks per sequence): the
-    tensor-core path, the fp32-state path at chunk 64 and at chunk 32, each
+    tensor-core path, the fp32-state path at chunks 128, 64 and 32, each
     against the oracle on 2 sampled heads per sequence."""
     base = workloads.adversarial(sub=sub)
     rng = np.random.default_rng(12)
@@ -85,7 +85,8 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
     for name, d in (("tensor-core, fp16 operands", QWEN35_4B),
                     ("tensor-core, bf16 operands", BF16_OPS),
                     ("fp32 state, chunk 64", FP32_STATE),
-                    ("fp32 state, chunk 32", dataclasses.replace(FP32_STATE, chunk=32))):
+                    ("fp32 state, chunk 32", dataclasses.replace(FP32_STATE, chunk=32)),
+                    ("fp32 state, chunk 128", dataclasses.replace(FP32_STATE, chunk=128))):
         inp = _with_dims(base, d)
         run = PrefillRun(inp)
         run()
@@ -102,4 +103,5 @@ def test_state_precision_ablation_adversarial(gpu_lib, sub):
     tc = errs["tensor-core, fp16 operands"][1]
     assert errs["fp32 state, chunk 64"][1] < tc
     assert errs["fp32 state, chunk 32"][1] < tc
+    assert errs["fp32 state, chunk 128"][1] < tc
     assert tc < errs["tensor-core, bf16 operands"][1]
