@@ -276,7 +276,8 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_params* params,
  * nothing.
  *   stage 0  front end: argument check on the device, conv + SiLU, L2 norm,
  *            gates, conv-window write-back
- *   stage 1  per-chunk state-independent work (tensor-core path only)
+ *   stage 1  per-chunk state-independent work (on the tensor-core path it
+ *            is part of stage 2 when the prep and the scan run overlapped)
  *   stage 2  cross-chunk state scan and outputs
  */
 #define GDN_NUM_STAGES 3
