@@ -1,6 +1,6 @@
 // gdn_prefill_simt.cu -- chunked prefill of the Gated DeltaNet layer on the
 // fp32 SIMT pipes, for every supported shape (d_k, d_v in {16,32,64,128},
-// chunk in {16,32,64}, fp32 or bf16 I/O).  The tensor-core path takes the
+// chunk in {16,32,64,128}, fp32 or bf16 I/O).  The tensor-core path takes the
 // Qwen3.5-4B layer shape; this path serves the other shapes and fp32 I/O, whose
 // 1e-3 tolerance bf16 tensor-core operands would not meet.
 //
@@ -25,7 +25,9 @@
 //       U = T diag(beta) V,  Wk = T diag(beta e^gamma) K,
 //       P = tril(Q K^T * e^{gamma_r - gamma_s})
 //   5. scan               one CTA per (sequence, value head, d_v tile),
-//                         sequential over chunks, state in shared memory:
+//                         sequential over chunks, state in shared memory
+//                         (the chunk inputs streamed through two buffers where
+//                         they would not fit side by side):
 //       W = U - Wk S^T
 //       O = diag(e^gamma) Q S^T + P W
 //       S^T <- e^{gamma_last} S^T + K^T diag(e^{gamma_last - gamma}) W
