@@ -54,6 +54,18 @@ def test_recurrence_matches_independent_chunked_form(C):
     assert np.abs(S - S_ref).max() <= 1e-10 * np.abs(S_ref).max()
 
 
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_recurrence_matches_chunked_form_at_the_gpu_chunk_lengths(C):
+    """The same independent chunked evaluation at the chunk lengths the GPU
+    paths run (several full chunks and a ragged tail): the chunk length only
+    changes rounding."""
+    q, k, v, g, beta, S0 = _rand_head(RNG(70 + C), 300, 8, 12)
+    o_ref, S_ref = chunked_wy(q, k, v, g, beta, S0, C=C)
+    o, S = oracle.recurrence(q, k, v, g, beta, S0)
+    assert np.abs(o - o_ref).max() <= 1e-10 * np.abs(o_ref).max()
+    assert np.abs(S - S_ref).max() <= 1e-10 * np.abs(S_ref).max()
+
+
 def test_beta_zero_is_pure_decay():
     """beta = 0: S_T = exp(sum g) S_0 and o_t = exp(sum_{s<=t} g_s) S_0 q_t."""
     q, k, v, g, _, S0 = _rand_head(RNG(11), 20, 8, 6, g_scale=2.0)
