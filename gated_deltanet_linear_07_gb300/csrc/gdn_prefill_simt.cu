@@ -432,7 +432,14 @@ __global__ void __launch_bounds__(256, 2) chunk_simt_kernel(const GdnPrefillArgs
   // takes rows ti + m C/4 and columns tj + n C/4
   const int nb = C / 4;
   for (int tile = tid; tile < nb * nb; tile += NT) {
-    const int ti = tile / nb, tj = tile % nb;
+    // a warp takes 4 row blocks x 8 column blocks (when nb allows): its eight
+    // K rows per load step sit 4 (d_k + 4) floats apart, eight distinct banks
+    int ti = tile / nb, tj = tile % nb;
+    if (nb % 8 == 0) {
+      const int blk = tile >> 5, ln = tile & 31, nbj = nb / 8;
+      ti = 4 * (blk / nbj) + (ln >> 3);
+      tj = 8 * (blk % nbj) + (ln & 7);
+    }
     float a[4][4] = {}, p[4][4] = {};
     tile_rows_rows<4, 4>(a, sK, KS, ti, sK, KS, tj, nb, DK);
     tile_rows_rows<4, 4>(p, sQV, QS, ti, sK, KS, tj, nb, DK);
