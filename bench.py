@@ -189,10 +189,11 @@ KERNEL_SOURCES = {
 
 def source_sha(kernel_key):
     """Hash of the sources a kernel is built from (the files named in
-    KERNEL_SOURCES; all of csrc/ for a kernel not listed)."""
+    KERNEL_SOURCES; all of csrc/ for a kernel not listed).  A key of the form
+    'kernel:workload' takes the kernel's sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_linear_07_gb300", "csrc")
-    files = KERNEL_SOURCES.get(kernel_key) or sorted(
+    files = KERNEL_SOURCES.get(kernel_key.split(":")[0]) or sorted(
         f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
     for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
@@ -201,7 +202,9 @@ def source_sha(kernel_key):
 
 def recorded_traffic(kernel_key):
     """DRAM bytes per launch of a kernel from the committed ncu summary, if its
-    sources have not changed since the counters were taken."""
+    sources have not changed since the counters were taken.  The key names the
+    kernel and, after a colon, the workload when the launch is not the T=4096
+    one (traffic is per launch, so each workload has its own record)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -393,7 +396,7 @@ def bench_large(torch, gdn, workloads, device, name, steps, warmup, peak_tf, pea
     res = time_prefill(torch, gdn, run, L2Flush(torch, device), steps, warmup)
     T = run.T
     ms = statistics.median(res["step_ms"])
-    roof, stage_tflops = prefill_roofline(d, T, res["stage_ms"], peak_tf, peak_src)
+    roof, stage_tflops = prefill_roofline(d, T, res["stage_ms"], peak_tf, peak_src, workload=name)
     flops = alg_flops_per_token_head(d.chunk, d.d_k) * T * d.h_v
     # minimum HBM bytes of the call: x, a, b in, o out, initial states read, final written
     nb = len(lengths)
@@ -826,13 +829,14 @@ def replica_throughput(world, units_per_rank, ms):
     return world * units_per_rank / (ms / 1e3)
 
 
-def prefill_roofline(d, T, stage, peak_tf, peak_src, reduce=lambda v: v):
+def prefill_roofline(d, T, stage, peak_tf, peak_src, reduce=lambda v: v, workload=None):
     """Roofline of the dominant prefill stage: the method's FLOPs that stage
     performs (per launch) over its event time, against the bf16 peak.  The
     chunk stage does K K^T, Q K^T, T (beta V), T (beta e^gamma K) (8 C d per
     token and head), the scan P W and Wk S^T, Q S^T, W^T K (2 C d + 6 d^2);
     in the overlapped launch the chunk work runs inside the scan stage's
-    interval, which then carries both shares."""
+    interval, which then carries both shares.  `workload` names a launch other
+    than the T=4096 one, whose DRAM traffic is recorded under its own key."""
     stage_flops = {"frontend": 0.0,
                    "chunk": 8.0 * d.chunk * d.d_k * T * d.h_v,
                    "scan": (2.0 * d.chunk * d.d_k + 6.0 * d.d_k * d.d_k) * T * d.h_v}
@@ -846,7 +850,8 @@ def prefill_roofline(d, T, stage, peak_tf, peak_src, reduce=lambda v: v):
         ach = stage_flops[dom] / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": ach / peak_tf,
-                "traffic": recorded_traffic("prefill_overlap" if overlapped else "prefill_" + dom),
+                "traffic": recorded_traffic(("prefill_overlap" if overlapped else "prefill_" + dom) +
+                                            (":" + workload if workload else "")),
                 "kernel": {"chunk": "prep_persistent_kernel (prefill stage 'chunk')",
                            "scan": ("scan_kernel (prefill stage 'scan')" if "chunk" in stage else
                                    "prep_persistent_kernel + scan_kernel, overlapped "
