@@ -12,8 +12,9 @@ large prefill workloads (4 x 32768 adversarial, a 16-sequence varlen batch)
 with their rooflines, the end-to-end figure through the C ABI with host
 buffers (and the host link's plain-copy ceiling), the side operations (gated
 norm, decay/beta projection, slot copy, checkpointed and fp32-state
-prefills), the roofline of the dominant kernel and the float64 CPU oracle
-timed on the host cores.
+prefills), side figures outside the headline (the prefill with a warm L2;
+the prefill and the decode step replayed from CUDA graphs), the roofline of
+the dominant kernel and the float64 CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
 
@@ -57,6 +58,8 @@ def parse_args():
                    help="measure only the decode step (profiling runs)")
     p.add_argument("--decode-layers", type=int, default=24)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the warm-L2 and CUDA-graph side figures")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-large", action="store_true",
                    help="skip the 4 x 32768 and the mixed varlen prefill workloads")
@@ -331,6 +334,77 @@ def trace_stages(torch, gdn, run, ev, flush):
         if vals:
             stage_ms[name] = statistics.median(vals)
     return stage_ms, launches
+
+
+def graph_replay_ms(torch, fn, steps, flush=None):
+    """`fn` (library calls on the current stream) captured once into a CUDA
+    graph and replayed: the median ms of `steps` replays with CUDA events
+    around each, `flush` (outside the graph) before each when given.  Returns
+    (ms, None), or (None, reason) when the capture is refused."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+    except RuntimeError as e:
+        torch.cuda.synchronize()
+        return None, (str(e).strip().splitlines() or ["capture failed"])[0][:200]
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for s_, e_ in ev:
+        if flush is not None:
+            flush()
+        s_.record()
+        g.replay()
+        e_.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(s_.elapsed_time(e_) for s_, e_ in ev)
+    del g
+    return ms, None
+
+
+def warm_l2_ms(torch, fn, steps):
+    """Median ms of `fn` called back to back without an L2 flush (inputs that
+    fit in L2 stay there), CUDA events around each call."""
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ev = [(mk(), mk()) for _ in range(steps)]
+    for s_, e_ in ev:
+        s_.record()
+        fn()
+        e_.record()
+    torch.cuda.synchronize()
+    return statistics.median(s_.elapsed_time(e_) for s_, e_ in ev)
+
+
+def bench_launch_variants(torch, pf_run, dec_step, steps, device):
+    """Side figures outside the headline: the T=4096 prefill back to back with
+    a warm L2, the same call and the 24-layer decode step replayed from CUDA
+    graphs (what a serving loop that captures its layers sees)."""
+    out = {"prefill_warm_l2_ms": warm_l2_ms(torch, pf_run, steps)}
+    ms, why = graph_replay_ms(torch, pf_run, steps, flush=L2Flush(torch, device))
+    out["prefill_cuda_graph_ms"] = ms
+    if why:
+        out["prefill_cuda_graph_error"] = why
+    if dec_step is not None:
+        ms, why = graph_replay_ms(torch, dec_step, steps)
+        out["decode_cuda_graph_ms_per_step"] = ms
+        if why:
+            out["decode_cuda_graph_error"] = why
+    out["note"] = ("not the headline: warm = no L2 flush between calls; graph = the same calls "
+                   "captured once with torch.cuda.CUDAGraph and replayed, L2 flushed before each "
+                   "prefill replay")
+    return out
 
 
 def bench_prefill(torch, gdn, workloads, device, steps, warmup):
@@ -733,7 +807,8 @@ def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=
     state_bytes = 2 * layers * slots * d.h_v * d.d_k * d.d_v * 4
     norm = bench_decode_gated_norm(torch, gdn, runs, status, steps, warmup)
     return {"step_ms": step_ms, "layer_ms": layer_ms, "state_bytes": state_bytes,
-            "layers": layers, "slots": slots, "status": int(status.item()), "gated_norm": norm}
+            "layers": layers, "slots": slots, "status": int(status.item()), "gated_norm": norm,
+            "step_fn": step}
 
 
 def bench_decode_gated_norm(torch, gdn, runs, status, steps, warmup):
@@ -959,6 +1034,8 @@ def run_gdn(args):
             dist.destroy_process_group()
         return 0
     e2e = None if args.no_e2e else bench_e2e(torch, gdn, pf["run"], args.steps, args.warmup)
+    variants = None if args.no_variants else bench_launch_variants(
+        torch, pf["run"], dec["step_fn"] if dec else None, args.steps, device)
 
     def max_ranks(v):
         return max_over_ranks(dist, world, v, device)
@@ -991,6 +1068,11 @@ def run_gdn(args):
         }
         if large:
             line["prefill_workloads"] = large
+        if variants:
+            if dec and variants.get("decode_cuda_graph_ms_per_step"):
+                variants["decode_cuda_graph_gbs"] = (
+                    dec["state_bytes"] / (variants["decode_cuda_graph_ms_per_step"] / 1e3) / 1e9)
+            line["launch_variants"] = variants
         if e2e:
             line["e2e"] = {"value": replica_throughput(world, T, max_ranks(e2e["ms"])),
                            "unit": "tokens/s", "ms_per_step": e2e["ms"],
