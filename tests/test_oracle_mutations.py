@@ -58,6 +58,21 @@ MUTATIONS = {
     "checkpoint_count": ("__init__.py", "n_b = max(0, -(-ln // every) - 1)", "n_b = max(0, ln // every)"),
     # snapshot copied the wrong way round
     "slot_copy_reversed": ("__init__.py", "st[d_] = st[s_]", "st[s_] = st[d_]"),
+    # decay rate from A_log itself instead of e^{A_log}
+    "A_log_not_exponentiated": ("const double A = exp((double)A_log[h]);",
+                                "const double A = (double)A_log[h];"),
+    # dt_bias left out of the softplus argument
+    "dt_bias_dropped": ("double z = (double)a[t * h_v + h] + (double)dt_bias[h];",
+                        "double z = (double)a[t * h_v + h];"),
+    # g with the wrong sign: growth instead of decay
+    "gate_sign": ("g[t] = -A * softplus(z);", "g[t] = A * softplus(z);"),
+    # beta taken as b itself, without the sigmoid
+    "beta_without_sigmoid": ("beta[t] = sigmoid((double)b[t * h_v + h]);",
+                             "beta[t] = (double)b[t * h_v + h];"),
+    # conv output used without the SiLU
+    "conv_without_silu": ("y[t * y_stride] = silu(acc);", "y[t * y_stride] = acc;"),
+    # keys left unnormalised
+    "key_not_normalised": ("l2_normalise_rows(T, d_k, l2_eps, 1.0, khat);", ";"),
 }
 
 
