@@ -349,7 +349,8 @@ def graph_replay_ms(torch, fn, steps, flush=None):
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        # thread-local: only this thread's calls are checked during the capture
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
             fn()
         torch.cuda.synchronize()
     except RuntimeError as e:
@@ -756,7 +757,7 @@ def bench_fp32_state(torch, gdn, inp, device, steps, warmup):
     return out
 
 
-def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64):
+def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=64, graph=True):
     runs = []
     for layer in range(layers):
         inp = workloads.decode_4b(layer, slots=slots)
@@ -798,7 +799,8 @@ def bench_decode(torch, gdn, workloads, device, steps, warmup, layers=24, slots=
     layer_ms = [s.elapsed_time(e) for s, e in one]
     # the same 24 calls captured once into a CUDA graph and replayed, as a
     # serving loop that captures its decode step launches them
-    graph_ms, graph_err = graph_replay_ms(torch, step, steps)
+    graph_ms, graph_err = (graph_replay_ms(torch, step, steps) if graph else
+                           (None, "not captured with more than one rank"))
     d = runs[0]["dims"]
     state_bytes = 2 * layers * slots * d.h_v * d.d_k * d.d_v * 4
     norm = bench_decode_gated_norm(torch, gdn, runs, status, steps, warmup)
@@ -1016,7 +1018,7 @@ def run_gdn(args):
     dec = None
     if not args.no_decode and not args.large_only:
         dec = bench_decode(torch, gdn, workloads, device, args.decode_steps or args.steps,
-                           args.warmup, layers=args.decode_layers)
+                           args.warmup, layers=args.decode_layers, graph=world == 1)
         barrier()
     clocks = sampler.stop()
     if pf is None:
@@ -1030,7 +1032,10 @@ def run_gdn(args):
             dist.destroy_process_group()
         return 0
     e2e = None if args.no_e2e else bench_e2e(torch, gdn, pf["run"], args.steps, args.warmup)
-    variants = None if args.no_variants else bench_launch_variants(torch, pf["run"], args.steps, device)
+    # CUDA-graph captures only in single-rank runs: a rank's process-group threads
+    # keep working during a capture
+    variants = None if args.no_variants or world > 1 else bench_launch_variants(
+        torch, pf["run"], args.steps, device)
 
     def max_ranks(v):
         return max_over_ranks(dist, world, v, device)
@@ -1147,7 +1152,7 @@ def run_gdn(args):
                 "metric": "decode state GB/s", "value": gbs, "unit": "GB/s",
                 "ms_per_step": step_ms, "steps": args.decode_steps or args.steps,
                 "launch": ("the 24 per-layer calls replayed from one CUDA graph" if graphed else
-                           "the 24 per-layer calls launched back to back (graph capture failed: "
+                           "the 24 per-layer calls launched back to back (no graph: "
                            f"{dec['graph_err']})"),
                 "plain_launches": {"value": plain_gbs, "ms_per_step": dms},
                 "config": {"workload": "decode step, 24 layers x 64 slots, one bf16 token per "
