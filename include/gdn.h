@@ -41,7 +41,10 @@
  * host during the call.  The library allocates no device memory, keeps no
  * mutable global state, never synchronises the stream and returns as soon as
  * the work is enqueued on `stream`.  Calls on different streams that touch
- * different slots may run concurrently.
+ * different slots may run concurrently.  Because a call only enqueues kernels
+ * on `stream`, it can be captured into a CUDA graph and replayed; a replay
+ * reuses the pointers, sizes and dimensions of the captured call (the first
+ * gdn_prefill_noalloc call on a device must come before any capture).
  *
  * Errors: a negative gdn_status is returned synchronously for anything the
  * host can check (null pointers, unsupported dimensions, misalignment, a
@@ -210,7 +213,9 @@ int gdn_gate_projection(const gdn_dims* dims, const void* hidden, const void* w_
                         int32_t d_model, int64_t n, void* a, void* b, int32_t* d_status,
                         gdn_stream_t stream);
 
-/* Bytes of device workspace gdn_prefill needs for this shape (0 on bad dims). */
+/* Bytes of device workspace gdn_prefill needs for this shape (0 on bad dims).
+ * Library plumbing, not an operation of the method: the workspace holds the
+ * per-chunk records between the state-independent stage and the scan. */
 size_t gdn_prefill_workspace_size(const gdn_dims* dims, int64_t total_tokens,
                                   int32_t num_seqs);
 
@@ -289,7 +294,8 @@ typedef struct {
 } gdn_trace;
 
 /* gdn_prefill with stage tracing; trace may be NULL (then identical to
- * gdn_prefill). */
+ * gdn_prefill).  Instrumentation for measuring the stages, not an operation
+ * of the method. */
 int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
                        const void* x, const void* a, const void* b,
                        const int32_t* cu_seqlens, int32_t num_seqs,
@@ -302,7 +308,7 @@ int gdn_prefill_traced(const gdn_dims* dims, const gdn_params* params,
 
 /*
  * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate device
- * memory (no counterpart in the paper: it is a deployment variant).  Code
+ * memory (a deployment variant; the pages define no such call).  Code
  * running inside a host framework whose allocator already owns nearly all of
  * HBM, or on a path where cudaMalloc's implicit synchronisation is not
  * acceptable, cannot obtain the workspace gdn_prefill wants.  This entry point
@@ -429,7 +435,8 @@ int gdn_decode_step_gated_norm(const gdn_dims* dims, const gdn_params* params,
                                const float* norm_weight, float eps, void* y,
                                int32_t* d_status, gdn_stream_t stream);
 
-/* Static description of a gdn_status code. */
+/* Static description of a gdn_status code (library plumbing).  The string is
+ * owned by the library and valid for the life of the process. */
 const char* gdn_status_str(int status);
 
 #ifdef __cplusplus
