@@ -865,10 +865,14 @@ def oracle_prefill_time(inp, n_threads):
 
 def prefill_dtype(d):
     """Arithmetic type of the prefill: the tensor-core path (Qwen3.5-4B layer
-    shape, bf16 I/O) multiplies bf16 operands with fp32 accumulation and an
-    fp32 state; every other shape runs fp32 SIMT arithmetic."""
-    tc = d.d_k == 128 and d.d_v == 128 and d.chunk == 64 and d.io == "bf16" and d.h_v == 2 * d.h_k
-    return "bf16" if tc else "f32"
+    shape, bf16 I/O) multiplies fp16 operands (bf16 with GDN_BF16_OPERANDS)
+    with fp32 accumulation and an fp32 state; every other shape, and
+    GDN_FP32_STATE, runs fp32 SIMT arithmetic."""
+    tc = (d.d_k == 128 and d.d_v == 128 and d.chunk == 64 and d.io == "bf16" and
+          d.h_v == 2 * d.h_k and not d.flags & 1)
+    if not tc:
+        return "f32"
+    return "bf16" if d.flags & 8 else "fp16"
 
 
 def config_of(inp):
@@ -877,6 +881,11 @@ def config_of(inp):
             "B": len(inp["lengths"]), "T": int(inp["x"].shape[0]), "h_k": d.h_k, "h_v": d.h_v,
             "d_k": d.d_k, "d_v": d.d_v, "conv_dim": d.conv_dim, "conv_w": d.conv_w,
             "chunk": d.chunk, "io": d.io, "state": "fp32, zero initial",
+            "arithmetic": {"fp16": "tensor-core products of fp16 operands (10-bit mantissa) "
+                                   "with fp32 accumulation; fp32 state, gates and norms",
+                           "bf16": "tensor-core products of bf16 operands with fp32 "
+                                   "accumulation; fp32 state, gates and norms",
+                           "f32": "fp32 SIMT arithmetic throughout"}[prefill_dtype(d)],
             "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
             "timing": "median of the K timed steps (CUDA events per step)",
             "parallelism": "replicas (no cross-GPU exchange in the layer)"}

@@ -82,3 +82,14 @@ def test_committed_records_name_their_summaries():
         assert rec["dram_bytes_per_launch"] > 0, key
         assert os.path.exists(os.path.join(ROOT, rec["summary"])), (key, rec["summary"])
         assert key.split(":")[0] in bench.KERNEL_SOURCES, key
+
+
+def test_line_dtype_names_the_arithmetic_of_the_path_taken():
+    import dataclasses
+    from gated_deltanet_linear_07_gb300 import _binding as b
+    from gated_deltanet_linear_07_gb300.workloads import TINY
+    assert bench.prefill_dtype(QWEN35_4B) == "fp16"      # tensor-core default: fp16 operands
+    assert bench.prefill_dtype(dataclasses.replace(QWEN35_4B, flags=b.GDN_BF16_OPERANDS)) == "bf16"
+    assert bench.prefill_dtype(dataclasses.replace(QWEN35_4B, flags=b.GDN_FP32_STATE)) == "f32"
+    assert bench.prefill_dtype(dataclasses.replace(QWEN35_4B, chunk=32)) == "f32"   # SIMT path
+    assert bench.prefill_dtype(TINY) == "f32"
