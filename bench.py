@@ -875,17 +875,19 @@ def prefill_dtype(d):
     return "bf16" if d.flags & 8 else "fp16"
 
 
+ARITHMETIC = {"fp16": "tensor-core products of fp16 operands (10-bit mantissa) with fp32 "
+                      "accumulation; fp32 state, gates and norms; bf16 I/O",
+              "bf16": "tensor-core products of bf16 operands with fp32 accumulation; fp32 "
+                      "state, gates and norms; bf16 I/O",
+              "f32": "fp32 SIMT arithmetic throughout"}
+
+
 def config_of(inp):
     d = inp["dims"]
     return {"workload": "Qwen3.5-4B-shaped Gated DeltaNet layer prefill",
             "B": len(inp["lengths"]), "T": int(inp["x"].shape[0]), "h_k": d.h_k, "h_v": d.h_v,
             "d_k": d.d_k, "d_v": d.d_v, "conv_dim": d.conv_dim, "conv_w": d.conv_w,
             "chunk": d.chunk, "io": d.io, "state": "fp32, zero initial",
-            "arithmetic": {"fp16": "tensor-core products of fp16 operands (10-bit mantissa) "
-                                   "with fp32 accumulation; fp32 state, gates and norms",
-                           "bf16": "tensor-core products of bf16 operands with fp32 "
-                                   "accumulation; fp32 state, gates and norms",
-                           "f32": "fp32 SIMT arithmetic throughout"}[prefill_dtype(d)],
             "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
             "timing": "median of the K timed steps (CUDA events per step)",
             "parallelism": "replicas (no cross-GPU exchange in the layer)"}
@@ -1069,7 +1071,8 @@ def run_gdn(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": prefill_dtype(inp["dims"]), "data": "synthetic", "config": config_of(inp),
+            "dtype": prefill_dtype(inp["dims"]), "arithmetic": ARITHMETIC[prefill_dtype(inp["dims"])],
+            "data": "synthetic", "config": config_of(inp),
             "roofline": roof,
             "tc_roofline_frac_whole_step": flops_launch / (ms / 1e3) / 1e12 / peak_tf,
             "stages_ms": stage, "stages_tflops": stage_tflops,
