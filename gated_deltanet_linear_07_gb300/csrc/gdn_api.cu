@@ -51,8 +51,12 @@ int check_prefill_dims(const gdn_dims* d) {
   return GDN_OK;
 }
 
-bool use_tc(const gdn_dims* d) {
-  return (d->flags & GDN_FP32_STATE) == 0 &&
+// The tensor-core path, for its shapes, when there are tokens.  A call whose
+// sequences are all empty has only states and windows to pass through (or to
+// zero): the SIMT path's check, window write-back and scan do exactly that
+// and build no tensor map over an x with no rows.
+bool use_tc(const gdn_dims* d, int64_t total_tokens) {
+  return total_tokens > 0 && (d->flags & GDN_FP32_STATE) == 0 &&
          gdn_tc_prefill_supported(d->h_k, d->h_v, d->d_k, d->d_v, d->chunk, d->io);
 }
 
@@ -70,7 +74,7 @@ PrefillLayout prefill_layout(const gdn_dims* d, int64_t T, int64_t B) {
   memset(&L, 0, sizeof(L));
   size_t o = 0;
   L.flag = o; o += align_up(16);
-  if (use_tc(d)) {
+  if (use_tc(d, T)) {
     L.max_chunks = (T + d->chunk - 1) / d->chunk + B;
     L.chunk_off = o; o += align_up((size_t)(B + 1) * sizeof(int32_t));
     L.ready = o; o += align_up((size_t)L.max_chunks * d->h_k * sizeof(int32_t));
@@ -252,7 +256,8 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
   p.ws_g = reinterpret_cast<float*>(ws + L.g);
   p.ws_beta = reinterpret_cast<float*>(ws + L.beta);
   cudaError_t e;
-  if (use_tc(dims)) {
+  const bool tc = use_tc(dims, total_tokens);
+  if (tc) {
     p.chunk_off = reinterpret_cast<int32_t*>(ws + L.chunk_off);
     p.chunk_ready = reinterpret_cast<int32_t*>(ws + L.ready);
     p.max_chunks = L.max_chunks;
@@ -276,7 +281,7 @@ static int prefill_impl(const gdn_dims* dims, const gdn_params* params, const vo
     e = gdn_launch_gated_rmsnorm(norm_weight, norm_eps, o, z, total_tokens * dims->h_v, dims->d_v,
                                  dims->io, o, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && check_finite)
-    e = check_stages(p, dims, use_tc(dims), reinterpret_cast<cudaStream_t>(stream));
+    e = check_stages(p, dims, tc, reinterpret_cast<cudaStream_t>(stream));
   return cuda_rc(e);
 }
 

@@ -77,6 +77,10 @@ def test_workspace_size_rules(lib):
     dfp = gdn.make_dims(**D4B, flags=gdn.GDN_FP32_STATE)
     assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) >= 4096 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
     assert gdn.gdn_prefill_workspace_size(dfp, 4096, 1) != w1
+    # a call whose sequences are all empty takes the SIMT path (states and
+    # windows pass through): no tensor-core chunk records
+    w0 = gdn.gdn_prefill_workspace_size(d, 0, 3)
+    assert 0 < w0 < 3 * (16 * 32768 + 32 * 41984)
     for bad_flags in (16, 32, -1):                 # unknown flag bits
         assert gdn.gdn_prefill_workspace_size(gdn.make_dims(**D4B, flags=bad_flags), 4096, 1) == 0
         assert _prefill(lib, gdn.make_dims(**D4B, flags=bad_flags)) == -1

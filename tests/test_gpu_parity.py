@@ -211,6 +211,18 @@ def test_prefill_with_empty_sequences_between(gpu_lib, name):
     check_prefill(inp, run.results(), oracle_prefill(inp, n_threads=NCPU))
 
 
+@pytest.mark.parametrize("name", ["qwen35_4b", "tiny"])
+def test_prefill_with_every_sequence_empty(gpu_lib, name):
+    """No tokens at all (x, a, b and o empty): each sequence's slot gets its
+    initial state and window back, or zeros without one; other slots stay bit
+    for bit."""
+    d = QWEN35_4B if name == "qwen35_4b" else TINY
+    inp = workloads.layer_inputs(d, [0, 0, 0], seed=77, init="mixed", num_slots=5)
+    run = PrefillRun(inp)
+    run()
+    check_prefill(inp, run.results(), oracle_prefill(inp))
+
+
 def test_device_status_bits(gpu_lib):
     d = TINY
     inp = workloads.layer_inputs(d, [5, 7], seed=2, init="random", num_slots=4)
